@@ -1,0 +1,173 @@
+"""CPU oracle for causal GQA attention with RoPE (forward and backward), float64.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only users.  The CUDA library never calls
+into this package and this package never imports the CUDA library.
+
+The arithmetic lives in ``ne_oracle.c`` (plain C, double precision, the full
+T x T score matrix).  This module compiles it on first use with the host C
+compiler and wraps it with ctypes.  What it computes, and where on the pages
+each step comes from, is stated in the header of ``ne_oracle.c``:
+
+* "NanoEuler: a GPT-2-scale LLM built from scratch in C and CUDA",
+  technical specification (RoPE on queries and keys; GQA; decoder-only) and
+  validation section (analytic gradients checked by central finite
+  differences in double precision);
+* "Rebuilding GPT-2 in one 100KB C/CUDA file (NanoEuler 116M walkthrough)",
+  section 3.4 (tiled FlashAttention with an online softmax, which is an exact
+  reorganisation of softmax attention, so the oracle is softmax attention).
+
+Every function is pinned by tests in ``tests/test_oracle.py`` against closed
+forms, invariants, finite differences and torch's CPU attention routine.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ne_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libne_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DP = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile ne_oracle.c into libne_oracle.so next to it (gcc, OpenMP, -O2)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    lib.ne_oracle_rope.restype = ctypes.c_int
+    lib.ne_oracle_rope.argtypes = [_DP, _DP] + [ctypes.c_int] * 4 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_fwd.restype = ctypes.c_int
+    lib.ne_oracle_fwd.argtypes = [_DP] * 5 + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_bwd.restype = ctypes.c_int
+    lib.ne_oracle_bwd.argtypes = [_DP] * 10 + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _c(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _p(x):
+    return None if x is None else x.ctypes.data_as(_DP)
+
+
+class Oracle:
+    """The oracle's entry points bound to one compiled copy of ne_oracle.c."""
+
+    def __init__(self, lib):
+        self._lib = lib
+
+    def max_threads(self) -> int:
+        return self._lib.ne_oracle_max_threads()
+
+    def rope(self, x, theta: float, pos_offset: int = 0, inverse: bool = False):
+        """Rotate-half RoPE of a [B, T, H, d] array: R(t + pos_offset) x, or R^T x if inverse."""
+        x = _c(x)
+        B, T, H, d = x.shape
+        y = np.empty_like(x)
+        rc = self._lib.ne_oracle_rope(_p(x), _p(y), B, T, H, d, float(theta), int(pos_offset),
+                                      int(inverse))
+        if rc:
+            raise ValueError(f"ne_oracle_rope rejected shape {x.shape}")
+        return y
+
+    def attn_fwd(self, q, k, v, theta: float, pos_offset: int = 0, threads: int = 0):
+        """Causal GQA attention with RoPE.  Returns (o [B,T,Hq,d], lse [B,Hq,T])."""
+        q, k, v = _c(q), _c(k), _c(v)
+        B, T, Hq, d = q.shape
+        Hkv = k.shape[2]
+        if k.shape != (B, T, Hkv, d) or v.shape != k.shape:
+            raise ValueError("k and v must be [B, T, Hkv, d] matching q")
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, T), dtype=np.float64)
+        rc = self._lib.ne_oracle_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, T, Hq, Hkv, d,
+                                     float(theta), int(pos_offset), int(threads))
+        if rc:
+            raise ValueError(f"ne_oracle_fwd failed with code {rc}")
+        return o, lse
+
+    def attn_bwd(self, q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0):
+        """Gradients of sum(O * dO): dict with dq, dk, dv and the oracle's o, lse, D."""
+        q, k, v, do = _c(q), _c(k), _c(v), _c(do)
+        B, T, Hq, d = q.shape
+        Hkv = k.shape[2]
+        if do.shape != q.shape or k.shape != (B, T, Hkv, d) or v.shape != k.shape:
+            raise ValueError("shape mismatch")
+        dq = np.empty_like(q)
+        dk = np.empty_like(k)
+        dv = np.empty_like(v)
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, T), dtype=np.float64)
+        D = np.empty((B, Hq, T), dtype=np.float64)
+        rc = self._lib.ne_oracle_bwd(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv),
+                                     _p(o), _p(lse), _p(D), B, T, Hq, Hkv, d, float(theta),
+                                     int(pos_offset), int(threads))
+        if rc:
+            raise ValueError(f"ne_oracle_bwd failed with code {rc}")
+        return {"dq": dq, "dk": dk, "dv": dv, "o": o, "lse": lse, "D": D}
+
+
+def compile_source(src_path: str, lib_path: str) -> str:
+    """Compile one copy of the oracle's C source into a shared library."""
+    tmp = lib_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src_path, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def load_from(lib_path: str) -> Oracle:
+    """Bind an Oracle to a specific compiled copy (tests use this for planted mistakes)."""
+    return Oracle(_bind(lib_path))
+
+
+def default() -> Oracle:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = Oracle(_bind(build()))
+    return _lib
+
+
+def max_threads() -> int:
+    return default().max_threads()
+
+
+def rope(x, theta: float, pos_offset: int = 0, inverse: bool = False):
+    return default().rope(x, theta, pos_offset, inverse)
+
+
+def attn_fwd(q, k, v, theta: float, pos_offset: int = 0, threads: int = 0):
+    return default().attn_fwd(q, k, v, theta, pos_offset, threads)
+
+
+def attn_bwd(q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0):
+    return default().attn_bwd(q, k, v, do, theta, pos_offset, threads)
+
+
+def group_slice(x: np.ndarray, b: int, j: int, heads_per_group: int):
+    """Slice one (batch b, kv head j) group out of a [B, T, H, d] array, H = Hq or Hkv.
+
+    Groups are independent in the definition (query head h only reads kv head
+    h // G), so the oracle on a group slice equals the same slice of the
+    oracle on the whole tensor.
+    """
+    return x[b:b + 1, :, j * heads_per_group:(j + 1) * heads_per_group, :]

@@ -1,0 +1,280 @@
+/*
+ * ne_oracle.c -- CPU oracle for causal grouped-query attention with rotary
+ * position embeddings (RoPE), forward and backward, in double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg are the only callers.  It shares no code with
+ * the CUDA library and must never be used as a fallback for it.
+ *
+ * What it computes (the plain definition, no tiling, no online softmax):
+ *
+ *   "NanoEuler: GPT-2 scale LLM in C and CUDA", technical specification:
+ *   RoPE is applied to the queries and keys; grouped-query attention shares a
+ *   smaller set of key/value heads among the query heads; the model is
+ *   decoder-only (causal).  "Building GPT-2 in a 100KB C/CUDA file" section
+ *   3.4: the FlashAttention kernel is tiled attention with an online softmax
+ *   that never stores the T x T matrix.  That is an exact reorganisation of
+ *   softmax attention, so the oracle is softmax attention itself, with the
+ *   T x T score matrix materialised.
+ *
+ *   RoPE (rotate-half pairing, positive angle, 0-based positions):
+ *     theta_i = theta^(-2i/d),  a = pos * theta_i,  i = 0 .. d/2-1
+ *     x'_i       = x_i cos a - x_{i+d/2} sin a
+ *     x'_{i+d/2} = x_{i+d/2} cos a + x_i sin a
+ *   GQA head map: query head h reads key/value head h / (Hq/Hkv).
+ *   S[t,s] = <q'[t,h], k'[s,kv(h)]> / sqrt(d) for s <= t, -inf otherwise.
+ *   P = row softmax of S;  lse[t] = ln sum_s exp S[t,s];  O[t] = sum_s P v[s].
+ *
+ *   Backward for the loss L = sum(O * dO):
+ *     dv[s]  = sum over heads of the group, sum_t P[t,s] dO[t]
+ *     dP     = dO v^T,  D[t] = <dO[t], O[t]>,  dS = P * (dP - D)
+ *     dq'[t] = sum_s dS[t,s] k'[s] / sqrt(d)
+ *     dk'[s] = sum over heads, sum_t dS[t,s] q'[t] / sqrt(d)
+ *     dq = R(t)^T dq',  dk = R(s)^T dk'    (rotation by -a)
+ *   The pages validate every analytic gradient against a central finite
+ *   difference in double precision ("Building GPT-2 ..." section 2.1); the
+ *   test suite applies that check to this file.
+ *
+ * Layout: q, o, dO, dq are [B][T][Hq][d]; k, v, dk, dv are [B][T][Hkv][d];
+ * lse and D are [B][Hq][T].  All arrays are contiguous float64.
+ * pos_offset shifts every position by a constant (a test hook for the
+ * relative-position property of RoPE); the library itself always uses 0.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define IDX(b, t, h, c, T, H, d) ((((size_t)(b) * (T) + (t)) * (H) + (h)) * (d) + (c))
+
+static void rope_row(const double *x, double *y, int d, double theta, long pos, int inverse)
+{
+    int half = d / 2;
+    for (int i = 0; i < half; ++i) {
+        double freq = pow(theta, -2.0 * (double)i / (double)d);
+        double a = (double)pos * freq;
+        double c = cos(a), s = sin(a);
+        if (inverse)
+            s = -s;
+        double x0 = x[i], x1 = x[i + half];
+        y[i] = x0 * c - x1 * s;
+        y[i + half] = x1 * c + x0 * s;
+    }
+}
+
+/* Rotate every row of a [B][T][H][d] array: y = R(pos) x (inverse: R(pos)^T x). */
+int ne_oracle_rope(const double *x, double *y, int B, int T, int H, int d, double theta,
+                   long pos_offset, int inverse)
+{
+    if (d <= 0 || d % 2)
+        return 1;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t)
+            for (int h = 0; h < H; ++h)
+                rope_row(x + IDX(b, t, h, 0, T, H, d), y + IDX(b, t, h, 0, T, H, d), d, theta,
+                         (long)t + pos_offset, inverse);
+    return 0;
+}
+
+static int check_shape(int B, int T, int Hq, int Hkv, int d)
+{
+    if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || d < 2 || d % 2 || Hq % Hkv)
+        return 1;
+    return 0;
+}
+
+/*
+ * Softmax probabilities of one (b, h): P is T x T, row-major, zero above the
+ * diagonal.  qr and kr are the rotated query / key rows of this head (T x d).
+ * Writes lse[t] (natural log) as well.
+ */
+static void probs(const double *qr, const double *kr, int T, int d, double *P, double *lse)
+{
+    double scale = 1.0 / sqrt((double)d);
+    for (int t = 0; t < T; ++t) {
+        double *S = P + (size_t)t * T;
+        for (int s = 0; s < T; ++s) {
+            if (s > t) {
+                S[s] = -INFINITY;
+                continue;
+            }
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += qr[(size_t)t * d + c] * kr[(size_t)s * d + c];
+            S[s] = acc * scale;
+        }
+        double mx = -INFINITY;
+        for (int s = 0; s <= t; ++s)
+            if (S[s] > mx)
+                mx = S[s];
+        double sum = 0.0;
+        for (int s = 0; s <= t; ++s)
+            sum += exp(S[s] - mx);
+        double l = mx + log(sum);
+        lse[t] = l;
+        for (int s = 0; s < T; ++s)
+            S[s] = (s <= t) ? exp(S[s] - l) : 0.0;
+    }
+}
+
+static void gather_rotated(const double *x, double *xr, int b, int h, int T, int H, int d,
+                           double theta, long pos_offset)
+{
+    for (int t = 0; t < T; ++t)
+        rope_row(x + IDX(b, t, h, 0, T, H, d), xr + (size_t)t * d, d, theta,
+                 (long)t + pos_offset, 0);
+}
+
+int ne_oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
+                  int B, int T, int Hq, int Hkv, int d, double theta, long pos_offset,
+                  int nthreads)
+{
+    if (check_shape(B, T, Hq, Hkv, d))
+        return 1;
+    int G = Hq / Hkv;
+    int nbh = B * Hq;
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+    for (int bh = 0; bh < nbh; ++bh) {
+        int b = bh / Hq, h = bh % Hq, j = h / G;
+        double *qr = malloc(sizeof(double) * (size_t)T * d);
+        double *kr = malloc(sizeof(double) * (size_t)T * d);
+        double *P = malloc(sizeof(double) * (size_t)T * T);
+        if (!qr || !kr || !P) {
+            err = 2;
+        } else {
+            gather_rotated(q, qr, b, h, T, Hq, d, theta, pos_offset);
+            gather_rotated(k, kr, b, j, T, Hkv, d, theta, pos_offset);
+            probs(qr, kr, T, d, P, lse + ((size_t)b * Hq + h) * T);
+            for (int t = 0; t < T; ++t) {
+                double *orow = o + IDX(b, t, h, 0, T, Hq, d);
+                for (int c = 0; c < d; ++c)
+                    orow[c] = 0.0;
+                for (int s = 0; s <= t; ++s) {
+                    double p = P[(size_t)t * T + s];
+                    const double *vrow = v + IDX(b, s, j, 0, T, Hkv, d);
+                    for (int c = 0; c < d; ++c)
+                        orow[c] += p * vrow[c];
+                }
+            }
+        }
+        free(qr);
+        free(kr);
+        free(P);
+    }
+    return err;
+}
+
+/*
+ * Backward.  Writes dq, dk, dv; optionally (non-NULL) o, lse and D as the
+ * oracle computes them.  Parallel over (b, kv head) groups so that dk and dv
+ * are summed over the group's query heads without races.
+ */
+int ne_oracle_bwd(const double *q, const double *k, const double *v, const double *dO,
+                  double *dq, double *dk, double *dv, double *o_out, double *lse_out,
+                  double *D_out, int B, int T, int Hq, int Hkv, int d, double theta,
+                  long pos_offset, int nthreads)
+{
+    if (check_shape(B, T, Hq, Hkv, d))
+        return 1;
+    int G = Hq / Hkv;
+    int ngroups = B * Hkv;
+    double scale = 1.0 / sqrt((double)d);
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+    for (int bj = 0; bj < ngroups; ++bj) {
+        int b = bj / Hkv, j = bj % Hkv;
+        size_t Td = (size_t)T * d;
+        double *qr = malloc(sizeof(double) * Td);
+        double *kr = malloc(sizeof(double) * Td);
+        double *dqr = malloc(sizeof(double) * Td);
+        double *dkr = calloc(Td, sizeof(double));
+        double *orow = malloc(sizeof(double) * d);
+        double *lse = malloc(sizeof(double) * T);
+        double *Dv = malloc(sizeof(double) * T);
+        double *P = malloc(sizeof(double) * (size_t)T * T);
+        if (!qr || !kr || !dqr || !dkr || !orow || !lse || !Dv || !P) {
+            err = 2;
+            goto done;
+        }
+        gather_rotated(k, kr, b, j, T, Hkv, d, theta, pos_offset);
+        for (int s = 0; s < T; ++s)
+            memset(dv + IDX(b, s, j, 0, T, Hkv, d), 0, sizeof(double) * d);
+        for (int h = j * G; h < (j + 1) * G; ++h) {
+            gather_rotated(q, qr, b, h, T, Hq, d, theta, pos_offset);
+            probs(qr, kr, T, d, P, lse);
+            memset(dqr, 0, sizeof(double) * Td);
+            for (int t = 0; t < T; ++t) {
+                const double *dorow = dO + IDX(b, t, h, 0, T, Hq, d);
+                /* O[t] and D[t] = <dO[t], O[t]> */
+                for (int c = 0; c < d; ++c)
+                    orow[c] = 0.0;
+                for (int s = 0; s <= t; ++s) {
+                    double p = P[(size_t)t * T + s];
+                    const double *vrow = v + IDX(b, s, j, 0, T, Hkv, d);
+                    for (int c = 0; c < d; ++c)
+                        orow[c] += p * vrow[c];
+                }
+                double Dt = 0.0;
+                for (int c = 0; c < d; ++c)
+                    Dt += dorow[c] * orow[c];
+                Dv[t] = Dt;
+                if (o_out)
+                    memcpy(o_out + IDX(b, t, h, 0, T, Hq, d), orow, sizeof(double) * d);
+                for (int s = 0; s <= t; ++s) {
+                    double p = P[(size_t)t * T + s];
+                    const double *vrow = v + IDX(b, s, j, 0, T, Hkv, d);
+                    double *dvrow = dv + IDX(b, s, j, 0, T, Hkv, d);
+                    double dp = 0.0;
+                    for (int c = 0; c < d; ++c)
+                        dp += dorow[c] * vrow[c];
+                    double ds = p * (dp - Dt);
+                    for (int c = 0; c < d; ++c) {
+                        dvrow[c] += p * dorow[c];
+                        dqr[(size_t)t * d + c] += scale * ds * kr[(size_t)s * d + c];
+                        dkr[(size_t)s * d + c] += scale * ds * qr[(size_t)t * d + c];
+                    }
+                }
+            }
+            for (int t = 0; t < T; ++t)
+                rope_row(dqr + (size_t)t * d, dq + IDX(b, t, h, 0, T, Hq, d), d, theta,
+                         (long)t + pos_offset, 1);
+            if (lse_out)
+                memcpy(lse_out + ((size_t)b * Hq + h) * T, lse, sizeof(double) * T);
+            if (D_out)
+                memcpy(D_out + ((size_t)b * Hq + h) * T, Dv, sizeof(double) * T);
+        }
+        for (int s = 0; s < T; ++s)
+            rope_row(dkr + (size_t)s * d, dk + IDX(b, s, j, 0, T, Hkv, d), d, theta,
+                     (long)s + pos_offset, 1);
+    done:
+        free(qr);
+        free(kr);
+        free(dqr);
+        free(dkr);
+        free(orow);
+        free(lse);
+        free(Dv);
+        free(P);
+    }
+    return err;
+}
+
+int ne_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
