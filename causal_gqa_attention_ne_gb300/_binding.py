@@ -1,0 +1,187 @@
+"""ctypes binding of libne_attn.so with the same entry-point names as the C ABI.
+
+Argument marshalling only: shape/dtype/device checks that keep the raw
+pointers in bounds, then one call into the library.  Streams are torch's
+current CUDA stream unless one is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+NE_STATUS = {
+    0: "NE_OK", 1: "NE_ERR_NULL", 2: "NE_ERR_SHAPE", 3: "NE_ERR_UNSUPPORTED", 4: "NE_ERR_ALIGN",
+    5: "NE_ERR_WORKSPACE", 6: "NE_ERR_CUDA", 7: "NE_ERR_TIMEOUT", 8: "NE_ERR_RANGE",
+    9: "NE_ERR_ARG",
+}
+
+EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn_get_error",
+            "ne_attn_status_string", "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NeAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {NE_STATUS.get(status, status)} "
+                         f"({_status_text(status)})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load libne_attn.so (building it first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            if not build_if_missing:
+                raise RuntimeError(f"{_build.LIB} is missing; run causal_gqa_attention_ne_gb300"
+                                   "._build.build() (needs nvcc)")
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.ne_attn_fwd.argtypes = [vp] * 5 + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd.restype = i
+        lib.ne_attn_bwd.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd.restype = i
+        lib.ne_attn_bwd_workspace_size.argtypes = [i] * 5
+        lib.ne_attn_bwd_workspace_size.restype = sz
+        lib.ne_attn_get_error.argtypes = [vp]
+        lib.ne_attn_get_error.restype = i
+        lib.ne_attn_status_string.argtypes = [i]
+        lib.ne_attn_status_string.restype = ctypes.c_char_p
+        lib.ne_attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.ne_attn_set_wait_limit_ns.restype = None
+        lib.ne_attn_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.ne_attn_selftest_timeout.restype = i
+        _lib = lib
+        return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load_library(build_if_missing=False).ne_attn_status_string(status).decode()
+    except Exception:  # the library may be the thing that failed to load
+        return "see ne_attn.h"
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(x: torch.Tensor, name: str, shape, dtype) -> None:
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if x.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(x.shape)}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, T, H, d]")
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    return B, T, Hq, Hkv, d
+
+
+def ne_attn_fwd(q, k, v, o, lse, rope_theta: float = 10000.0, stream=None) -> None:
+    """Forward into caller-allocated o [B,T,Hq,d] bf16 and lse [B,Hq,T] fp32."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (B, T, Hq, d), bf)
+    _check(k, "k", (B, T, Hkv, d), bf)
+    _check(v, "v", (B, T, Hkv, d), bf)
+    _check(o, "o", (B, T, Hq, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    rc = load_library().ne_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), B, T, Hq, Hkv, d, float(rope_theta),
+                                    _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd")
+
+
+def ne_attn_bwd_workspace_size(B: int, T: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(load_library().ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
+
+
+def ne_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, rope_theta: float = 10000.0,
+                stream=None) -> None:
+    """Backward into caller-allocated dq, dk, dv; workspace is a uint8 CUDA tensor."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load_library().ne_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), workspace.data_ptr(), wbytes, B, T, Hq, Hkv,
+                                    d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd")
+
+
+def ne_attn_get_error(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device-side status code."""
+    return int(load_library().ne_attn_get_error(_stream_ptr(stream)))
+
+
+def ne_attn_status_string(status: int) -> str:
+    return load_library().ne_attn_status_string(int(status)).decode()
+
+
+def ne_attn_set_wait_limit_ns(limit_ns: int) -> None:
+    load_library().ne_attn_set_wait_limit_ns(int(limit_ns))
+
+
+def ne_attn_selftest_timeout(limit_ns: int, stream=None) -> None:
+    rc = load_library().ne_attn_selftest_timeout(int(limit_ns), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_selftest_timeout")
+
+
+# ---- conveniences that allocate outputs with torch (device memory only) ----
+
+def attention_forward(q, k, v, rope_theta: float = 10000.0, stream=None):
+    """Allocate o and lse on q's device and run ne_attn_fwd.  Returns (o, lse)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+    ne_attn_fwd(q, k, v, o, lse, rope_theta, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, do, rope_theta: float = 10000.0, stream=None,
+                       workspace=None):
+    """Allocate dq, dk, dv (and a workspace if none is given) and run ne_attn_bwd."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d),
+                                dtype=torch.uint8, device=q.device)
+    ne_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, rope_theta, stream)
+    return dq, dk, dv

@@ -1,0 +1,333 @@
+// ne_api.cu -- the C ABI of include/ne_attn.h: argument validation, TMA
+// descriptor construction, launch sequencing and the device status word.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ne_attn.h"
+#include "ne_common.cuh"
+#include "ne_kernels.h"
+
+namespace {
+
+// One status word per device (module-scope device variable): bounded waits
+// that run out and fp16 range overflows are OR-ed into it by the kernels.
+__device__ uint32_t g_status_word;
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    uint32_t *status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+EncodeTiledFn encode_fn()
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+// Returns NE_OK and the device's status-word address, or an error status.
+int device_state(uint32_t **status)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return NE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return NE_ERR_CUDA;
+        s.supported = (major == 10 && minor == 3);
+        if (s.supported) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess)
+                return NE_ERR_CUDA;
+            s.status = static_cast<uint32_t *>(p);
+        }
+        s.probed = true;
+    }
+    if (!s.supported)
+        return NE_ERR_UNSUPPORTED;
+    *status = s.status;
+    return NE_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_shape(int B, int T, int Hq, int Hkv, int d, float theta)
+{
+    if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+        return NE_ERR_SHAPE;
+    if (d != 32 && d != 64 && d != 128)
+        return NE_ERR_UNSUPPORTED;
+    if (!(theta > 0.f) || !std::isfinite(theta))
+        return NE_ERR_ARG;
+    // Grid sizes and 32-bit row positions must not overflow.
+    const long long M = (T + 127) / 128;
+    if (T > (1 << 24) || M * B * Hq > 0x7fffffffLL)
+        return NE_ERR_SHAPE;
+    return NE_OK;
+}
+
+// 4-D TMA descriptor over a contiguous [B][T][H][d] 16-bit tensor; box is
+// (one swizzle span of columns, 1 head, 128 rows, 1 batch).
+int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return NE_ERR_CUDA;
+    const int swb = (2 * d < 128) ? 2 * d : 128;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                             static_cast<cuuint64_t>(T) * H * d * 2};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(swb / 2), 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// Fixed-point RoPE frequencies: round(2^32 * theta^(-2i/d) / (2 pi)) mod 2^32.
+void fill_rope(ne::RopeFreqs &fr, int d, float theta)
+{
+    std::memset(&fr, 0, sizeof(fr));
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < d / 2; ++i) {
+        double f = std::pow(static_cast<double>(theta), -2.0 * i / d) / two_pi;
+        f -= std::floor(f);
+        const unsigned long long v =
+            static_cast<unsigned long long>(std::llround(f * 4294967296.0));
+        fr.turn[i] = static_cast<uint32_t>(v & 0xffffffffull);
+    }
+}
+
+ne::AttnParams base_params(int B, int T, int Hq, int Hkv, int d, float theta, uint32_t *status)
+{
+    ne::AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = B;
+    p.T = T;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.M = (T + 127) / 128;
+    p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.status = status;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    fill_rope(p.rope, d, theta);
+    return p;
+}
+
+int largest_divisor_at_most(int G, int cap)
+{
+    for (int g = cap; g >= 1; --g)
+        if (G % g == 0)
+            return g;
+    return 1;
+}
+
+__global__ void timeout_selftest_kernel(uint32_t *status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        ne::mbar_init(ne::smem_u32(&bar), 1);
+        ne::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const ne::WaitCtl wc{&abort_flag, status, limit_ns};
+        // Nothing ever arrives on `bar`: this wait can only end by its limit.
+        ne::mbar_wait(ne::smem_u32(&bar), 0, wc);
+    }
+}
+
+} // namespace
+
+namespace ne {
+
+int fwd_heads_per_cta(int d, int G) { return largest_divisor_at_most(G, d == 128 ? 2 : 4); }
+int dq_heads_per_cta(int d, int G) { return d == 128 ? 1 : largest_divisor_at_most(G, 4); }
+
+cudaError_t launch_timeout_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream)
+{
+    timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+} // namespace ne
+
+extern "C" {
+
+int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int T,
+                int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    if (!q || !k || !v || !o || !lse)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
+    if (rc != NE_OK)
+        return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, rope_theta, status);
+    p.GC = ne::fwd_heads_per_cta(d, p.G);
+    p.nchunks = p.G / p.GC;
+    p.out0 = o;
+    p.lse = lse;
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
+        make_map(&mv, v, B, T, Hkv, d))
+        return NE_ERR_CUDA;
+    cudaError_t e = ne::launch_fwd(d, mq, mk, mv, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
+{
+    if (check_shape(B, T, Hq, Hkv, d, 1.0f) != NE_OK)
+        return 0;
+    const size_t bytes = static_cast<size_t>(B) * Hq * T * sizeof(float);
+    return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, float rope_theta,
+                void *stream)
+{
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
+    if (rc != NE_OK)
+        return rc;
+    if (!workspace || workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
+        !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, rope_theta, status);
+    p.o_in = o;
+    p.do_in = dO;
+    p.lse = const_cast<float *>(lse);
+    p.Dws = static_cast<float *>(workspace);
+    CUtensorMap mq, mk, mv, mdo;
+    if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
+        make_map(&mv, v, B, T, Hkv, d) || make_map(&mdo, dO, B, T, Hq, d))
+        return NE_ERR_CUDA;
+    cudaError_t e = ne::launch_bwd_pre(d, p, st);
+    if (e != cudaSuccess)
+        return NE_ERR_CUDA;
+    ne::AttnParams pq = p;
+    pq.GC = ne::dq_heads_per_cta(d, p.G);
+    pq.nchunks = p.G / pq.GC;
+    pq.out0 = dq;
+    e = ne::launch_bwd_dq(d, mq, mk, mv, mdo, pq, st);
+    if (e != cudaSuccess)
+        return NE_ERR_CUDA;
+    ne::AttnParams pk = p;
+    pk.out0 = dk;
+    pk.out1 = dv;
+    e = ne::launch_bwd_dkdv(d, mq, mk, mv, mdo, pk, st);
+    return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+int ne_attn_get_error(void *stream)
+{
+    uint32_t *status = nullptr;
+    int rc = device_state(&status);
+    if (rc != NE_OK)
+        return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return NE_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess)
+        return NE_ERR_CUDA;
+    if (word) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+            return NE_ERR_CUDA;
+    }
+    if (word & ne::kDevTimeout)
+        return NE_ERR_TIMEOUT;
+    if (word & ne::kDevRange)
+        return NE_ERR_RANGE;
+    return NE_OK;
+}
+
+const char *ne_attn_status_string(int status)
+{
+    switch (status) {
+    case NE_OK: return "ok";
+    case NE_ERR_NULL: return "a required pointer is NULL";
+    case NE_ERR_SHAPE: return "invalid shape (B, T, Hq, Hkv) or Hq % Hkv != 0";
+    case NE_ERR_UNSUPPORTED: return "unsupported head dim or device (needs d in {32,64,128}, sm_103)";
+    case NE_ERR_ALIGN: return "pointer misaligned (tensors need 16 bytes, lse 4 bytes)";
+    case NE_ERR_WORKSPACE: return "workspace missing or too small";
+    case NE_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case NE_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    case NE_ERR_RANGE: return "an fp16 tensor-core operand exceeded 65504";
+    case NE_ERR_ARG: return "invalid argument (rope_theta must be finite and > 0)";
+    default: return "unknown status";
+    }
+}
+
+void ne_attn_set_wait_limit_ns(uint64_t limit_ns)
+{
+    g_wait_limit_ns.store(limit_ns ? limit_ns : 1);
+}
+
+int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream)
+{
+    uint32_t *status = nullptr;
+    int rc = device_state(&status);
+    if (rc != NE_OK)
+        return rc;
+    cudaError_t e = ne::launch_timeout_selftest(status, limit_ns ? limit_ns : 1,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // extern "C"

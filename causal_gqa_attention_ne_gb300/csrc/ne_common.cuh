@@ -1,0 +1,174 @@
+// ne_common.cuh -- tile geometry, RoPE helpers and launch parameters shared by
+// the forward and backward attention kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+
+namespace ne {
+
+constexpr int kRows = 128;          // query rows and key rows per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kFp16Max = 65504.0f;
+
+// Kernels that allocate all 512 TMEM columns request at least this much
+// dynamic shared memory, so two of their CTAs never share an SM (the second
+// would otherwise stall in tcgen05.alloc until the first exits).
+constexpr int kOneCtaPerSmSmem = 116 * 1024;
+constexpr int smem_one_cta(int bytes) { return bytes > kOneCtaPerSmSmem ? bytes : kOneCtaPerSmSmem; }
+
+// Geometry of one 128-row tile of head dimension D in shared memory, exactly
+// as TMA lands it: the D columns are split into NB column blocks of SWB bytes
+// per row (SWB = 128 for D >= 64, 64 for D = 32); each block is 128 rows of
+// SWB bytes with the matching TMA/UMMA swizzle (128-byte or 64-byte).
+template <int D>
+struct Tile {
+    static constexpr int SWB = (2 * D < 128) ? 2 * D : 128;
+    static constexpr int NB = 2 * D / SWB;
+    static constexpr int BLOCK = kRows * SWB;        // bytes per column block
+    static constexpr int BYTES = kRows * 2 * D;      // bytes per tile
+    static constexpr uint32_t LAYOUT = (SWB == 128) ? 2u : 4u;
+    static constexpr int BOX_COLS = SWB / 2;         // TMA box width in elements
+    static constexpr int NPV = (D < 64) ? D : 64;    // N of one MN-major MMA (one swizzle atom)
+};
+
+// Physical byte offset of logical byte `lin` of a swizzled block whose rows
+// are `swb` bytes: 16-byte chunk bits [4,6|7) are XOR-ed with address bits
+// [7,9|10).
+template <int SWB>
+__device__ __forceinline__ uint32_t swz(uint32_t lin)
+{
+    constexpr uint32_t mask = (SWB == 128) ? 7u : 3u;
+    return lin ^ (((lin >> 7) & mask) << 4);
+}
+
+// Byte offset of the 16-byte chunk holding elements [8c, 8c+8) of row r of a
+// D-wide tile.
+template <int D>
+__device__ __forceinline__ uint32_t tile_chunk(int r, int c)
+{
+    using TL = Tile<D>;
+    constexpr int CPB = TL::SWB / 16;   // chunks per block row
+    return (c / CPB) * TL::BLOCK + swz<TL::SWB>(r * TL::SWB + (c % CPB) * 16);
+}
+
+// Byte offset of chunk c (8 keys) of row r of a 128x128 16-bit tile (P, dS):
+// two column blocks of 64 elements, 128-byte swizzle.
+__device__ __forceinline__ uint32_t ptile_chunk(int r, int c)
+{
+    return (c >> 3) * (kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// K-major operand descriptor of a D-wide tile for K step kk (16 elements).
+template <int D>
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_addr, int kk)
+{
+    using TL = Tile<D>;
+    const int byte = kk * 32;
+    return smem_desc(tile_addr + (byte / TL::SWB) * TL::BLOCK + (byte % TL::SWB), 16,
+                     8 * TL::SWB, TL::LAYOUT);
+}
+
+// K-major descriptor of a 128x128 16-bit tile (P or dS) for K step kk.
+__device__ __forceinline__ uint64_t desc_ptile(uint32_t tile_addr, int kk)
+{
+    return smem_desc(tile_addr + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024, 2u);
+}
+
+// MN-major descriptor of a D-wide tile used as the B operand with N = the
+// tile's columns and K = its rows: N chunk nc (one swizzle atom, NPV
+// columns), K step kk (16 rows).  The operand never spans two atoms along N,
+// so only the K-direction stride between 8-row groups matters; it is written
+// into both offset fields.
+template <int D>
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_addr, int nc, int kk)
+{
+    using TL = Tile<D>;
+    return smem_desc(tile_addr + nc * TL::BLOCK + kk * 16 * TL::SWB, 8 * TL::SWB, 8 * TL::SWB,
+                     TL::LAYOUT);
+}
+
+// RoPE angles.  Frequency i is passed as a 32-bit fixed-point number of turns
+// per position, F_i = round(2^32 * theta^(-2i/d) / (2 pi)).  The angle of
+// position p is then p * F_i modulo 2^32 turns (exact integer wrap-around),
+// mapped to [-pi, pi) before the hardware sine/cosine.
+struct RopeFreqs {
+    uint32_t turn[64];
+};
+
+__device__ __forceinline__ void rope_sincos(uint32_t pos, uint32_t f, float &s, float &c)
+{
+    const int32_t t = static_cast<int32_t>(pos * f);
+    const float ang = static_cast<float>(t) * 1.4629180792671596e-09f;   // 2 pi / 2^32
+    __sincosf(ang, &s, &c);
+}
+
+// Rotate row r of a bf16 tile in place, writing fp16 (the score-side operand
+// type).  x'_i = x_i cos - x_{i+D/2} sin, x'_{i+D/2} = x_{i+D/2} cos + x_i sin.
+// Returns the largest |x'| seen (for the fp16 range check).
+template <int D>
+__device__ __forceinline__ float rope_row_to_f16(uint8_t *tile, int r, uint32_t pos,
+                                                 const RopeFreqs &fr)
+{
+    constexpr int HC = D / 16;   // chunks in the first half of the row
+    float mx = 0.f;
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        uint4 *pa = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c));
+        uint4 *pb = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c + HC));
+        const uint4 a = *pa, b = *pb;
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+        uint32_t ao[4], bo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float s0, c0, s1, c1;
+            rope_sincos(pos, fr.turn[8 * c + 2 * e], s0, c0);
+            rope_sincos(pos, fr.turn[8 * c + 2 * e + 1], s1, c1);
+            const float x0 = bf16_lo(av[e]), x1 = bf16_hi(av[e]);
+            const float y0 = bf16_lo(bv[e]), y1 = bf16_hi(bv[e]);
+            const float u0 = x0 * c0 - y0 * s0, w0 = y0 * c0 + x0 * s0;
+            const float u1 = x1 * c1 - y1 * s1, w1 = y1 * c1 + x1 * s1;
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(u0), fabsf(w0)), fmaxf(fabsf(u1), fabsf(w1))));
+            ao[e] = pack_f16x2(u0, u1);
+            bo[e] = pack_f16x2(w0, w1);
+        }
+        *pa = make_uint4(ao[0], ao[1], ao[2], ao[3]);
+        *pb = make_uint4(bo[0], bo[1], bo[2], bo[3]);
+    }
+    return mx;
+}
+
+// Inverse rotation (by -angle) of a pair of fp32 values held in registers.
+__device__ __forceinline__ void rope_inverse_pair(float &x, float &y, uint32_t pos, uint32_t f)
+{
+    float s, c;
+    rope_sincos(pos, f, s, c);
+    const float u = x * c + y * s;
+    const float w = y * c - x * s;
+    x = u;
+    y = w;
+}
+
+// Launch parameters (everything except the TMA descriptors).
+struct AttnParams {
+    int B, T, Hq, Hkv, G, M;     // M = number of 128-row tiles along T
+    int GC, nchunks;             // query heads per CTA, CTAs per KV group (Q-major kernels)
+    float scale_log2;            // log2(e) / sqrt(d)
+    float scale;                 // 1 / sqrt(d)
+    const void *o_in;            // backward: forward output O (preprocess)
+    const void *do_in;           // backward: dO (preprocess)
+    void *out0;                  // forward: O; backward: dq / dk
+    void *out1;                  // backward: dv
+    float *lse;                  // forward: written; backward: read
+    float *Dws;                  // backward: D = rowsum(dO * O), [B][Hq][T]
+    uint32_t *status;            // device status word
+    uint64_t wait_limit_ns;
+    RopeFreqs rope;
+};
+
+} // namespace ne

@@ -1,0 +1,35 @@
+// ne_kernels.h -- internal launchers of the attention kernels (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ne_common.cuh"
+
+namespace ne {
+
+// Forward: grid = M * B * Hkv * nchunks CTAs of 320 threads.
+cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                       const AttnParams &p, cudaStream_t stream);
+
+// Backward preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c].
+cudaError_t launch_bwd_pre(int d, const AttnParams &p, cudaStream_t stream);
+
+// Backward dQ (query-tile major, recomputes S and dP).
+cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                          const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream);
+
+// Backward dK, dV (key-tile major; dK and dV summed over the query heads of
+// each KV head inside the CTA).
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,
+                            const CUtensorMap &v, const CUtensorMap &dO, const AttnParams &p,
+                            cudaStream_t stream);
+
+// Heads per CTA the Q-major kernels support for head dim d and group size G.
+int fwd_heads_per_cta(int d, int G);
+int dq_heads_per_cta(int d, int G);
+
+// One-block kernel whose wait can never complete (checks the timeout path).
+cudaError_t launch_timeout_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream);
+
+} // namespace ne

@@ -1,0 +1,133 @@
+/*
+ * ne_attn.h -- C ABI of the GB300 (sm_103a) causal grouped-query attention
+ * library with rotary position embeddings: forward and backward.
+ *
+ * What is computed.  The attention of a NanoEuler-style decoder block
+ * ("NanoEuler: a GPT-2-scale LLM built from scratch in C and CUDA",
+ * technical specification: RoPE applied to queries and keys, grouped-query
+ * attention sharing a smaller set of key/value heads, decoder-only; the
+ * "CUDA engine" section: a hand-written FlashAttention kernel that tiles the
+ * computation and uses an online softmax so the T x T matrix is never stored).
+ * With G = Hq / Hkv and kv(h) = floor(h / G):
+ *
+ *   q'[t,h]  = R(t) q[t,h],  k'[s,j] = R(s) k[s,j]        (rotate-half RoPE:
+ *              pairs (i, i + d/2) rotated by angle pos * theta^(-2i/d))
+ *   S[t,s]   = <q'[t,h], k'[s,kv(h)]> / sqrt(d)  for s <= t (causal)
+ *   lse[t]   = ln sum_{s<=t} exp S[t,s]
+ *   O[t,h]   = sum_{s<=t} exp(S[t,s] - lse[t]) v[s,kv(h)]
+ *
+ * and the backward of L = sum(O * dO) with respect to the pre-RoPE q, k and
+ * v; dk and dv are summed over the G query heads sharing each key/value head.
+ *
+ * Layouts (all row-major, contiguous, no padding):
+ *   q, o, dO, dq : bf16 [B][T][Hq][d]
+ *   k, v, dk, dv : bf16 [B][T][Hkv][d]
+ *   lse          : fp32 [B][Hq][T]     natural-log logsumexp of the scaled scores
+ *
+ * Ownership.  The caller allocates and owns every buffer (device memory for
+ * tensors; the library allocates no memory).  Outputs are overwritten, never
+ * accumulated into.  Calls are asynchronous on `stream` (a cudaStream_t
+ * passed as void*, NULL = the legacy default stream); the caller keeps
+ * buffers alive until the stream has passed the call.  The library is
+ * reentrant; its only global state is one device status word per GPU that
+ * records device-side errors (read and cleared by ne_attn_get_error).
+ *
+ * Preconditions: B, T >= 1; Hq, Hkv >= 1 and Hq % Hkv == 0; d in {32, 64,
+ * 128}; rope_theta > 0 and finite; every pointer 16-byte aligned; the current
+ * device is an sm_103 GPU.  Score-side operands (the rotated q and k, and the
+ * backward's dS) go through the tensor cores as fp16, so elements of q and k,
+ * and of dS = P (dP - D), must stay below 65504 in magnitude; a kernel that
+ * sees a larger value records NE_ERR_RANGE in the status word.
+ *
+ * Errors.  Argument errors are returned synchronously and launch nothing.
+ * Launch failures return NE_ERR_CUDA.  Device-side errors (a bounded wait
+ * that ran out, a value out of fp16 range) are recorded in the device
+ * status word and reported by ne_attn_get_error.  Nothing aborts, prints or
+ * throws across this interface, and there is no CPU fallback.
+ */
+#ifndef NE_ATTN_H
+#define NE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NE_OK = 0,
+    NE_ERR_NULL = 1,        /* a required pointer is NULL */
+    NE_ERR_SHAPE = 2,       /* B, T, Hq, Hkv out of range or Hq % Hkv != 0 */
+    NE_ERR_UNSUPPORTED = 3, /* d not in {32, 64, 128}, or the device is not sm_103 */
+    NE_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    NE_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than ne_attn_bwd_workspace_size */
+    NE_ERR_CUDA = 6,        /* a CUDA runtime / driver call or a launch failed */
+    NE_ERR_TIMEOUT = 7,     /* a device-side bounded wait ran out (reported by get_error) */
+    NE_ERR_RANGE = 8,       /* an fp16 tensor-core operand overflowed (reported by get_error) */
+    NE_ERR_ARG = 9          /* another invalid argument (rope_theta <= 0, NaN, ...) */
+} ne_status;
+
+/*
+ * Forward.  Reads q, k, v; writes o and lse.
+ * Section "CUDA engine / kernel implementation" of the NanoEuler README page
+ * (tiled FlashAttention with online softmax); RoPE and GQA from its
+ * technical specification.
+ */
+int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+
+/*
+ * Bytes of device workspace ne_attn_bwd needs for this shape (the per-row
+ * dO.O dot products D, fp32 [B][Hq][T], rounded up to 256 bytes).
+ * Returns 0 for a shape ne_attn_bwd would reject.
+ */
+size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
+
+/*
+ * Backward of L = sum(O * dO).  Reads q, k, v, o, lse (as written by
+ * ne_attn_fwd for the same inputs) and dO; writes dq, dk, dv (gradients with
+ * respect to the pre-RoPE q and k, and v).  `workspace` is caller-owned
+ * device memory of at least ne_attn_bwd_workspace_size(...) bytes; its
+ * contents on entry do not matter.  Deterministic: no floating-point atomics,
+ * so repeated calls on the same inputs give bitwise-equal results.
+ * The pages validate the hand-written backward by central finite differences
+ * in double precision (NanoEuler walkthrough, section 2.1).
+ */
+int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                float rope_theta, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status of
+ * the current device: NE_ERR_TIMEOUT or NE_ERR_RANGE if a kernel recorded
+ * one since the last call, NE_ERR_CUDA if the stream reports a CUDA error,
+ * else NE_OK.
+ */
+int ne_attn_get_error(void *stream);
+
+/* Static, human-readable text for a status code. */
+const char *ne_attn_status_string(int status);
+
+/*
+ * Upper bound, in nanoseconds, on every device-side wait of later launches
+ * (default 2e9).  A wait that runs out makes its kernel record NE_ERR_TIMEOUT,
+ * drain its own in-flight work and return.  Not thread-safe against
+ * concurrent launches from other host threads.
+ */
+void ne_attn_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Check of the bounded-wait machinery: launches one block whose wait can
+ * never be satisfied (a barrier nothing arrives on) under a wait limit of
+ * `limit_ns`.  The launch itself returns NE_OK; a following
+ * ne_attn_get_error(stream) must then report NE_ERR_TIMEOUT.
+ */
+int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NE_ATTN_H */
