@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Benchmark of causal GQA + RoPE attention, forward + backward, on GB300.
+
+Workload: the attention of one full training step of the NanoEuler 116M model
+("NanoEuler: a GPT-2-scale LLM built from scratch in C and CUDA", model
+configuration table: dim 768, 12/4 heads, 16 layers, context 512), batch 64:
+16 independent layers, each B=64 T=512 Hq=12 Hkv=4 d=64, forward then
+backward on one stream, every layer with its own buffers (4.3 GB in all, so
+each layer's inputs are cold in the 129 MB L2).  Synthetic seeded N(0, 1)
+inputs (see ne_inputs.py).
+
+A step = 16 x (ne_attn_fwd, then the three backward steps) through the C ABI.
+The step is captured in a CUDA graph so Python call overhead does not leave
+the GPU idle; CUDA events inside the graph time every kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle (the only reference this
+subject has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import ne_inputs  # noqa: E402
+
+W = ne_inputs.STEP_116M
+METRIC = "causal GQA attn fwd+bwd TFLOP/s and tokens/s at T=512 12/4 heads; % BF16 peak"
+UNIT = "TFLOP/s"
+CONFIG = {
+    "workload": W.name,
+    "layers": W.layers, "B": W.B, "T": W.T, "Hq": W.Hq, "Hkv": W.Hkv, "d": W.d,
+    "causal": True, "rope_theta": W.theta,
+    "l2": "inputs larger than L2: 16 layers x 270 MB of separate buffers",
+}
+FLOP_PER_LAYER = W.flops_fwd() + W.flops_bwd()
+FLOP_PER_STEP = FLOP_PER_LAYER * W.layers
+TOKENS_PER_STEP = W.tokens()          # B*T tokens go through all 16 layers per step
+
+
+# ------------------------------------------------------------ roofline ---
+
+def _mb(n_elem, bytes_per):
+    return n_elem * bytes_per
+
+
+def kernel_work(w=W):
+    """Algorithmic flops and compulsory HBM bytes of ONE launch of each kernel
+    for one layer (per-unit figures x the units one launch processes)."""
+    B, T, Hq, Hkv, d = w.B, w.T, w.Hq, w.Hkv, w.d
+    pairs = w.pairs * B * Hq                       # causal (t, s) pairs x heads
+    q = B * T * Hq * d * 2
+    kv = B * T * Hkv * d * 2
+    row = B * Hq * T * 4                           # lse or D
+    return {
+        # QK^T and PV: 2 GEMMs of 2d flops per pair; reads Q K V, writes O lse
+        "fwd": {"flops": 4.0 * d * pairs, "bytes": q + 2 * kv + q + row},
+        # D = rowsum(dO * O): reads O and dO, writes D
+        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 2 * q + row},
+        # dQ = dS K' (one GEMM; the S and dP recompute is not algorithmic work)
+        "bwd_dq": {"flops": 2.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + q},
+        # S, dP, dV, dK (four GEMMs); reads Q K V dO lse D, writes dK dV
+        "bwd_dkdv": {"flops": 8.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + 2 * kv},
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "causal_gqa_attention_ne_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_gpt116m_step.txt")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"csrc_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or m.group(1) != csrc_hash():
+        return None
+    m = re.search(rf"^{kernel}\s+([0-9.eE+]+)\s*$", text, re.M)
+    return float(m.group(1)) if m else None
+
+
+# -------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, start: bool):
+        if start:
+            self.t_start = time.time()
+        else:
+            self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        win = [l for (t, l) in self.lines if self.t_start and self.t_start - 0.06 <= t <= (
+            self.t_end or t) + 0.06]
+        if len(win) < 3:
+            win = [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in win:
+            parts = [p.strip() for p in l.split(",")]
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+# ---------------------------------------------------------- our arm ---
+
+def make_event(torch, external):
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            pass
+    return torch.cuda.Event(enable_timing=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import causal_gqa_attention_ne_gb300 as ne
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ne.load_library()
+
+    layers = []
+    for layer in range(W.layers):
+        x = ne_inputs.make_inputs(W, layer)
+        host = {n: t.pin_memory() for n, t in x.items()}
+        d = {n: t.to(dev) for n, t in x.items()}
+        d["o"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(W.B, W.Hq, W.T, dtype=torch.float32, device=dev)
+        d["dq"] = torch.empty_like(d["q"])
+        d["dk"] = torch.empty_like(d["k"])
+        d["dv"] = torch.empty_like(d["v"])
+        d["ws"] = torch.empty(ne.ne_attn_bwd_workspace_size(W.B, W.T, W.Hq, W.Hkv, W.d),
+                              dtype=torch.uint8, device=dev)
+        out_host = {n: torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True)
+                    for n in ("o", "lse", "dq", "dk", "dv")}
+        layers.append((host, d, out_host))
+    theta = W.theta
+    names = ("fwd", "bwd_pre", "bwd_dq", "bwd_dkdv")
+
+    def step(evs=None):
+        for li, (_, d, _) in enumerate(layers):
+            if evs is not None:
+                evs[li][0].record()
+            ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], theta)
+            if evs is not None:
+                evs[li][1].record()
+            ne.ne_attn_bwd_preprocess(d["o"], d["do"], d["ws"])
+            if evs is not None:
+                evs[li][2].record()
+            ne.ne_attn_bwd_dq(d["q"], d["k"], d["v"], d["lse"], d["do"], d["dq"], d["ws"], theta)
+            if evs is not None:
+                evs[li][3].record()
+            ne.ne_attn_bwd_dkdv(d["q"], d["k"], d["v"], d["lse"], d["do"], d["dk"], d["dv"],
+                                d["ws"], theta)
+            if evs is not None:
+                evs[li][4].record()
+
+    # eager warm-up call (sets kernel attributes, checks status)
+    step()
+    torch.cuda.synchronize()
+    st = ne.ne_attn_get_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)} after warm-up")
+
+    # one CUDA graph per timed step, each with its own timing events
+    K, Wm = args.steps, args.warmup
+    graphs, events = [], []
+    cap_stream = torch.cuda.Stream()
+    external_ok = True
+    for k in range(K):
+        evs = [[make_event(torch, external_ok) for _ in range(5)] for _ in range(W.layers)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            step(evs)
+        graphs.append(g)
+        events.append(evs)
+    torch.cuda.synchronize()
+
+    warm = max(Wm, 1)
+    for i in range(warm):
+        graphs[i % K].replay()
+    for g in graphs[warm:]:                # every graph replayed once before timing
+        g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    t0.record()
+    for g in graphs:
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    st = ne.ne_attn_get_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)} after timed region")
+
+    # per-kernel durations from the in-graph events
+    per = {n: [] for n in names}
+    for evs in events:
+        for le in evs:
+            for i, n in enumerate(names):
+                per[n].append(le[i].elapsed_time(le[i + 1]))
+    avg_ms = {n: statistics.mean(v) for n, v in per.items()}
+
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    ms_per_step = elapsed_ms / K
+    value = world * FLOP_PER_STEP * K / (elapsed_ms * 1e-3) / 1e12
+    tokens_per_s = world * TOKENS_PER_STEP * K / (elapsed_ms * 1e-3)
+
+    # end to end: host buffers in, host buffers out, through the eager C-ABI calls
+    e2e_steps = max(1, min(args.e2e_steps, K))
+    h2d = sum(sum(t.numel() * t.element_size() for t in host.values()) for host, _, _ in layers)
+    d2h = sum(sum(t.numel() * t.element_size() for t in oh.values()) for _, _, oh in layers)
+    s = torch.cuda.current_stream()
+    for rep in range(e2e_steps + 1):          # first pass warms the copy path
+        if rep == 1:
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            h0 = time.perf_counter()
+        for host, d, oh in layers:
+            for n in ("q", "k", "v", "do"):
+                d[n].copy_(host[n], non_blocking=True)
+            ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], theta)
+            ne.ne_attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"],
+                           d["dv"], d["ws"], theta)
+            for n in ("o", "lse", "dq", "dk", "dv"):
+                oh[n].copy_(d[n], non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    host_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps
+    e2e_ms = max(e2e_ms, host_ms)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    st = ne.ne_attn_get_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)} after e2e")
+
+    # roofline of the dominant kernel (largest share of the step)
+    peaks = load_peaks()
+    work = kernel_work()
+    dom = max(names, key=lambda n: avg_ms[n])
+    wk = work[dom]
+    t_tensor = wk["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = wk["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    dur_s = avg_ms[dom] * 1e-3
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": wk["flops"] / dur_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": wk["bytes"] / dur_s / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = measured_traffic(dom)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peaks['source']} (burst: kernels timed inside a short step)"
+    roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
+
+    kernels = {n: {"avg_us": avg_ms[n] * 1e3, "launches": len(per[n]),
+                   "share": avg_ms[n] / sum(avg_ms.values()),
+                   "tflops": work[n]["flops"] / (avg_ms[n] * 1e-3) / 1e12,
+                   "gbs": work[n]["bytes"] / (avg_ms[n] * 1e-3) / 1e9} for n in names}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "operand_dtypes": {"qk_scores_and_dS": "fp16", "p_v_dO": "bf16", "accumulate": "fp32"},
+        "data": "synthetic (seeded N(0,1), see ne_inputs.py)",
+        "config": CONFIG,
+        "tokens_per_s": tokens_per_s,
+        "pct_bf16_peak": value / (peaks["bf16_tflops"] * world) * 100.0,
+        "e2e": {"value": world * FLOP_PER_STEP / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 4 * W.layers * K,
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": sampler.summary(),
+    }
+    return result
+
+
+# --------------------------------------------------------- CPU oracle ---
+
+def oracle_sample(batch_rows: int, threads: int = 0, layer: int = 0):
+    """Time the float64 oracle (fwd + bwd) on the first `batch_rows` rows of one layer."""
+    import oracle
+    x = ne_inputs.make_inputs(W, layer)
+    q, k, v, do = (ne_inputs.as_f64(x[n][:batch_rows]) for n in ("q", "k", "v", "do"))
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, W.theta, threads=threads)
+    oracle.attn_bwd(q, k, v, do, W.theta, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = FLOP_PER_LAYER * batch_rows / W.B
+    used = threads if threads > 0 else oracle.max_threads()
+    return flops / dt / 1e12, dt, used
+
+
+def cpu_baseline(n_layers: int):
+    """The oracle on the first `n_layers` full layers of the workload (fwd + bwd)."""
+    total, used = 0.0, 1
+    for layer in range(n_layers):
+        _, dt, used = oracle_sample(W.B, layer=layer)
+        total += dt
+    val = FLOP_PER_LAYER * n_layers / total / 1e12
+    return {"value": val, "unit": UNIT, "cores": used, "kind": "oracle", "seconds": total,
+            "sample": f"layers 0-{n_layers - 1} of the {W.layers} of {W.name} (all {W.B} batch "
+                      f"rows), fwd + bwd in float64 (OpenMP over heads / kv groups)"}
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle, timed on the host cores."""
+    rows = args.ref_batch_rows
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    times = []
+    used = 1
+    for _ in range(args.steps):
+        _, dt, used = oracle_sample(rows)
+        times.append(dt)
+    flops = FLOP_PER_LAYER * rows / W.B
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = (f"each step: layer 0 of {W.name}, first {rows} of {W.B} batch rows, "
+              f"fwd + bwd in float64")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), see ne_inputs.py)", "config": CONFIG,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-layers", type=int, default=6,
+                    help="full layers of the workload the CPU-baseline oracle sample covers")
+    ap.add_argument("--ref-batch-rows", type=int, default=4,
+                    help="batch rows per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    # CPU baseline first (before any CUDA work; the oracle uses OpenMP threads)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_layers)
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        result["cpu_baseline"] = cpu
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -20,8 +20,9 @@ NE_STATUS = {
     9: "NE_ERR_ARG",
 }
 
-EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn_get_error",
-            "ne_attn_status_string", "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout")
+EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn_bwd_preprocess",
+            "ne_attn_bwd_dq", "ne_attn_bwd_dkdv", "ne_attn_get_error", "ne_attn_status_string",
+            "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +56,12 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_fwd.restype = i
         lib.ne_attn_bwd.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd.restype = i
+        lib.ne_attn_bwd_preprocess.argtypes = [vp] * 3 + [sz] + [i] * 5 + [vp]
+        lib.ne_attn_bwd_preprocess.restype = i
+        lib.ne_attn_bwd_dq.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_dq.restype = i
+        lib.ne_attn_bwd_dkdv.argtypes = [vp] * 8 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_dkdv.restype = i
         lib.ne_attn_bwd_workspace_size.argtypes = [i] * 5
         lib.ne_attn_bwd_workspace_size.restype = sz
         lib.ne_attn_get_error.argtypes = [vp]
@@ -143,6 +150,55 @@ def ne_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, rope_theta: float = 
                                     d, float(rope_theta), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd")
+
+
+def _bwd_common(q, k, v, lse, do, workspace):
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (do, "do", Hq)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return B, T, Hq, Hkv, d, workspace.numel() * workspace.element_size()
+
+
+def ne_attn_bwd_preprocess(o, do, workspace, stream=None) -> None:
+    """D = rowsum(dO * O) into the workspace (first backward step)."""
+    B, T, Hq, d = o.shape
+    _check(o, "o", (B, T, Hq, d), torch.bfloat16)
+    _check(do, "do", (B, T, Hq, d), torch.bfloat16)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load_library().ne_attn_bwd_preprocess(o.data_ptr(), do.data_ptr(), workspace.data_ptr(),
+                                               wbytes, B, T, Hq, Hq, d, _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_preprocess")
+
+
+def ne_attn_bwd_dq(q, k, v, lse, do, dq, workspace, rope_theta: float = 10000.0,
+                   stream=None) -> None:
+    B, T, Hq, Hkv, d, wbytes = _bwd_common(q, k, v, lse, do, workspace)
+    _check(dq, "dq", (B, T, Hq, d), torch.bfloat16)
+    rc = load_library().ne_attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(),
+                                       do.data_ptr(), dq.data_ptr(), workspace.data_ptr(), wbytes,
+                                       B, T, Hq, Hkv, d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_dq")
+
+
+def ne_attn_bwd_dkdv(q, k, v, lse, do, dk, dv, workspace, rope_theta: float = 10000.0,
+                     stream=None) -> None:
+    B, T, Hq, Hkv, d, wbytes = _bwd_common(q, k, v, lse, do, workspace)
+    _check(dk, "dk", (B, T, Hkv, d), torch.bfloat16)
+    _check(dv, "dv", (B, T, Hkv, d), torch.bfloat16)
+    rc = load_library().ne_attn_bwd_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                         lse.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                         dv.data_ptr(), workspace.data_ptr(), wbytes, B, T, Hq,
+                                         Hkv, d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_dkdv")
 
 
 def ne_attn_get_error(stream=None) -> int:

@@ -228,50 +228,145 @@ size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
     return (bytes + 255) & ~static_cast<size_t>(255);
 }
 
-int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                const void *dO, void *dq, void *dk, void *dv, void *workspace,
-                size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, float rope_theta,
-                void *stream)
+} // extern "C"
+
+namespace {
+
+// Validation shared by the backward entry points; fills the common params.
+int bwd_setup(const void *q, const void *k, const void *v, const float *lse, const void *dO,
+              void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+              float rope_theta, ne::AttnParams *p, CUtensorMap *mq, CUtensorMap *mk,
+              CUtensorMap *mv, CUtensorMap *mdo)
 {
-    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
+    if (!q || !k || !v || !lse || !dO)
         return NE_ERR_NULL;
     int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
     if (!workspace || workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
         return NE_ERR_WORKSPACE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse) ||
         !aligned16(workspace))
         return NE_ERR_ALIGN;
     uint32_t *status = nullptr;
     if ((rc = device_state(&status)) != NE_OK)
         return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, rope_theta, status);
+    *p = base_params(B, T, Hq, Hkv, d, rope_theta, status);
+    p->do_in = dO;
+    p->lse = const_cast<float *>(lse);
+    p->Dws = static_cast<float *>(workspace);
+    if (make_map(mq, q, B, T, Hq, d) || make_map(mk, k, B, T, Hkv, d) ||
+        make_map(mv, v, B, T, Hkv, d) || make_map(mdo, dO, B, T, Hq, d))
+        return NE_ERR_CUDA;
+    return NE_OK;
+}
+
+int run_dq(int d, const ne::AttnParams &base, void *dq, const CUtensorMap &mq,
+           const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdo, cudaStream_t st)
+{
+    ne::AttnParams p = base;
+    p.GC = ne::dq_heads_per_cta(d, p.G);
+    p.nchunks = p.G / p.GC;
+    p.out0 = dq;
+    return ne::launch_bwd_dq(d, mq, mk, mv, mdo, p, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+int run_dkdv(int d, const ne::AttnParams &base, void *dk, void *dv, const CUtensorMap &mq,
+             const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdo,
+             cudaStream_t st)
+{
+    ne::AttnParams p = base;
+    p.out0 = dk;
+    p.out1 = dv;
+    return ne::launch_bwd_dkdv(d, mq, mk, mv, mdo, p, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+int ne_attn_bwd_preprocess(const void *o, const void *dO, void *workspace,
+                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                           void *stream)
+{
+    if (!o || !dO)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, 1.0f);
+    if (rc != NE_OK)
+        return rc;
+    if (!workspace || workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, 1.0f, status);
     p.o_in = o;
     p.do_in = dO;
-    p.lse = const_cast<float *>(lse);
     p.Dws = static_cast<float *>(workspace);
+    return ne::launch_bwd_pre(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? NE_OK
+               : NE_ERR_CUDA;
+}
+
+int ne_attn_bwd_dq(const void *q, const void *k, const void *v, const float *lse,
+                   const void *dO, void *dq, const void *workspace, size_t workspace_bytes,
+                   int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    if (!dq)
+        return NE_ERR_NULL;
+    if (!aligned16(dq))
+        return NE_ERR_ALIGN;
+    ne::AttnParams p;
     CUtensorMap mq, mk, mv, mdo;
-    if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
-        make_map(&mv, v, B, T, Hkv, d) || make_map(&mdo, dO, B, T, Hq, d))
+    int rc = bwd_setup(q, k, v, lse, dO, const_cast<void *>(workspace), workspace_bytes, B, T,
+                       Hq, Hkv, d, rope_theta, &p, &mq, &mk, &mv, &mdo);
+    if (rc != NE_OK)
+        return rc;
+    return run_dq(d, p, dq, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream));
+}
+
+int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *lse,
+                     const void *dO, void *dk, void *dv, const void *workspace,
+                     size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                     float rope_theta, void *stream)
+{
+    if (!dk || !dv)
+        return NE_ERR_NULL;
+    if (!aligned16(dk) || !aligned16(dv))
+        return NE_ERR_ALIGN;
+    ne::AttnParams p;
+    CUtensorMap mq, mk, mv, mdo;
+    int rc = bwd_setup(q, k, v, lse, dO, const_cast<void *>(workspace), workspace_bytes, B, T,
+                       Hq, Hkv, d, rope_theta, &p, &mq, &mk, &mv, &mdo);
+    if (rc != NE_OK)
+        return rc;
+    return run_dkdv(d, p, dk, dv, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream));
+}
+
+int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, float rope_theta,
+                void *stream)
+{
+    if (!o || !dq || !dk || !dv)
+        return NE_ERR_NULL;
+    if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return NE_ERR_ALIGN;
+    ne::AttnParams p;
+    CUtensorMap mq, mk, mv, mdo;
+    int rc = bwd_setup(q, k, v, lse, dO, workspace, workspace_bytes, B, T, Hq, Hkv, d,
+                       rope_theta, &p, &mq, &mk, &mv, &mdo);
+    if (rc != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.o_in = o;
+    if (ne::launch_bwd_pre(d, p, st) != cudaSuccess)
         return NE_ERR_CUDA;
-    cudaError_t e = ne::launch_bwd_pre(d, p, st);
-    if (e != cudaSuccess)
-        return NE_ERR_CUDA;
-    ne::AttnParams pq = p;
-    pq.GC = ne::dq_heads_per_cta(d, p.G);
-    pq.nchunks = p.G / pq.GC;
-    pq.out0 = dq;
-    e = ne::launch_bwd_dq(d, mq, mk, mv, mdo, pq, st);
-    if (e != cudaSuccess)
-        return NE_ERR_CUDA;
-    ne::AttnParams pk = p;
-    pk.out0 = dk;
-    pk.out1 = dv;
-    e = ne::launch_bwd_dkdv(d, mq, mk, mv, mdo, pk, st);
-    return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+    if ((rc = run_dq(d, p, dq, mq, mk, mv, mdo, st)) != NE_OK)
+        return rc;
+    return run_dkdv(d, p, dk, dv, mq, mk, mv, mdo, st);
 }
 
 int ne_attn_get_error(void *stream)

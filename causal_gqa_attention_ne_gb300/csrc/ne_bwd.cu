@@ -777,8 +777,8 @@ static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const
 {
     using C = DqCfg<D, GC, ST>;
     auto kern = dq_kernel<D, GC, ST>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    static bool attr_done[64] = {};   // one flag set per template instantiation
+    cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
         return e;
     const unsigned grid = static_cast<unsigned>(p.M) * p.B * p.Hkv * p.nchunks;
@@ -823,8 +823,8 @@ static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, con
 {
     using C = DkvCfg<D, ST>;
     auto kern = dkdv_kernel<D, ST>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    static bool attr_done[64] = {};   // one flag set per template instantiation
+    cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
         return e;
     const unsigned grid = static_cast<unsigned>(p.M) * p.B * p.Hkv;

@@ -154,6 +154,24 @@ __device__ __forceinline__ void rope_inverse_pair(float &x, float &y, uint32_t p
     y = w;
 }
 
+// Raises a kernel's dynamic shared-memory limit once per device (not on
+// every launch, so launches stay cheap and capturable in CUDA graphs).
+// `done` must be a flag array owned by exactly one kernel instantiation.
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel kern, int bytes, bool (&done)[64])
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && done[dev])
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        done[dev] = true;
+    return e;
+}
+
 // Launch parameters (everything except the TMA descriptors).
 struct AttnParams {
     int B, T, Hq, Hkv, G, M;     // M = number of 128-row tiles along T

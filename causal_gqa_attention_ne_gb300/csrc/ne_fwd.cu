@@ -391,8 +391,8 @@ static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, cons
 {
     using C = FwdCfg<D, GC, ST, NP>;
     auto kern = fwd_kernel<D, GC, ST, NP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    static bool attr_done[64] = {};   // one flag set per template instantiation
+    cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
         return e;
     const unsigned grid = static_cast<unsigned>(p.M) * p.B * p.Hkv * p.nchunks;

@@ -32,9 +32,9 @@
  * reentrant; its only global state is one device status word per GPU that
  * records device-side errors (read and cleared by ne_attn_get_error).
  *
- * Preconditions: B, T >= 1; Hq, Hkv >= 1 and Hq % Hkv == 0; d in {32, 64,
- * 128}; rope_theta > 0 and finite; every pointer 16-byte aligned; the current
- * device is an sm_103 GPU.  Score-side operands (the rotated q and k, and the
+ * Preconditions: B, T >= 1 (T <= 2^24); Hq, Hkv >= 1 and Hq % Hkv == 0; d in
+ * {32, 64, 128}; rope_theta > 0 and finite; tensor and workspace pointers
+ * 16-byte aligned, lse 4-byte aligned; the current device is an sm_103 GPU.  Score-side operands (the rotated q and k, and the
  * backward's dS) go through the tensor cores as fp16, so elements of q and k,
  * and of dS = P (dP - D), must stay below 65504 in magnitude; a kernel that
  * sees a larger value records NE_ERR_RANGE in the status word.
@@ -98,6 +98,31 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
                 const void *dO, void *dq, void *dk, void *dv, void *workspace,
                 size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
                 float rope_theta, void *stream);
+
+/*
+ * The three steps ne_attn_bwd runs, in this order, exposed so a caller can
+ * time them or run the two independent steps (dq, and dk/dv) on two streams
+ * once the preprocess has finished.  Arguments mean what they mean for
+ * ne_attn_bwd; `workspace` carries D from the preprocess to the other two.
+ *
+ * ne_attn_bwd_preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c] in fp32
+ *   (the row dot product the backward of a softmax needs), written into the
+ *   workspace.
+ * ne_attn_bwd_dq: dq from q, k, v, lse, dO and D (query-tile major: recomputes
+ *   the scores and dP = dO v^T per key tile; dq = R(t)^T sum_s dS k' / sqrt(d)).
+ * ne_attn_bwd_dkdv: dk and dv from the same inputs (key-tile major: dk and dv
+ *   summed over the query heads of each key/value head inside one CTA).
+ */
+int ne_attn_bwd_preprocess(const void *o, const void *dO, void *workspace,
+                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                           void *stream);
+int ne_attn_bwd_dq(const void *q, const void *k, const void *v, const float *lse,
+                   const void *dO, void *dq, const void *workspace, size_t workspace_bytes,
+                   int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *lse,
+                     const void *dO, void *dk, void *dv, const void *workspace,
+                     size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                     float rope_theta, void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status of

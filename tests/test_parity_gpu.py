@@ -141,3 +141,23 @@ def test_rejects_bad_arguments_on_device():
     assert lib.ne_attn_bwd(*(y.data_ptr(),) * 9, y.data_ptr(), 0, 1, 1, 1, 1, 32, 10000.0,
                            None) == 5
     assert ne.ne_attn_get_error() == 0
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_substeps_match_full_backward(d):
+    """preprocess -> dq -> dkdv through their own entry points equals ne_attn_bwd
+    bitwise, also when kernels of other head dims ran in between."""
+    import causal_gqa_attention_ne_gb300 as ne
+    B, T, Hq, Hkv = 2, 300, 6, 2
+    xd = to_dev(ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=40 + d))
+    o, lse = ne.attention_forward(xd["q"], xd["k"], xd["v"], THETA)
+    dq, dk, dv = ne.attention_backward(xd["q"], xd["k"], xd["v"], o, lse, xd["do"], THETA)
+    ws = torch.empty(ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8,
+                     device="cuda")
+    dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    ne.ne_attn_bwd_preprocess(o, xd["do"], ws)
+    ne.ne_attn_bwd_dkdv(xd["q"], xd["k"], xd["v"], lse, xd["do"], dk2, dv2, ws, THETA)
+    ne.ne_attn_bwd_dq(xd["q"], xd["k"], xd["v"], lse, xd["do"], dq2, ws, THETA)
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 0
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
