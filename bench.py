@@ -385,6 +385,22 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def run_one_layer_for_profiler():
+    """One layer (B64 T512 12/4 d64, 270 MB of buffers), fwd then bwd, twice.
+    The first pass warms up; a profiler captures the second (-s 4 -c 4)."""
+    import torch
+
+    import causal_gqa_attention_ne_gb300 as ne
+    x = {n: t.cuda() for n, t in ne_inputs.make_inputs(W, 0).items()}
+    for _ in range(2):
+        o, lse = ne.attention_forward(x["q"], x["k"], x["v"], W.theta)
+        ne.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], W.theta)
+    torch.cuda.synchronize()
+    st = ne.ne_attn_get_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)}")
+
+
 # --------------------------------------------------------- CPU oracle ---
 
 def oracle_sample(batch_rows: int, threads: int = 0, layer: int = 0):
@@ -452,7 +468,13 @@ def main():
     ap.add_argument("--ref-batch-rows", type=int, default=4,
                     help="batch rows per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-layer", action="store_true",
+                    help="profiler mode: run one layer of the workload (fwd, then the three "
+                         "backward steps) twice, eagerly, and exit; no timing, no JSON")
     args = ap.parse_args()
+    if args.ncu_layer:
+        run_one_layer_for_profiler()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
