@@ -68,11 +68,12 @@ def kernel_work(w=W):
     return {
         # QK^T and PV: 2 GEMMs of 2d flops per pair; reads Q K V, writes O lse
         "fwd": {"flops": 4.0 * d * pairs, "bytes": q + 2 * kv + q + row},
-        # D = rowsum(dO * O): reads O and dO, writes D
-        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 2 * q + row},
+        # D = rowsum(dO * O), Q' = R(t) q, K' = R(s) k: reads O, dO, q, k;
+        # writes D and fp16 Q', K'
+        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 4 * q + row + 2 * kv},
         # dQ = dS K' (one GEMM; the S and dP recompute is not algorithmic work)
         "bwd_dq": {"flops": 2.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + q},
-        # S, dP, dV, dK (four GEMMs); reads Q K V dO lse D, writes dK dV
+        # S, dP, dV, dK (four GEMMs); reads Q' K' (fp16) V dO lse D, writes dK dV
         "bwd_dkdv": {"flops": 8.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + 2 * kv},
     }
 
@@ -226,7 +227,7 @@ def run_ours(args, rank, world, local_rank):
             ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], theta)
             if evs is not None:
                 evs[li][1].record()
-            ne.ne_attn_bwd_preprocess(d["o"], d["do"], d["ws"])
+            ne.ne_attn_bwd_preprocess(d["q"], d["k"], d["o"], d["do"], d["ws"], theta)
             if evs is not None:
                 evs[li][2].record()
             ne.ne_attn_bwd_dq(d["q"], d["k"], d["v"], d["lse"], d["do"], d["dq"], d["ws"], theta)

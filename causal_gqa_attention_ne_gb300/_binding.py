@@ -56,7 +56,7 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_fwd.restype = i
         lib.ne_attn_bwd.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd.restype = i
-        lib.ne_attn_bwd_preprocess.argtypes = [vp] * 3 + [sz] + [i] * 5 + [vp]
+        lib.ne_attn_bwd_preprocess.argtypes = [vp] * 5 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd_preprocess.restype = i
         lib.ne_attn_bwd_dq.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd_dq.restype = i
@@ -163,16 +163,19 @@ def _bwd_common(q, k, v, lse, do, workspace):
     return B, T, Hq, Hkv, d, workspace.numel() * workspace.element_size()
 
 
-def ne_attn_bwd_preprocess(o, do, workspace, stream=None) -> None:
-    """D = rowsum(dO * O) into the workspace (first backward step)."""
-    B, T, Hq, d = o.shape
-    _check(o, "o", (B, T, Hq, d), torch.bfloat16)
-    _check(do, "do", (B, T, Hq, d), torch.bfloat16)
+def ne_attn_bwd_preprocess(q, k, o, do, workspace, rope_theta: float = 10000.0,
+                           stream=None) -> None:
+    """D = rowsum(dO * O) and the rotated fp16 Q', K' into the workspace (first
+    backward step)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (o, "o", Hq), (do, "do", Hq)):
+        _check(x, n, (B, T, h, d), torch.bfloat16)
     if workspace.device.type != "cuda" or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
     wbytes = workspace.numel() * workspace.element_size()
-    rc = load_library().ne_attn_bwd_preprocess(o.data_ptr(), do.data_ptr(), workspace.data_ptr(),
-                                               wbytes, B, T, Hq, Hq, d, _stream_ptr(stream))
+    rc = load_library().ne_attn_bwd_preprocess(q.data_ptr(), k.data_ptr(), o.data_ptr(),
+                                               do.data_ptr(), workspace.data_ptr(), wbytes, B, T,
+                                               Hq, Hkv, d, float(rope_theta), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd_preprocess")
 

@@ -101,7 +101,7 @@ int check_shape(int B, int T, int Hq, int Hkv, int d, float theta)
 
 // 4-D TMA descriptor over a contiguous [B][T][H][d] 16-bit tensor; box is
 // (one swizzle span of columns, 1 head, 128 rows, 1 batch).
-int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d)
+int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d, bool fp16 = false)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
@@ -113,7 +113,8 @@ int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d)
                              static_cast<cuuint64_t>(T) * H * d * 2};
     cuuint32_t box[4] = {static_cast<cuuint32_t>(swb / 2), 1, 128, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims,
+    CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     4, const_cast<void *>(ptr), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -132,6 +133,17 @@ void fill_rope(ne::RopeFreqs &fr, int d, float theta)
             static_cast<unsigned long long>(std::llround(f * 4294967296.0));
         fr.turn[i] = static_cast<uint32_t>(v & 0xffffffffull);
     }
+}
+
+// Backward workspace: [D: fp32 B*Hq*T][Q': fp16 B*T*Hq*d][K': fp16 B*T*Hkv*d],
+// each 256-aligned.
+size_t ws_d_bytes(int B, int T, int Hq)
+{
+    return ((static_cast<size_t>(B) * Hq * T * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+}
+size_t ws_q_bytes(int B, int T, int Hq, int d)
+{
+    return ((static_cast<size_t>(B) * T * Hq * d * 2) + 255) & ~static_cast<size_t>(255);
 }
 
 ne::AttnParams base_params(int B, int T, int Hq, int Hkv, int d, float theta, uint32_t *status)
@@ -182,7 +194,10 @@ __global__ void timeout_selftest_kernel(uint32_t *status, uint64_t limit_ns)
 namespace ne {
 
 int fwd_heads_per_cta(int d, int G) { return largest_divisor_at_most(G, d == 128 ? 2 : 4); }
-int dq_heads_per_cta(int d, int G) { return d == 128 ? 1 : largest_divisor_at_most(G, 4); }
+int dq_heads_per_cta(int d, int G)
+{
+    return d == 128 ? 1 : largest_divisor_at_most(G, d == 64 ? 3 : 4);
+}
 
 cudaError_t launch_timeout_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream)
 {
@@ -224,8 +239,7 @@ size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
 {
     if (check_shape(B, T, Hq, Hkv, d, 1.0f) != NE_OK)
         return 0;
-    const size_t bytes = static_cast<size_t>(B) * Hq * T * sizeof(float);
-    return (bytes + 255) & ~static_cast<size_t>(255);
+    return ws_d_bytes(B, T, Hq) + ws_q_bytes(B, T, Hq, d) + ws_q_bytes(B, T, Hkv, d);
 }
 
 } // extern "C"
@@ -236,7 +250,7 @@ namespace {
 int bwd_setup(const void *q, const void *k, const void *v, const float *lse, const void *dO,
               void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
               float rope_theta, ne::AttnParams *p, CUtensorMap *mq, CUtensorMap *mk,
-              CUtensorMap *mv, CUtensorMap *mdo)
+              CUtensorMap *mv, CUtensorMap *mdo, CUtensorMap *mqr, CUtensorMap *mkr)
 {
     if (!q || !k || !v || !lse || !dO)
         return NE_ERR_NULL;
@@ -255,8 +269,11 @@ int bwd_setup(const void *q, const void *k, const void *v, const float *lse, con
     p->do_in = dO;
     p->lse = const_cast<float *>(lse);
     p->Dws = static_cast<float *>(workspace);
+    void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);
+    void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
     if (make_map(mq, q, B, T, Hq, d) || make_map(mk, k, B, T, Hkv, d) ||
-        make_map(mv, v, B, T, Hkv, d) || make_map(mdo, dO, B, T, Hq, d))
+        make_map(mv, v, B, T, Hkv, d) || make_map(mdo, dO, B, T, Hq, d) ||
+        make_map(mqr, qrot, B, T, Hq, d, true) || make_map(mkr, krot, B, T, Hkv, d, true))
         return NE_ERR_CUDA;
     return NE_OK;
 }
@@ -285,27 +302,31 @@ int run_dkdv(int d, const ne::AttnParams &base, void *dk, void *dv, const CUtens
 
 extern "C" {
 
-int ne_attn_bwd_preprocess(const void *o, const void *dO, void *workspace,
-                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
-                           void *stream)
+int ne_attn_bwd_preprocess(const void *q, const void *k, const void *o, const void *dO,
+                           void *workspace, size_t workspace_bytes, int B, int T, int Hq,
+                           int Hkv, int d, float rope_theta, void *stream)
 {
-    if (!o || !dO)
+    if (!q || !k || !o || !dO)
         return NE_ERR_NULL;
-    int rc = check_shape(B, T, Hq, Hkv, d, 1.0f);
+    int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
     if (!workspace || workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
         return NE_ERR_WORKSPACE;
-    if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace))
+    if (!aligned16(q) || !aligned16(k) || !aligned16(o) || !aligned16(dO) ||
+        !aligned16(workspace))
         return NE_ERR_ALIGN;
     uint32_t *status = nullptr;
     if ((rc = device_state(&status)) != NE_OK)
         return rc;
-    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, 1.0f, status);
+    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, rope_theta, status);
     p.o_in = o;
     p.do_in = dO;
     p.Dws = static_cast<float *>(workspace);
-    return ne::launch_bwd_pre(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+    void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);
+    void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
+    return ne::launch_bwd_pre(d, p, q, qrot, k, krot, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
                ? NE_OK
                : NE_ERR_CUDA;
 }
@@ -319,12 +340,12 @@ int ne_attn_bwd_dq(const void *q, const void *k, const void *v, const float *lse
     if (!aligned16(dq))
         return NE_ERR_ALIGN;
     ne::AttnParams p;
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mqr, mkr;
     int rc = bwd_setup(q, k, v, lse, dO, const_cast<void *>(workspace), workspace_bytes, B, T,
-                       Hq, Hkv, d, rope_theta, &p, &mq, &mk, &mv, &mdo);
+                       Hq, Hkv, d, rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
     if (rc != NE_OK)
         return rc;
-    return run_dq(d, p, dq, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream));
+    return run_dq(d, p, dq, mqr, mkr, mv, mdo, static_cast<cudaStream_t>(stream));
 }
 
 int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *lse,
@@ -337,12 +358,12 @@ int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *l
     if (!aligned16(dk) || !aligned16(dv))
         return NE_ERR_ALIGN;
     ne::AttnParams p;
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mqr, mkr;
     int rc = bwd_setup(q, k, v, lse, dO, const_cast<void *>(workspace), workspace_bytes, B, T,
-                       Hq, Hkv, d, rope_theta, &p, &mq, &mk, &mv, &mdo);
+                       Hq, Hkv, d, rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
     if (rc != NE_OK)
         return rc;
-    return run_dkdv(d, p, dk, dv, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream));
+    return run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, static_cast<cudaStream_t>(stream));
 }
 
 int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -355,18 +376,20 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
     if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return NE_ERR_ALIGN;
     ne::AttnParams p;
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mqr, mkr;
     int rc = bwd_setup(q, k, v, lse, dO, workspace, workspace_bytes, B, T, Hq, Hkv, d,
-                       rope_theta, &p, &mq, &mk, &mv, &mdo);
+                       rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
     if (rc != NE_OK)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.o_in = o;
-    if (ne::launch_bwd_pre(d, p, st) != cudaSuccess)
+    void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);
+    void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
+    if (ne::launch_bwd_pre(d, p, q, qrot, k, krot, st) != cudaSuccess)
         return NE_ERR_CUDA;
-    if ((rc = run_dq(d, p, dq, mq, mk, mv, mdo, st)) != NE_OK)
+    if ((rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
         return rc;
-    return run_dkdv(d, p, dk, dv, mq, mk, mv, mdo, st);
+    return run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st);
 }
 
 int ne_attn_get_error(void *stream)

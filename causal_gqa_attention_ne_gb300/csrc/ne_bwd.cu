@@ -20,32 +20,66 @@ namespace ne {
 
 // ---------------------------------------------------------- preprocess ---
 
-// One thread per 16-byte chunk (8 elements) of a (b, t, h) row; the D/8
-// threads of a row reduce with shuffles.  Pure streaming over O and dO.
+// One pass over the query-side rows (b, t, h), one thread per pair of
+// 16-byte chunks (c, c + D/16) of a row, so the thread holds rotate-half
+// partners:
+//   D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c]       (fp32; the D/16
+//                threads of a row reduce with shuffles)
+//   Q'[b,t,h,:] = R(t) q[b,t,h,:] as fp16              (the score-side operands
+//   K'[b,s,j,:] = R(s) k[b,s,j,:] as fp16               of the backward, rotated
+//                once here instead of once per tile inside the loops)
+// Pure streaming over O, dO, q and k.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p)
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const uint4 *q,
+                                                      uint4 *qrot, const uint4 *k, uint4 *krot)
 {
-    constexpr int TPR = D / 8;   // threads per row
+    constexpr int TPR = D / 16;          // threads per row
+    constexpr int CPR = D / 8;           // 16-byte chunks per row
     const size_t nrows = static_cast<size_t>(p.B) * p.T * p.Hq;
-    const size_t nchunks = nrows * TPR;
+    const size_t nthreads = nrows * TPR;
     const uint4 *o = static_cast<const uint4 *>(p.o_in);
     const uint4 *g = static_cast<const uint4 *>(p.do_in);
-    for (size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-         c - (threadIdx.x % 32) < nchunks;   // keep whole warps in the loop for the shuffles
-         c += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float mx = 0.f;
+    for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         idx - (threadIdx.x % 32) < nthreads;   // whole warps stay in the loop for the shuffles
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
         float acc = 0.f;
-        if (c < nchunks) {
-            const uint4 a = o[c], b = g[c];
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+        const size_t row = idx / TPR;                // ((b*T + t)*Hq + h)
+        const int c = static_cast<int>(idx % TPR);
+        if (idx < nthreads) {
+            const size_t c0 = row * CPR + c, c1 = c0 + TPR;
+            const uint4 oa = o[c0], ob = o[c1], ga = g[c0], gb = g[c1];
+            const uint4 qa = q[c0], qb = q[c1];
+            const uint32_t oav[4] = {oa.x, oa.y, oa.z, oa.w}, obv[4] = {ob.x, ob.y, ob.z, ob.w};
+            const uint32_t gav[4] = {ga.x, ga.y, ga.z, ga.w}, gbv[4] = {gb.x, gb.y, gb.z, gb.w};
+            const uint32_t qav[4] = {qa.x, qa.y, qa.z, qa.w}, qbv[4] = {qb.x, qb.y, qb.z, qb.w};
+            const uint32_t t = static_cast<uint32_t>((row / p.Hq) % p.T);
+            uint32_t ra[4], rb[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc += bf16_lo(av[e]) * bf16_lo(bv[e]) + bf16_hi(av[e]) * bf16_hi(bv[e]);
+            for (int e = 0; e < 4; ++e) {
+                acc += bf16_lo(oav[e]) * bf16_lo(gav[e]) + bf16_hi(oav[e]) * bf16_hi(gav[e]);
+                acc += bf16_lo(obv[e]) * bf16_lo(gbv[e]) + bf16_hi(obv[e]) * bf16_hi(gbv[e]);
+                float u[2], w[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float sn, cs;
+                    rope_sincos(t, p.rope.turn[8 * c + 2 * e + hh], sn, cs);
+                    const float x = hh ? bf16_hi(qav[e]) : bf16_lo(qav[e]);
+                    const float y = hh ? bf16_hi(qbv[e]) : bf16_lo(qbv[e]);
+                    u[hh] = x * cs - y * sn;
+                    w[hh] = y * cs + x * sn;
+                    mx = fmaxf(mx, fmaxf(fabsf(u[hh]), fabsf(w[hh])));
+                }
+                ra[e] = pack_f16x2(u[0], u[1]);
+                rb[e] = pack_f16x2(w[0], w[1]);
+            }
+            qrot[c0] = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+            qrot[c1] = make_uint4(rb[0], rb[1], rb[2], rb[3]);
         }
 #pragma unroll
         for (int off = TPR / 2; off >= 1; off /= 2)
             acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (c < nchunks && (c % TPR) == 0) {
-            const size_t row = c / TPR;                  // ((b*T + t)*Hq + h)
+        if (idx < nthreads && c == 0) {
             const int h = static_cast<int>(row % p.Hq);
             const size_t bt = row / p.Hq;
             const int t = static_cast<int>(bt % p.T);
@@ -53,19 +87,55 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p)
             p.Dws[(static_cast<size_t>(b) * p.Hq + h) * p.T + t] = acc;
         }
     }
+    // K' = R(s) k as fp16, same layout as k.
+    const size_t krows = static_cast<size_t>(p.B) * p.T * p.Hkv;
+    for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         idx < krows * TPR; idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t row = idx / TPR;                // ((b*T + s)*Hkv + j)
+        const int c = static_cast<int>(idx % TPR);
+        const size_t c0 = row * CPR + c, c1 = c0 + TPR;
+        const uint4 ka = k[c0], kb = k[c1];
+        const uint32_t kav[4] = {ka.x, ka.y, ka.z, ka.w}, kbv[4] = {kb.x, kb.y, kb.z, kb.w};
+        const uint32_t pos = static_cast<uint32_t>((row / p.Hkv) % p.T);
+        uint32_t ra[4], rb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float u[2], w[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float sn, cs;
+                rope_sincos(pos, p.rope.turn[8 * c + 2 * e + hh], sn, cs);
+                const float x = hh ? bf16_hi(kav[e]) : bf16_lo(kav[e]);
+                const float y = hh ? bf16_hi(kbv[e]) : bf16_lo(kbv[e]);
+                u[hh] = x * cs - y * sn;
+                w[hh] = y * cs + x * sn;
+                mx = fmaxf(mx, fmaxf(fabsf(u[hh]), fabsf(w[hh])));
+            }
+            ra[e] = pack_f16x2(u[0], u[1]);
+            rb[e] = pack_f16x2(w[0], w[1]);
+        }
+        krot[c0] = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+        krot[c1] = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+    }
+    if (mx > kFp16Max)
+        atomicOr(p.status, kDevRange);
 }
 
-cudaError_t launch_bwd_pre(int d, const AttnParams &p, cudaStream_t stream)
+cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot, const void *k,
+                           void *krot, cudaStream_t stream)
 {
-    const size_t nchunks = static_cast<size_t>(p.B) * p.T * p.Hq * (d / 8);
-    size_t blocks = (nchunks + 255) / 256;
+    const size_t nthreads = static_cast<size_t>(p.B) * p.T * p.Hq * (d / 16);
+    size_t blocks = (nthreads + 255) / 256;
     const size_t cap = 152 * 16;
     if (blocks > cap)
         blocks = cap;
+    const uint4 *qi = static_cast<const uint4 *>(q), *ki = static_cast<const uint4 *>(k);
+    uint4 *qo = static_cast<uint4 *>(qrot), *ko = static_cast<uint4 *>(krot);
+    const unsigned nb = static_cast<unsigned>(blocks);
     switch (d) {
-    case 32: bwd_pre_kernel<32><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p); break;
-    case 64: bwd_pre_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p); break;
-    case 128: bwd_pre_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p); break;
+    case 32: bwd_pre_kernel<32><<<nb, 256, 0, stream>>>(p, qi, qo, ki, ko); break;
+    case 64: bwd_pre_kernel<64><<<nb, 256, 0, stream>>>(p, qi, qo, ki, ko); break;
+    case 128: bwd_pre_kernel<128><<<nb, 256, 0, stream>>>(p, qi, qo, ki, ko); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -129,26 +199,54 @@ __device__ __forceinline__ void epilogue_inverse_rope(uint32_t taddr, float scal
 
 // ------------------------------------------------------------------ dQ ---
 //
-// CTA = (b, kv head j, query tile m, GC query heads).  Roles as in the
-// forward kernel.  TMEM: S [0,128), dP [128,256), dQ of head g at 256 + g*D.
+// Persistent: one CTA per SM walks a snake-ordered list of work units
+// (b, kv head j, query tile m, chunk of GC query heads), heaviest (largest m)
+// first.  Per unit the loop runs over the causal key tiles jk <= m and the GC
+// heads ("items"); each K'/V tile is loaded once and used by the GC heads.
+// Warp roles (384 threads):
+//   warps 0-7   two row warpgroups; warpgroup w handles key columns
+//               [64w, 64w+64) of every 128x128 tile: P = exp(S - lse),
+//               dS = P (dP - D), dS (fp16) to TMEM as the A operand of
+//               dQ += dS K'; at the end of a unit, dQ * scale with the inverse
+//               RoPE to bf16 (warpgroup w takes heads g = w, w+2, ...).
+//   warp 8      TMA producer.   warp 9  TMEM allocator + S/dP issuer.
+//   warp 10     dQ issuer.      warp 11 idle.
+// TMEM: S [0,128) dP [128,256) dS [256,320) dQ of head g at 320 + g*D.
 
 template <int D, int GC, int ST>
 struct DqCfg {
     using TL = Tile<D>;
-    static constexpr int PTILE = kRows * 128 * 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_DO = OFF_Q + GC * TL::BYTES;
     static constexpr int OFF_K = OFF_DO + GC * TL::BYTES;
     static constexpr int OFF_V = OFF_K + ST * TL::BYTES;
-    static constexpr int OFF_DS = OFF_V + ST * TL::BYTES;
-    static constexpr int SMEM_BYTES = smem_one_cta(OFF_DS + PTILE + 1024);
+    static constexpr int SMEM_BYTES = smem_one_cta(OFF_V + ST * TL::BYTES + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(256 + GC * D <= 512, "TMEM budget");
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DS = 256, COL_DQ = 320;
+    static_assert(COL_DQ + GC * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+struct DqUnit {
+    int m, b, j, h0;
+};
+
+__device__ __forceinline__ DqUnit dq_unit(int u, int GC, const AttnParams &p)
+{
+    DqUnit w;
+    const int per_m = p.B * p.Hkv * p.nchunks;
+    w.m = p.M - 1 - u / per_m;
+    int rem = u % per_m;
+    const int chunk = rem % p.nchunks;
+    rem /= p.nchunks;
+    w.j = rem % p.Hkv;
+    w.b = rem / p.Hkv;
+    w.h0 = w.j * p.G + chunk * GC;
+    return w;
+}
+
 template <int D, int GC, int ST>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const AttnParams p)
@@ -158,42 +256,33 @@ __global__ void __launch_bounds__(320, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_q_full, bar_do_full, bar_q_ready, bar_drain;
-    __shared__ uint64_t bar_k_full[ST], bar_k_ready[ST], bar_v_full[ST], bar_kv_empty[ST];
-    __shared__ uint64_t bar_s_full, bar_s_empty, bar_ds_full, bar_dq_done[2];
+    __shared__ uint64_t bar_q_full[GC], bar_q_empty[GC];
+    __shared__ uint64_t bar_kv_full[ST], bar_kv_empty[ST];
+    __shared__ uint64_t bar_s_full, bar_s_empty, bar_ds_full, bar_ds_empty;
+    __shared__ uint64_t bar_dq_done, bar_dq_free, bar_drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int per_m = p.B * p.Hkv * p.nchunks;
-    const int m = p.M - 1 - static_cast<int>(blockIdx.x) / per_m;
-    int rem = static_cast<int>(blockIdx.x) % per_m;
-    const int chunk = rem % p.nchunks;
-    rem /= p.nchunks;
-    const int j = rem % p.Hkv;
-    const int b = rem / p.Hkv;
-    const int h0 = j * p.G + chunk * GC;
-    const int t0 = m * kRows;
-    const int nkv = m + 1;
-    const int nitems = nkv * GC;
+    const int cta = static_cast<int>(blockIdx.x), P = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         abort_s = 0;
-        mbar_init(smem_u32(&bar_q_full), 1);
-        mbar_init(smem_u32(&bar_do_full), 1);
-        mbar_init(smem_u32(&bar_q_ready), 4);
-        mbar_init(smem_u32(&bar_drain), 1);
+        for (int g = 0; g < GC; ++g) {
+            mbar_init(smem_u32(&bar_q_full[g]), 1);
+            mbar_init(smem_u32(&bar_q_empty[g]), 1);
+        }
         for (int s = 0; s < ST; ++s) {
-            mbar_init(smem_u32(&bar_k_full[s]), 1);
-            mbar_init(smem_u32(&bar_k_ready[s]), 4);
-            mbar_init(smem_u32(&bar_v_full[s]), 1);
+            mbar_init(smem_u32(&bar_kv_full[s]), 1);
             mbar_init(smem_u32(&bar_kv_empty[s]), 1);
         }
         mbar_init(smem_u32(&bar_s_full), 1);
-        mbar_init(smem_u32(&bar_s_empty), 4);
-        mbar_init(smem_u32(&bar_ds_full), 4);
-        mbar_init(smem_u32(&bar_dq_done[0]), 1);
-        mbar_init(smem_u32(&bar_dq_done[1]), 1);
+        mbar_init(smem_u32(&bar_s_empty), 8);
+        mbar_init(smem_u32(&bar_ds_full), 8);
+        mbar_init(smem_u32(&bar_ds_empty), 1);
+        mbar_init(smem_u32(&bar_dq_done), 1);
+        mbar_init(smem_u32(&bar_dq_free), 8);
+        mbar_init(smem_u32(&bar_drain), 2);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -205,289 +294,406 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_base_s;
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
+    auto teardown = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 9) {
+            tc_fence_after();
+            tmem_dealloc(tbase, C::TMEM_COLS);
+        }
+    };
 
-    if (warp == 8) {
-        if (lane == 0) {
+    // Register budgets after the split (launched with 168 per thread x 384):
+    // rows 216 x 256 + the rest 64 x 128 <= 64512.
+    if (warp >= 8) {
+        regs_release<64>();
+        if (warp == 8 && lane == 0) {
+            // ------------------------------------------------ TMA producer ---
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmDO);
-            const uint32_t qb = smem_u32(&bar_q_full), db = smem_u32(&bar_do_full);
-            mbar_arrive_expect_tx(qb, GC * TL::BYTES);
-            for (int g = 0; g < GC; ++g)
-                for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_Q + g * TL::BYTES + cb * TL::BLOCK), &tmQ,
-                                qb, cb * TL::BOX_COLS, h0 + g, t0, b);
-            mbar_arrive_expect_tx(db, GC * TL::BYTES);
-            for (int g = 0; g < GC; ++g)
-                for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_DO + g * TL::BYTES + cb * TL::BLOCK),
-                                &tmDO, db, cb * TL::BOX_COLS, h0 + g, t0, b);
-            int issued = 0;
-            for (int jk = 0; jk < nkv; ++jk) {
-                const int st = jk % ST, u = jk / ST;
-                if (u >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u - 1) & 1, wc))
+            bool ok = true;
+            int kt = 0, k = 0;
+            for (; ok; ++k) {
+                const int u = snake_unit(k, cta, P);
+                if (u >= p.num_units)
                     break;
-                const uint32_t kb = smem_u32(&bar_k_full[st]), vb = smem_u32(&bar_v_full[st]);
-                mbar_arrive_expect_tx(kb, TL::BYTES);
-                for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK), &tmK,
-                                kb, cb * TL::BOX_COLS, j, jk * kRows, b);
-                mbar_arrive_expect_tx(vb, TL::BYTES);
-                for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK), &tmV,
-                                vb, cb * TL::BOX_COLS, j, jk * kRows, b);
-                issued = jk + 1;
-            }
-            if (*wc.abort) {
-                mbar_wait_drain(smem_u32(&bar_do_full), 0, wc.limit_ns);
-                for (int jk = (issued > ST ? issued - ST : 0); jk < issued; ++jk) {
-                    const int st = jk % ST, u = jk / ST;
-                    mbar_wait_drain(smem_u32(&bar_k_full[st]), u & 1, wc.limit_ns);
-                    mbar_wait_drain(smem_u32(&bar_v_full[st]), u & 1, wc.limit_ns);
+                const DqUnit w = dq_unit(u, GC, p);
+                for (int g = 0; g < GC && ok; ++g) {
+                    if (k >= 1 && !mbar_wait(smem_u32(&bar_q_empty[g]), (k - 1) & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t qb = smem_u32(&bar_q_full[g]);
+                    mbar_arrive_expect_tx(qb, 2 * TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb) {
+                        tma_load_4d(smem_u32(smem + C::OFF_Q + g * TL::BYTES + cb * TL::BLOCK),
+                                    &tmQ, qb, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                        tma_load_4d(smem_u32(smem + C::OFF_DO + g * TL::BYTES + cb * TL::BLOCK),
+                                    &tmDO, qb, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                    }
+                }
+                for (int jk = 0; jk <= w.m && ok; ++jk, ++kt) {
+                    const int st = kt % ST, u2 = kt / ST;
+                    if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t kb = smem_u32(&bar_kv_full[st]);
+                    mbar_arrive_expect_tx(kb, 2 * TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb) {
+                        tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmK, kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                        tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmV, kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                    }
                 }
             }
-        }
-    } else if (warp == 9) {
-        if (lane == 0) {
+            if (*wc.abort) {
+                for (int g = 0; g < GC; ++g)
+                    mbar_wait_drain(smem_u32(&bar_q_full[g]), (k > 0 ? k - 1 : 0) & 1, wc.limit_ns);
+                for (int t = (kt > ST ? kt - ST : 0); t < kt; ++t)
+                    mbar_wait_drain(smem_u32(&bar_kv_full[t % ST]), (t / ST) & 1, wc.limit_ns);
+            }
+        } else if (warp == 9 || warp == 10) {
+            // -------------------------------------------------- MMA issuers ---
             constexpr uint32_t ID_S = idesc_f16(128, 128, false, false, false);
             constexpr uint32_t ID_DP = idesc_f16(128, 128, true, false, false);
             constexpr uint32_t ID_DQ = idesc_f16(128, TL::NPV, false, false, true);
-            const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
-            const uint32_t do_addr = smem_u32(smem + C::OFF_DO);
-            const uint32_t k_addr = smem_u32(smem + C::OFF_K);
-            const uint32_t v_addr = smem_u32(smem + C::OFF_V);
-            const uint32_t ds_addr = smem_u32(smem + C::OFF_DS);
-            bool ok = mbar_wait(smem_u32(&bar_q_ready), 0, wc) &&
-                      mbar_wait(smem_u32(&bar_do_full), 0, wc);
-            auto do_dq = [&](int x) -> bool {
-                const int jx = x / GC, gx = x % GC, stx = jx % ST;
-                if (!mbar_wait(smem_u32(&bar_ds_full), x & 1, wc))
-                    return false;
-                tc_fence_after();
-                const uint32_t ka = k_addr + stx * TL::BYTES;
-                const uint32_t dd = tbase + 256 + gx * D;
+            constexpr uint32_t TSTEP = TL::BYTES >> 4;
+            const uint32_t sbase = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
+            const uint32_t tb = __shfl_sync(0xffffffffu, tbase, 0);
+            bool ok = true;
+            int gi = 0, kt = 0;
+            if (warp == 9) {
+                const uint64_t dQ0 = desc_kmajor_base<D>(sbase + C::OFF_Q);
+                const uint64_t dO0 = desc_kmajor_base<D>(sbase + C::OFF_DO);
+                const uint64_t dK0 = desc_kmajor_base<D>(sbase + C::OFF_K);
+                const uint64_t dV0 = desc_kmajor_base<D>(sbase + C::OFF_V);
+                for (int k = 0; ok; ++k) {
+                    const int u = snake_unit(k, cta, P);
+                    if (u >= p.num_units)
+                        break;
+                    const DqUnit w = dq_unit(u, GC, p);
+                    const int nitems = (w.m + 1) * GC;
+                    for (int it = 0; it < nitems; ++it, ++gi) {
+                        const int jk = it / GC, g = it % GC;
+                        const int st = kt % ST;
+                        if ((g == 0 && !mbar_wait_warp(smem_u32(&bar_kv_full[st]), (kt / ST) & 1, wc)) ||
+                            (jk == 0 && !mbar_wait_warp(smem_u32(&bar_q_full[g]), k & 1, wc)) ||
+                            (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_s_empty), (gi - 1) & 1, wc))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t qd = dQ0 + g * TSTEP, od = dO0 + g * TSTEP;
+                        const uint64_t kd = dK0 + st * TSTEP, vd = dV0 + st * TSTEP;
+                        if (elect_one()) {
 #pragma unroll
-                for (int nc = 0; nc < D / TL::NPV; ++nc)
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_f16_ss(tb + C::COL_S, qd + kmajor_off<D>(kk),
+                                           kd + kmajor_off<D>(kk), ID_S, kk > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(dd + nc * TL::NPV, desc_ptile(ds_addr, kk),
-                                   desc_mnmajor<D>(ka, nc, kk), ID_DQ,
-                                   (jx > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(smem_u32(&bar_dq_done[x % 2]));
-                if (gx == GC - 1)
-                    mma_commit(smem_u32(&bar_kv_empty[stx]));
-                return true;
-            };
-            for (int i = 0; ok && i < nitems; ++i) {
-                const int jk = i / GC, g = i % GC, st = jk % ST;
-                if (g == 0 && !(mbar_wait(smem_u32(&bar_k_ready[st]), (jk / ST) & 1, wc) &&
-                                mbar_wait(smem_u32(&bar_v_full[st]), (jk / ST) & 1, wc))) {
-                    ok = false;
-                    break;
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_f16_ss(tb + C::COL_DP, od + kmajor_off<D>(kk),
+                                           vd + kmajor_off<D>(kk), ID_DP, kk > 0 ? 1u : 0u);
+                            mma_commit(smem_u32(&bar_s_full));
+                            if (jk == w.m)   // last use of head g's Q'/dO in this unit
+                                mma_commit(smem_u32(&bar_q_empty[g]));
+                        }
+                        __syncwarp();
+                        if (g == GC - 1)
+                            ++kt;
+                    }
                 }
-                if (i >= 1 && !mbar_wait(smem_u32(&bar_s_empty), (i - 1) & 1, wc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t qa = q_addr + g * TL::BYTES, oa = do_addr + g * TL::BYTES;
-                const uint32_t ka = k_addr + st * TL::BYTES, va = v_addr + st * TL::BYTES;
+            } else {
+                const uint64_t dKm0 = desc_mnmajor_base<D>(sbase + C::OFF_K);
+                for (int k = 0; ok; ++k) {
+                    const int u = snake_unit(k, cta, P);
+                    if (u >= p.num_units)
+                        break;
+                    const DqUnit w = dq_unit(u, GC, p);
+                    const int nitems = (w.m + 1) * GC;
+                    for (int it = 0; it < nitems; ++it, ++gi) {
+                        const int jk = it / GC, g = it % GC;
+                        const int st = kt % ST;
+                        if (!mbar_wait_warp(smem_u32(&bar_ds_full), gi & 1, wc) ||
+                            (it == 0 && k >= 1 &&
+                             !mbar_wait_warp(smem_u32(&bar_dq_free), (k - 1) & 1, wc))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t km = dKm0 + st * TSTEP;
+                        const uint32_t first = (jk > 0) ? 1u : 0u;
+                        if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16_ss(tbase, desc_kmajor<D>(qa, kk), desc_kmajor<D>(ka, kk), ID_S,
-                               kk > 0 ? 1u : 0u);
+                            for (int nc = 0; nc < D / TL::NPV; ++nc)
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16_ss(tbase + 128, desc_kmajor<D>(oa, kk), desc_kmajor<D>(va, kk), ID_DP,
-                               kk > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&bar_s_full));
-                if (i >= 1 && !do_dq(i - 1)) {
-                    ok = false;
-                    break;
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_f16_ts(tb + C::COL_DQ + g * D + nc * TL::NPV,
+                                               tb + C::COL_DS + 8 * kk, km + mnmajor_off<D>(nc, kk),
+                                               ID_DQ, kk > 0 ? 1u : first);
+                            mma_commit(smem_u32(&bar_ds_empty));
+                            if (g == GC - 1)
+                                mma_commit(smem_u32(&bar_kv_empty[st]));
+                            if (it == nitems - 1)
+                                mma_commit(smem_u32(&bar_dq_done));
+                        }
+                        __syncwarp();
+                        if (g == GC - 1)
+                            ++kt;
+                    }
                 }
             }
-            if (ok)
-                do_dq(nitems - 1);
-            mma_commit(smem_u32(&bar_drain));
-            mbar_wait(smem_u32(&bar_drain), 0, wc);
-        }
-    } else if (warp >= 4) {
-        const int r = threadIdx.x - 128;
-        float mx = 0.f;
-        bool ok = mbar_wait_warp(smem_u32(&bar_q_full), 0, wc);
-        if (ok) {
-            for (int g = 0; g < GC; ++g)
-                mx = fmaxf(mx, rope_row_to_f16<D>(smem + C::OFF_Q + g * TL::BYTES, r,
-                                                  static_cast<uint32_t>(t0 + r), p.rope));
-            fence_proxy_async_smem();
+            if (elect_one())
+                mma_commit(smem_u32(&bar_drain));
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_q_ready));
-            for (int jk = 0; jk < nkv; ++jk) {
-                const int st = jk % ST;
-                if (!mbar_wait_warp(smem_u32(&bar_k_full[st]), (jk / ST) & 1, wc))
-                    break;
-                mx = fmaxf(mx, rope_row_to_f16<D>(smem + C::OFF_K + st * TL::BYTES, r,
-                                                  static_cast<uint32_t>(jk * kRows + r), p.rope));
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&bar_k_ready[st]));
-            }
+            mbar_wait_warp(smem_u32(&bar_drain), 0, wc);
         }
-        if (mx > kFp16Max)
-            atomicOr(p.status, kDevRange);
-    } else {
-        const int r = threadIdx.x;
-        const int t = t0 + r;
-        const uint32_t lane_base = tmem_addr(tbase, warp * 32, 0);
-        float lse2[GC], Dv[GC];
+        teardown();
+        return;
+    }
+
+    // ---------------------------------------------------- row warpgroups ---
+    regs_claim<216>();
+    const int w = warp >> 2;                // key-column half of the score tile
+    const int r = threadIdx.x & 127;        // query row == TMEM lane
+    const uint32_t lane_base = tmem_addr(tbase, (warp & 3) * 32, 0);
+    float maxds = 0.f;
+    bool ok = true;
+    int gi = 0;
+    float nl2[GC], nD[GC];
+    auto fetch = [&](int k, float (&l2)[GC], float (&dd)[GC]) {
+        const int u = snake_unit(k, cta, P);
 #pragma unroll
         for (int g = 0; g < GC; ++g) {
-            const size_t idx = (static_cast<size_t>(b) * p.Hq + h0 + g) * p.T + t;
-            lse2[g] = (t < p.T) ? p.lse[idx] * kLog2e : 0.f;
-            Dv[g] = (t < p.T) ? p.Dws[idx] : 0.f;
+            l2[g] = 0.f;
+            dd[g] = 0.f;
         }
-        float maxds = 0.f;
-        bool ok = true;
-        uint8_t *dst = smem + C::OFF_DS;
-        for (int i = 0; i < nitems; ++i) {
-            const int jk = i / GC, g = i % GC;
-            if (!mbar_wait_warp(smem_u32(&bar_s_full), i & 1, wc)) {
+        if (u >= p.num_units)
+            return;
+        const DqUnit un = dq_unit(u, GC, p);
+        const int t = un.m * kRows + r;
+        if (t < p.T) {
+#pragma unroll
+            for (int g = 0; g < GC; ++g) {
+                const size_t idx = (static_cast<size_t>(un.b) * p.Hq + un.h0 + g) * p.T + t;
+                l2[g] = p.lse[idx] * kLog2e;
+                dd[g] = p.Dws[idx];
+            }
+        }
+    };
+    fetch(0, nl2, nD);
+    for (int k = 0; ok; ++k) {
+        const int u = snake_unit(k, cta, P);
+        if (u >= p.num_units)
+            break;
+        const DqUnit un = dq_unit(u, GC, p);
+        float l2[GC], dd[GC];
+#pragma unroll
+        for (int g = 0; g < GC; ++g) {
+            l2[g] = nl2[g];
+            dd[g] = nD[g];
+        }
+        fetch(k + 1, nl2, nD);              // next unit's row scalars, in flight meanwhile
+        const int nitems = (un.m + 1) * GC;
+        for (int it = 0; it < nitems; ++it, ++gi) {
+            const int jk = it / GC, g = it % GC;
+            if (!mbar_wait_warp(smem_u32(&bar_s_full), gi & 1, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            if (i >= 1 &&
-                !mbar_wait_warp(smem_u32(&bar_dq_done[(i - 1) % 2]), ((i - 1) / 2) & 1, wc)) {
+            uint32_t sv[2][32], pv[2][32];
+            tmem_ld32(lane_base + C::COL_S + 64 * w, sv[0]);
+            tmem_ld32(lane_base + C::COL_S + 64 * w + 32, sv[1]);
+            tmem_ld32(lane_base + C::COL_DP + 64 * w, pv[0]);
+            tmem_ld32(lane_base + C::COL_DP + 64 * w + 32, pv[1]);
+            tmem_ld_wait_only();
+            tmem_tie(sv[0]);
+            tmem_tie(sv[1]);
+            tmem_tie(pv[0]);
+            tmem_tie(pv[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&bar_s_empty));
+
+            // the per-head row scalars, selected without dynamic indexing
+            float lg = l2[0], dg = dd[0];
+#pragma unroll
+            for (int q = 1; q < GC; ++q)
+                if (g == q) {
+                    lg = l2[q];
+                    dg = dd[q];
+                }
+            const float sl2 = p.scale_log2;
+            uint32_t dk[32];
+            if (jk != un.m) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -lg));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -lg));
+                        const float d0 = p0 * (__uint_as_float(pv[h][e]) - dg);
+                        const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - dg);
+                        maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
+                        dk[16 * h + e / 2] = pack_f16x2(d0, d1);
+                    }
+            } else {
+                // diagonal tile: key column c > query row r is masked
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int c = 64 * w + 32 * h + e;
+                        float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -lg));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -lg));
+                        p0 = (c > r) ? 0.f : p0;
+                        p1 = (c + 1 > r) ? 0.f : p1;
+                        const float d0 = p0 * (__uint_as_float(pv[h][e]) - dg);
+                        const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - dg);
+                        maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
+                        dk[16 * h + e / 2] = pack_f16x2(d0, d1);
+                    }
+            }
+            if (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_ds_empty), (gi - 1) & 1, wc)) {
                 ok = false;
                 break;
             }
-            const bool diag = (jk == m);
-            const float lg = lse2[g], dg = Dv[g];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sv[32], pv[32];
-                tmem_ld32(lane_base + cc * 32, sv);
-                tmem_ld32(lane_base + 128 + cc * 32, pv);
-                tmem_ld_wait(sv);
-                tmem_tie(pv);
-                if (cc == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&bar_s_empty));
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int c = cc * 32 + e;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -lg));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -lg));
-                    if (diag && c > r)
-                        p0 = 0.f;
-                    if (diag && c + 1 > r)
-                        p1 = 0.f;
-                    const float d0 = p0 * (__uint_as_float(pv[e]) - dg);
-                    const float d1 = p1 * (__uint_as_float(pv[e + 1]) - dg);
-                    maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
-                    pk[e / 2] = pack_f16x2(d0, d1);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(dst + ptile_chunk(r, cc * 4 + q)) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-            fence_proxy_async_smem();
+            tc_fence_after();
+            tmem_st32(lane_base + C::COL_DS + 32 * w, dk);
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&bar_ds_full));
         }
-        if (maxds > kFp16Max)
-            atomicOr(p.status, kDevRange);
-        if (ok) {
-            const int x = nitems - 1;
-            ok = mbar_wait_warp(smem_u32(&bar_dq_done[x % 2]), (x / 2) & 1, wc);
+        if (!ok)
+            break;
+        // ---- unit epilogue: dq = R(t)^T dQ' * scale, bf16 ----
+        if (!mbar_wait_warp(smem_u32(&bar_dq_done), k & 1, wc)) {
+            ok = false;
+            break;
         }
-        if (ok) {
-            tc_fence_after();
-            __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.out0);
+        tc_fence_after();
+        const int t = un.m * kRows + r;
+        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.out0);
 #pragma unroll
-            for (int g = 0; g < GC; ++g) {
+        for (int g = 0; g < GC; ++g)
+            if ((g & 1) == w) {
                 __nv_bfloat16 *row =
-                    dq + ((static_cast<size_t>(b) * p.T + t) * p.Hq + h0 + g) * D;
-                epilogue_inverse_rope<D>(lane_base + 256 + g * D, p.scale,
+                    dq + ((static_cast<size_t>(un.b) * p.T + t) * p.Hq + un.h0 + g) * D;
+                epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
                                          static_cast<uint32_t>(t), p.rope, row, t < p.T);
             }
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&bar_dq_free));
     }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 9) {
-        tc_fence_after();
-        tmem_dealloc(tbase, C::TMEM_COLS);
-    }
+    if (maxds > kFp16Max)
+        atomicOr(p.status, kDevRange);
+    teardown();
 }
 
 // ---------------------------------------------------------------- dK dV ---
 //
-// CTA = (b, kv head j, key tile n).  K' and V stay in shared memory; the loop
-// runs over the G query heads of the group and the causal query tiles m >= n.
-// Transposed scores: thread r owns key row r.  TMEM: S^T [0,128),
-// dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
+// Persistent: one CTA per SM walks a snake-ordered list of work units
+// (b, kv head j, key tile n), heaviest (n = 0) first.  Within a unit K' and
+// V stay in shared memory and the loop runs over the G query heads of the
+// group and the causal query tiles m >= n ("items").  Transposed scores: key
+// row r lives in TMEM lane r.  K/V are double-buffered across units (D <= 64)
+// so the next unit's tiles land and are rotated while the current one runs.
+// Warp roles (512 threads):
+//   warps 0-7   two "row" warpgroups; warpgroup w handles query columns
+//               [64w, 64w+64) of every 128x128 tile of S^T and dP^T: reads them
+//               from TMEM, computes P^T = exp(S^T - lse) and
+//               dS^T = P^T (dP^T - D), writes both back to TMEM (bf16 / fp16)
+//               where they are the A operands of dV += P^T dO and dK += dS^T Q';
+//               at the end of a unit they store dV (warpgroup 0) and dK
+//               (warpgroup 1, inverse RoPE).
+//   warps 8-11  lse/D of each item's 128 queries into shared memory.  Q' and
+//               K' arrive already rotated (fp16) from the preprocess pass,
+//               through the workspace.
+//   warp 12     TMA producer.      warp 13  TMEM allocator + S^T/dP^T issuer.
+//   warp 14     dV/dK issuer.
+// TMEM (D <= 64): S^T [0,128) dP^T [128,256) P^T [256,320) dS^T [320,384)
+// dV [384, 384+D) dK [384+D, 384+2D).  D = 128: P^T / dS^T overwrite the
+// half of S^T / dP^T each warpgroup has already read, dV [256,384),
+// dK [384,512), and the items run in order (no overlap of item i's dV/dK
+// with item i+1's scores).
 
 template <int D, int ST>
 struct DkvCfg {
     using TL = Tile<D>;
-    static constexpr int PTILE = kRows * 128 * 2;
+    static constexpr bool ALIAS = (D == 128);
+    static constexpr int KB = (D == 128) ? 1 : 2;                    // K/V buffers
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = TL::BYTES;
-    static constexpr int OFF_Q = 2 * TL::BYTES;
+    static constexpr int OFF_V = KB * TL::BYTES;
+    static constexpr int OFF_Q = 2 * KB * TL::BYTES;
     static constexpr int OFF_DO = OFF_Q + ST * TL::BYTES;
-    static constexpr int OFF_PT = OFF_DO + ST * TL::BYTES;
-    static constexpr int OFF_DST = OFF_PT + PTILE;
-    static constexpr int SMEM_BYTES = smem_one_cta(OFF_DST + PTILE + 1024);
+    static constexpr int OFF_LSED = OFF_DO + ST * TL::BYTES;          // float2 [ST][128]
+    static constexpr int SMEM_BYTES = smem_one_cta(OFF_LSED + ST * kRows * 8 + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(256 + 2 * D <= 512, "TMEM budget");
+    static constexpr uint32_t COL_S = 0, COL_DP = 128;
+    static constexpr uint32_t COL_DV = ALIAS ? 256 : 384;
+    static constexpr uint32_t COL_DK = COL_DV + D;
+    static __host__ __device__ constexpr uint32_t col_p(int w) { return ALIAS ? 64 * w : 256 + 32 * w; }
+    static __host__ __device__ constexpr uint32_t col_ds(int w) { return ALIAS ? 128 + 64 * w : 320 + 32 * w; }
+    static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+struct DkvUnit {
+    int n, b, j, nitems;
+};
+
+__device__ __forceinline__ DkvUnit dkv_unit(int u, const AttnParams &p)
+{
+    DkvUnit w;
+    const int per_n = p.B * p.Hkv;
+    w.n = u / per_n;
+    const int rem = u % per_n;
+    w.j = rem % p.Hkv;
+    w.b = rem / p.Hkv;
+    w.nitems = (p.M - w.n) * p.G;
+    return w;
+}
+
 template <int D, int ST>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                 const AttnParams p)
 {
     using C = DkvCfg<D, ST>;
     using TL = Tile<D>;
+    constexpr int KB = C::KB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_k_full, bar_v_full, bar_k_ready, bar_drain, bar_acc_done;
+    __shared__ uint64_t bar_k_full[KB], bar_v_full[KB], bar_kv_empty[KB];
     __shared__ uint64_t bar_q_full[ST], bar_do_full[ST], bar_q_ready[ST], bar_st_empty[ST];
     __shared__ uint64_t bar_s_full, bar_s_empty, bar_pds_full, bar_pds_empty;
-    __shared__ float2 lsed[2][kRows];
+    __shared__ uint64_t bar_acc_done, bar_acc_free, bar_drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
+    float2 *lsed = reinterpret_cast<float2 *>(smem + C::OFF_LSED);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int per_n = p.B * p.Hkv;
-    const int n = static_cast<int>(blockIdx.x) / per_n;   // heaviest (n = 0) first
-    const int rem = static_cast<int>(blockIdx.x) % per_n;
-    const int j = rem % p.Hkv;
-    const int b = rem / p.Hkv;
-    const int s0 = n * kRows;
-    const int nitems = (p.M - n) * p.G;
+    const int cta = static_cast<int>(blockIdx.x), P = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         abort_s = 0;
-        mbar_init(smem_u32(&bar_k_full), 1);
-        mbar_init(smem_u32(&bar_v_full), 1);
-        mbar_init(smem_u32(&bar_k_ready), 4);
-        mbar_init(smem_u32(&bar_drain), 1);
-        mbar_init(smem_u32(&bar_acc_done), 1);
+        for (int s = 0; s < KB; ++s) {
+            mbar_init(smem_u32(&bar_k_full[s]), 1);
+            mbar_init(smem_u32(&bar_v_full[s]), 1);
+            mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+        }
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&bar_q_full[s]), 1);
             mbar_init(smem_u32(&bar_do_full[s]), 1);
@@ -495,12 +701,15 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(smem_u32(&bar_st_empty[s]), 1);
         }
         mbar_init(smem_u32(&bar_s_full), 1);
-        mbar_init(smem_u32(&bar_s_empty), 4);
-        mbar_init(smem_u32(&bar_pds_full), 4);
+        mbar_init(smem_u32(&bar_s_empty), 8);
+        mbar_init(smem_u32(&bar_pds_full), 8);
         mbar_init(smem_u32(&bar_pds_empty), 1);
+        mbar_init(smem_u32(&bar_acc_done), 1);
+        mbar_init(smem_u32(&bar_acc_free), 8);
+        mbar_init(smem_u32(&bar_drain), 2);
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
         tmem_relinquish();
         tc_fence_before();
@@ -509,142 +718,250 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_base_s;
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
+    // Each role ends with its own copy of the teardown: warps run under
+    // different register budgets after setmaxnreg, so their code paths never
+    // re-join.
+    auto teardown = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 13) {
+            tc_fence_after();
+            tmem_dealloc(tbase, C::TMEM_COLS);
+        }
+    };
 
-    if (warp == 8) {
-        if (lane == 0) {
+    // Register budgets after the split (launched with 128 per thread x 512):
+    // rows 184 x 256 + RoPE 56 x 128 + TMA/MMA 80 x 128 <= 65536.
+    if (warp >= 12) {
+        regs_release<80>();
+        if (warp == 12 && lane == 0) {
+            // ------------------------------------------------ TMA producer ---
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmDO);
-            const uint32_t kb = smem_u32(&bar_k_full), vb = smem_u32(&bar_v_full);
-            mbar_arrive_expect_tx(kb, TL::BYTES);
-            for (int cb = 0; cb < TL::NB; ++cb)
-                tma_load_4d(smem_u32(smem + C::OFF_K + cb * TL::BLOCK), &tmK, kb,
-                            cb * TL::BOX_COLS, j, s0, b);
-            mbar_arrive_expect_tx(vb, TL::BYTES);
-            for (int cb = 0; cb < TL::NB; ++cb)
-                tma_load_4d(smem_u32(smem + C::OFF_V + cb * TL::BLOCK), &tmV, vb,
-                            cb * TL::BOX_COLS, j, s0, b);
-            int issued = 0;
-            for (int i = 0; i < nitems; ++i) {
-                const int st = i % ST, u = i / ST;
-                if (u >= 1 && !mbar_wait(smem_u32(&bar_st_empty[st]), (u - 1) & 1, wc))
+            bool ok = true;
+            int gi = 0, k = 0;
+            for (; ok; ++k) {
+                const int u = snake_unit(k, cta, P);
+                if (u >= p.num_units)
                     break;
-                const int mt = n + i / p.G, h = j * p.G + i % p.G;
-                const uint32_t qb = smem_u32(&bar_q_full[st]), db = smem_u32(&bar_do_full[st]);
-                mbar_arrive_expect_tx(qb, TL::BYTES);
+                const DkvUnit w = dkv_unit(u, p);
+                const int kb = k % KB, ku = k / KB;
+                if (ku >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[kb]), (ku - 1) & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kbar = smem_u32(&bar_k_full[kb]), vbar = smem_u32(&bar_v_full[kb]);
+                mbar_arrive_expect_tx(kbar, TL::BYTES);
                 for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_Q + st * TL::BYTES + cb * TL::BLOCK), &tmQ,
-                                qb, cb * TL::BOX_COLS, h, mt * kRows, b);
-                mbar_arrive_expect_tx(db, TL::BYTES);
+                    tma_load_4d(smem_u32(smem + C::OFF_K + kb * TL::BYTES + cb * TL::BLOCK), &tmK,
+                                kbar, cb * TL::BOX_COLS, w.j, w.n * kRows, w.b);
+                mbar_arrive_expect_tx(vbar, TL::BYTES);
                 for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_DO + st * TL::BYTES + cb * TL::BLOCK),
-                                &tmDO, db, cb * TL::BOX_COLS, h, mt * kRows, b);
-                issued = i + 1;
-            }
-            if (*wc.abort) {
-                mbar_wait_drain(smem_u32(&bar_k_full), 0, wc.limit_ns);
-                mbar_wait_drain(smem_u32(&bar_v_full), 0, wc.limit_ns);
-                for (int i = (issued > ST ? issued - ST : 0); i < issued; ++i) {
-                    const int st = i % ST, u = i / ST;
-                    mbar_wait_drain(smem_u32(&bar_q_full[st]), u & 1, wc.limit_ns);
-                    mbar_wait_drain(smem_u32(&bar_do_full[st]), u & 1, wc.limit_ns);
+                    tma_load_4d(smem_u32(smem + C::OFF_V + kb * TL::BYTES + cb * TL::BLOCK), &tmV,
+                                vbar, cb * TL::BOX_COLS, w.j, w.n * kRows, w.b);
+                for (int it = 0; it < w.nitems; ++it, ++gi) {
+                    const int st = gi % ST, su = gi / ST;
+                    if (su >= 1 && !mbar_wait(smem_u32(&bar_st_empty[st]), (su - 1) & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const int mt = w.n + it / p.G, h = w.j * p.G + it % p.G;
+                    const uint32_t qb = smem_u32(&bar_q_full[st]), db = smem_u32(&bar_do_full[st]);
+                    mbar_arrive_expect_tx(qb, TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb)
+                        tma_load_4d(smem_u32(smem + C::OFF_Q + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmQ, qb, cb * TL::BOX_COLS, h, mt * kRows, w.b);
+                    mbar_arrive_expect_tx(db, TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb)
+                        tma_load_4d(smem_u32(smem + C::OFF_DO + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmDO, db, cb * TL::BOX_COLS, h, mt * kRows, w.b);
                 }
             }
-        }
-    } else if (warp == 9) {
-        if (lane == 0) {
+            if (*wc.abort) {
+                // Drain this CTA's own copies still in flight (each buffer's
+                // latest load), bounded, before the CTA exits.
+                for (int kk = (k > KB ? k - KB : 0); kk <= k && kk >= 0; ++kk) {
+                    const int kb = kk % KB, ku = kk / KB;
+                    mbar_wait_drain(smem_u32(&bar_k_full[kb]), ku & 1, wc.limit_ns);
+                    mbar_wait_drain(smem_u32(&bar_v_full[kb]), ku & 1, wc.limit_ns);
+                }
+                for (int g = (gi > ST ? gi - ST : 0); g < gi; ++g) {
+                    const int st = g % ST, su = g / ST;
+                    mbar_wait_drain(smem_u32(&bar_q_full[st]), su & 1, wc.limit_ns);
+                    mbar_wait_drain(smem_u32(&bar_do_full[st]), su & 1, wc.limit_ns);
+                }
+            }
+        } else if (warp == 13 || warp == 14) {
+            // -------------------------------------------------- MMA issuers ---
+            // Two warps issue independently so neither stream blocks the other:
+            // warp 13 issues S^T and dP^T as soon as an item's operands are in,
+            // warp 14 issues dV/dK as soon as the rows have written P^T / dS^T.
+            // Each warp runs its loop whole (warp-uniform descriptor math) and
+            // one elected lane issues.  The releases of K/V and Q/dO buffers are
+            // committed by warp 14 only: warp 13's MMAs on an item complete
+            // before s_full, which precedes the rows' pds_full for that item.
             constexpr uint32_t ID_S = idesc_f16(128, 128, false, false, false);
             constexpr uint32_t ID_DP = idesc_f16(128, 128, true, false, false);
             constexpr uint32_t ID_DV = idesc_f16(128, TL::NPV, true, false, true);
             constexpr uint32_t ID_DK = idesc_f16(128, TL::NPV, false, false, true);
-            const uint32_t k_addr = smem_u32(smem + C::OFF_K);
-            const uint32_t v_addr = smem_u32(smem + C::OFF_V);
-            const uint32_t q_addr = smem_u32(smem + C::OFF_Q);
-            const uint32_t do_addr = smem_u32(smem + C::OFF_DO);
-            const uint32_t pt_addr = smem_u32(smem + C::OFF_PT);
-            const uint32_t dst_addr = smem_u32(smem + C::OFF_DST);
-            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, wc) &&
-                      mbar_wait(smem_u32(&bar_v_full), 0, wc);
-            auto do_acc = [&](int x) -> bool {
-                const int stx = x % ST;
-                if (!mbar_wait(smem_u32(&bar_pds_full), x & 1, wc))
-                    return false;
-                tc_fence_after();
-                const uint32_t oa = do_addr + stx * TL::BYTES, qa = q_addr + stx * TL::BYTES;
+            constexpr uint32_t TSTEP = TL::BYTES >> 4;
+            const uint32_t sbase = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
+            const uint32_t tb = __shfl_sync(0xffffffffu, tbase, 0);
+            bool ok = true;
+            int gi = 0;
+            if (warp == 13) {
+                const uint64_t dK0 = desc_kmajor_base<D>(sbase + C::OFF_K);
+                const uint64_t dV0 = desc_kmajor_base<D>(sbase + C::OFF_V);
+                const uint64_t dQk0 = desc_kmajor_base<D>(sbase + C::OFF_Q);
+                const uint64_t dOk0 = desc_kmajor_base<D>(sbase + C::OFF_DO);
+                const uint32_t b_s_full = smem_u32(&bar_s_full);
+                const uint32_t b_s_empty = smem_u32(&bar_s_empty);
+                const uint32_t b_pds_empty = smem_u32(&bar_pds_empty);
+                for (int k = 0; ok; ++k) {
+                    const int u = snake_unit(k, cta, P);
+                    if (u >= p.num_units)
+                        break;
+                    const DkvUnit w = dkv_unit(u, p);
+                    const int kb = k % KB, ku = k / KB;
+                    if (!(mbar_wait_warp(smem_u32(&bar_k_full[kb]), ku & 1, wc) &&
+                          mbar_wait_warp(smem_u32(&bar_v_full[kb]), ku & 1, wc))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t kd = dK0 + kb * TSTEP, vd = dV0 + kb * TSTEP;
+                    for (int it = 0; it < w.nitems; ++it, ++gi) {
+                        const int st = gi % ST, su = gi / ST;
+                        if (!(mbar_wait_warp(smem_u32(&bar_q_ready[st]), su & 1, wc) &&
+                              mbar_wait_warp(smem_u32(&bar_do_full[st]), su & 1, wc))) {
+                            ok = false;
+                            break;
+                        }
+                        if (gi >= 1 && !mbar_wait_warp(b_s_empty, (gi - 1) & 1, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        // D = 128: P^T / dS^T live in S^T / dP^T's columns, so the
+                        // previous item's dV/dK must be done before S^T is rewritten.
+                        if (C::ALIAS && gi >= 1 &&
+                            !mbar_wait_warp(b_pds_empty, (gi - 1) & 1, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t qd = dQk0 + st * TSTEP, od = dOk0 + st * TSTEP;
+                        if (elect_one()) {
 #pragma unroll
-                for (int nc = 0; nc < D / TL::NPV; ++nc)
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_f16_ss(tb + C::COL_S, kd + kmajor_off<D>(kk),
+                                           qd + kmajor_off<D>(kk), ID_S, kk > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(tbase + 256 + nc * TL::NPV, desc_ptile(pt_addr, kk),
-                                   desc_mnmajor<D>(oa, nc, kk), ID_DV,
-                                   (x > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int nc = 0; nc < D / TL::NPV; ++nc)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(tbase + 256 + D + nc * TL::NPV, desc_ptile(dst_addr, kk),
-                                   desc_mnmajor<D>(qa, nc, kk), ID_DK,
-                                   (x > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(smem_u32(&bar_pds_empty));
-                mma_commit(smem_u32(&bar_st_empty[stx]));
-                return true;
-            };
-            for (int i = 0; ok && i < nitems; ++i) {
-                const int st = i % ST, u = i / ST;
-                if (!(mbar_wait(smem_u32(&bar_q_ready[st]), u & 1, wc) &&
-                      mbar_wait(smem_u32(&bar_do_full[st]), u & 1, wc))) {
-                    ok = false;
-                    break;
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_f16_ss(tb + C::COL_DP, vd + kmajor_off<D>(kk),
+                                           od + kmajor_off<D>(kk), ID_DP, kk > 0 ? 1u : 0u);
+                            mma_commit(b_s_full);
+                        }
+                        __syncwarp();
+                    }
                 }
-                if (i >= 1 && !mbar_wait(smem_u32(&bar_s_empty), (i - 1) & 1, wc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t qa = q_addr + st * TL::BYTES, oa = do_addr + st * TL::BYTES;
+            } else {
+                const uint64_t dQm0 = desc_mnmajor_base<D>(sbase + C::OFF_Q);
+                const uint64_t dOm0 = desc_mnmajor_base<D>(sbase + C::OFF_DO);
+                const uint32_t b_pds_full = smem_u32(&bar_pds_full);
+                const uint32_t b_pds_empty = smem_u32(&bar_pds_empty);
+                for (int k = 0; ok; ++k) {
+                    const int u = snake_unit(k, cta, P);
+                    if (u >= p.num_units)
+                        break;
+                    const DkvUnit w = dkv_unit(u, p);
+                    const int kb = k % KB;
+                    for (int it = 0; it < w.nitems; ++it, ++gi) {
+                        const int st = gi % ST;
+                        if (!mbar_wait_warp(b_pds_full, gi & 1, wc) ||
+                            (it == 0 && k >= 1 &&
+                             !mbar_wait_warp(smem_u32(&bar_acc_free), (k - 1) & 1, wc))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t om = dOm0 + st * TSTEP, qm = dQm0 + st * TSTEP;
+                        const uint32_t first = (it > 0) ? 1u : 0u;
+                        if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16_ss(tbase, desc_kmajor<D>(k_addr, kk), desc_kmajor<D>(qa, kk), ID_S,
-                               kk > 0 ? 1u : 0u);
+                            for (int nc = 0; nc < D / TL::NPV; ++nc)
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16_ss(tbase + 128, desc_kmajor<D>(v_addr, kk), desc_kmajor<D>(oa, kk),
-                               ID_DP, kk > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&bar_s_full));
-                // With two or more Q/dO stages, item i's S^T and dP^T are issued
-                // before item i-1's dV/dK so the tensor core overlaps the softmax
-                // work; with a single stage, item i's tile can only land after
-                // item i-1's dV/dK have released the stage, so they go in order.
-                const int acc_item = (ST >= 2) ? i - 1 : i;
-                if (acc_item >= 0 && !do_acc(acc_item)) {
-                    ok = false;
-                    break;
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_f16_ts(tb + C::COL_DV + nc * TL::NPV,
+                                               tb + C::col_p(kk >> 2) + 8 * (kk & 3),
+                                               om + mnmajor_off<D>(nc, kk), ID_DV,
+                                               kk > 0 ? 1u : first);
+#pragma unroll
+                            for (int nc = 0; nc < D / TL::NPV; ++nc)
+#pragma unroll
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_f16_ts(tb + C::COL_DK + nc * TL::NPV,
+                                               tb + C::col_ds(kk >> 2) + 8 * (kk & 3),
+                                               qm + mnmajor_off<D>(nc, kk), ID_DK,
+                                               kk > 0 ? 1u : first);
+                            mma_commit(b_pds_empty);
+                            mma_commit(smem_u32(&bar_st_empty[st]));
+                            if (it == w.nitems - 1) {
+                                mma_commit(smem_u32(&bar_acc_done));
+                                mma_commit(smem_u32(&bar_kv_empty[kb]));
+                            }
+                        }
+                        __syncwarp();
+                    }
                 }
             }
-            if (ok && (ST == 1 || do_acc(nitems - 1)))
-                mma_commit(smem_u32(&bar_acc_done));
-            mma_commit(smem_u32(&bar_drain));
-            mbar_wait(smem_u32(&bar_drain), 0, wc);
-        }
-    } else if (warp >= 4) {
-        const int r = threadIdx.x - 128;
-        float mx = 0.f;
-        bool ok = mbar_wait_warp(smem_u32(&bar_k_full), 0, wc);
-        if (ok) {
-            mx = rope_row_to_f16<D>(smem + C::OFF_K, r, static_cast<uint32_t>(s0 + r), p.rope);
-            fence_proxy_async_smem();
+            // Drain: each issuing warp's MMAs complete before TMEM is freed.
+            if (elect_one())
+                mma_commit(smem_u32(&bar_drain));
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_k_ready));
-            for (int i = 0; i < nitems; ++i) {
-                const int st = i % ST, u = i / ST;
-                const int mt = n + i / p.G;
-                if (!mbar_wait_warp(smem_u32(&bar_q_full[st]), u & 1, wc))
+            mbar_wait_warp(smem_u32(&bar_drain), 0, wc);
+        }
+        teardown();
+        return;
+    } else if (warp >= 8) {
+        // ---------------------------------------- lse / D staging ---
+        regs_release<56>();
+        const int r = threadIdx.x - 256;
+        bool ok = true;
+        int gi = 0;
+        float mx = 0.f;
+        for (int k = 0; ok; ++k) {
+            const int u = snake_unit(k, cta, P);
+            if (u >= p.num_units)
+                break;
+            const DkvUnit w = dkv_unit(u, p);
+            // lse and D of the item's queries are fetched one item ahead so the
+            // global-load latency overlaps the wait for the previous item.
+            auto fetch = [&](int it, float &l, float &dd) {
+                const int mt = w.n + it / p.G, h = w.j * p.G + it % p.G;
+                const int t = mt * kRows + r;
+                l = INFINITY;
+                dd = 0.f;
+                if (t < p.T) {
+                    const size_t idx = (static_cast<size_t>(w.b) * p.Hq + h) * p.T + t;
+                    l = p.lse[idx];
+                    dd = p.Dws[idx];
+                }
+            };
+            float nl, nd;
+            fetch(0, nl, nd);
+            for (int it = 0; it < w.nitems; ++it, ++gi) {
+                const int st = gi % ST, su = gi / ST;
+                const float l2 = nl * kLog2e, dd = nd;
+                if (it + 1 < w.nitems)
+                    fetch(it + 1, nl, nd);
+                // The stage's previous item is finished once the TMA has refilled
+                // it, so its lse/D slots can be overwritten.
+                if (!mbar_wait_warp(smem_u32(&bar_q_full[st]), su & 1, wc)) {
+                    ok = false;
                     break;
-                mx = fmaxf(mx, rope_row_to_f16<D>(smem + C::OFF_Q + st * TL::BYTES, r,
-                                                  static_cast<uint32_t>(mt * kRows + r), p.rope));
-                fence_proxy_async_smem();
+                }
+                lsed[st * kRows + r] = make_float2(l2, dd);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_q_ready[st]));
@@ -652,120 +969,133 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (mx > kFp16Max)
             atomicOr(p.status, kDevRange);
+        teardown();
+        return;
     } else {
-        const int r = threadIdx.x;            // key row == TMEM lane
-        const int s = s0 + r;
-        const uint32_t lane_base = tmem_addr(tbase, warp * 32, 0);
-        auto fetch = [&](int i, float &l2, float &dd) {
-            const int mt = n + i / p.G, h = j * p.G + i % p.G;
-            const int t = mt * kRows + r;
-            const size_t idx = (static_cast<size_t>(b) * p.Hq + h) * p.T + t;
-            l2 = (t < p.T) ? p.lse[idx] * kLog2e : INFINITY;
-            dd = (t < p.T) ? p.Dws[idx] : 0.f;
-        };
-        float nl2, ndd;
-        fetch(0, nl2, ndd);
+        // ---------------------------------------------- row warpgroups ---
+        regs_claim<184>();
+        const int w = warp >> 2;                // column half of the score tile
+        const int r = threadIdx.x & 127;        // key row == TMEM lane
+        const uint32_t lane_base = tmem_addr(tbase, (warp & 3) * 32, 0);
         float maxds = 0.f;
         bool ok = true;
-        uint8_t *pt = smem + C::OFF_PT;
-        uint8_t *dst = smem + C::OFF_DST;
-        for (int i = 0; i < nitems; ++i) {
-            const int mt = n + i / p.G;
-            lsed[i % 2][r] = make_float2(nl2, ndd);
-            if (i + 1 < nitems)
-                fetch(i + 1, nl2, ndd);
-            // Every warp passes this barrier once per item, also after an
-            // abort (a failed warp keeps looping without work), so no warp is
-            // ever left waiting here.
-            named_bar_sync(1, 128);
+        int gi = 0;
+        for (int k = 0; ok; ++k) {
+            const int u = snake_unit(k, cta, P);
+            if (u >= p.num_units)
+                break;
+            const DkvUnit un = dkv_unit(u, p);
+            for (int it = 0; it < un.nitems; ++it, ++gi) {
+                const int st = gi % ST, su = gi / ST;
+                const int mt = un.n + it / p.G;
+                if (!mbar_wait_warp(smem_u32(&bar_q_ready[st]), su & 1, wc) ||
+                    !mbar_wait_warp(smem_u32(&bar_s_full), gi & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sv[2][32], pv[2][32];
+                tmem_ld32(lane_base + C::COL_S + 64 * w, sv[0]);
+                tmem_ld32(lane_base + C::COL_S + 64 * w + 32, sv[1]);
+                tmem_ld32(lane_base + C::COL_DP + 64 * w, pv[0]);
+                tmem_ld32(lane_base + C::COL_DP + 64 * w + 32, pv[1]);
+                tmem_ld_wait_only();
+                tmem_tie(sv[0]);
+                tmem_tie(sv[1]);
+                tmem_tie(pv[0]);
+                tmem_tie(pv[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_s_empty));
+
+                const float4 *ld4 = reinterpret_cast<const float4 *>(lsed + st * kRows + 64 * w);
+                uint32_t pp[32], dk[32];
+                const float sl2 = p.scale_log2;
+                if (mt != un.n) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float4 a = ld4[(32 * h + e) >> 1];   // (l2, D) of 2 columns
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -a.x));
+                            const float p1 =
+                                ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -a.z));
+                            const float d0 = p0 * (__uint_as_float(pv[h][e]) - a.y);
+                            const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - a.w);
+                            maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
+                            pp[16 * h + e / 2] = pack_bf16x2(p0, p1);
+                            dk[16 * h + e / 2] = pack_f16x2(d0, d1);
+                        }
+                } else {
+                    // diagonal tile: query column c < key row r is masked
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int c = 64 * w + 32 * h + e;
+                            const float4 a = ld4[(32 * h + e) >> 1];
+                            float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -a.x));
+                            float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -a.z));
+                            p0 = (c < r) ? 0.f : p0;
+                            p1 = (c + 1 < r) ? 0.f : p1;
+                            const float d0 = p0 * (__uint_as_float(pv[h][e]) - a.y);
+                            const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - a.w);
+                            maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
+                            pp[16 * h + e / 2] = pack_bf16x2(p0, p1);
+                            dk[16 * h + e / 2] = pack_f16x2(d0, d1);
+                        }
+                }
+                if (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_pds_empty), (gi - 1) & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st32(lane_base + C::col_p(w), pp);
+                tmem_st32(lane_base + C::col_ds(w), dk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_pds_full));
+            }
             if (!ok)
-                continue;
-            if (!mbar_wait_warp(smem_u32(&bar_s_full), i & 1, wc)) {
+                break;
+            // ---- unit epilogue: dV (warpgroup 0) and dK (warpgroup 1) ----
+            if (!mbar_wait_warp(smem_u32(&bar_acc_done), k & 1, wc)) {
                 ok = false;
-                continue;
+                break;
             }
             tc_fence_after();
-            if (i >= 1 && !mbar_wait_warp(smem_u32(&bar_pds_empty), (i - 1) & 1, wc)) {
-                ok = false;
-                continue;
+            const int s = un.n * kRows + r;
+            const size_t rowoff = ((static_cast<size_t>(un.b) * p.T + s) * p.Hkv + un.j) * D;
+            if (w == 0) {
+                __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.out1) + rowoff;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t a[32];
+                    tmem_ld32(lane_base + C::COL_DV + cc * 32, a);
+                    tmem_ld_wait(a);
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        x[e] = __uint_as_float(a[e]);
+                    if (s < p.T)
+                        store_row32_bf16(dv + cc * 32, x);
+                }
+            } else {
+                __nv_bfloat16 *dkp = static_cast<__nv_bfloat16 *>(p.out0) + rowoff;
+                epilogue_inverse_rope<D>(lane_base + C::COL_DK, p.scale, static_cast<uint32_t>(s),
+                                         p.rope, dkp, s < p.T);
             }
-            const bool diag = (mt == n);
-            const float2 *ld = lsed[i % 2];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sv[32], pv[32];
-                tmem_ld32(lane_base + cc * 32, sv);
-                tmem_ld32(lane_base + 128 + cc * 32, pv);
-                tmem_ld_wait(sv);
-                tmem_tie(pv);
-                if (cc == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&bar_s_empty));
-                }
-                uint32_t pp[16], dk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int c = cc * 32 + e;
-                    const float2 a0 = ld[c], a1 = ld[c + 1];
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -a0.x));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -a1.x));
-                    if (diag && c < r)
-                        p0 = 0.f;
-                    if (diag && c + 1 < r)
-                        p1 = 0.f;
-                    const float d0 = p0 * (__uint_as_float(pv[e]) - a0.y);
-                    const float d1 = p1 * (__uint_as_float(pv[e + 1]) - a1.y);
-                    maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
-                    pp[e / 2] = pack_bf16x2(p0, p1);
-                    dk[e / 2] = pack_f16x2(d0, d1);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t off = ptile_chunk(r, cc * 4 + q);
-                    *reinterpret_cast<uint4 *>(pt + off) =
-                        make_uint4(pp[4 * q], pp[4 * q + 1], pp[4 * q + 2], pp[4 * q + 3]);
-                    *reinterpret_cast<uint4 *>(dst + off) =
-                        make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
-                }
-            }
-            fence_proxy_async_smem();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_u32(&bar_pds_full));
+                mbar_arrive(smem_u32(&bar_acc_free));
         }
         if (maxds > kFp16Max)
             atomicOr(p.status, kDevRange);
-        if (ok)
-            ok = mbar_wait_warp(smem_u32(&bar_acc_done), 0, wc);
-        if (ok) {
-            tc_fence_after();
-            const size_t rowoff = ((static_cast<size_t>(b) * p.T + s) * p.Hkv + j) * D;
-            __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.out1) + rowoff;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t a[32];
-                tmem_ld32(lane_base + 256 + cc * 32, a);
-                tmem_ld_wait(a);
-                float x[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    x[e] = __uint_as_float(a[e]);
-                if (s < p.T)
-                    store_row32_bf16(dv + cc * 32, x);
-            }
-            __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(p.out0) + rowoff;
-            epilogue_inverse_rope<D>(lane_base + 256 + D, p.scale, static_cast<uint32_t>(s),
-                                     p.rope, dk, s < p.T);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 9) {
-        tc_fence_after();
-        tmem_dealloc(tbase, C::TMEM_COLS);
+        teardown();
     }
 }
 
@@ -773,7 +1103,7 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, int GC, int ST>
 static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
+                               const CUtensorMap &dO, const AttnParams &p0, cudaStream_t stream)
 {
     using C = DqCfg<D, GC, ST>;
     auto kern = dq_kernel<D, GC, ST>;
@@ -781,8 +1111,14 @@ static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
         return e;
-    const unsigned grid = static_cast<unsigned>(p.M) * p.B * p.Hkv * p.nchunks;
-    kern<<<grid, 320, C::SMEM_BYTES, stream>>>(q, k, v, dO, p);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    AttnParams p = p0;
+    p.num_units = p.M * p.B * p.Hkv * p.nchunks;
+    const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
+    kern<<<grid, 384, C::SMEM_BYTES, stream>>>(q, k, v, dO, p);
     return cudaGetLastError();
 }
 
@@ -792,19 +1128,18 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, con
     switch (d) {
     case 32:
         switch (p.GC) {
-        case 1: return launch_dq_t<32, 1, 2>(q, k, v, dO, p, stream);
-        case 2: return launch_dq_t<32, 2, 2>(q, k, v, dO, p, stream);
-        case 3: return launch_dq_t<32, 3, 2>(q, k, v, dO, p, stream);
-        case 4: return launch_dq_t<32, 4, 2>(q, k, v, dO, p, stream);
+        case 1: return launch_dq_t<32, 1, 4>(q, k, v, dO, p, stream);
+        case 2: return launch_dq_t<32, 2, 4>(q, k, v, dO, p, stream);
+        case 3: return launch_dq_t<32, 3, 4>(q, k, v, dO, p, stream);
+        case 4: return launch_dq_t<32, 4, 4>(q, k, v, dO, p, stream);
         default: break;
         }
         break;
     case 64:
         switch (p.GC) {
-        case 1: return launch_dq_t<64, 1, 2>(q, k, v, dO, p, stream);
-        case 2: return launch_dq_t<64, 2, 2>(q, k, v, dO, p, stream);
-        case 3: return launch_dq_t<64, 3, 2>(q, k, v, dO, p, stream);
-        case 4: return launch_dq_t<64, 4, 2>(q, k, v, dO, p, stream);
+        case 1: return launch_dq_t<64, 1, 3>(q, k, v, dO, p, stream);
+        case 2: return launch_dq_t<64, 2, 3>(q, k, v, dO, p, stream);
+        case 3: return launch_dq_t<64, 3, 3>(q, k, v, dO, p, stream);
         default: break;
         }
         break;
@@ -819,7 +1154,7 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, con
 
 template <int D, int ST>
 static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                 const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
+                                 const CUtensorMap &dO, const AttnParams &p0, cudaStream_t stream)
 {
     using C = DkvCfg<D, ST>;
     auto kern = dkdv_kernel<D, ST>;
@@ -827,8 +1162,14 @@ static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, con
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
         return e;
-    const unsigned grid = static_cast<unsigned>(p.M) * p.B * p.Hkv;
-    kern<<<grid, 320, C::SMEM_BYTES, stream>>>(q, k, v, dO, p);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    AttnParams p = p0;
+    p.num_units = p.M * p.B * p.Hkv;
+    const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
+    kern<<<grid, 512, C::SMEM_BYTES, stream>>>(q, k, v, dO, p);
     return cudaGetLastError();
 }
 
@@ -837,8 +1178,8 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,
                             cudaStream_t stream)
 {
     switch (d) {
-    case 32: return launch_dkdv_t<32, 2>(q, k, v, dO, p, stream);
-    case 64: return launch_dkdv_t<64, 2>(q, k, v, dO, p, stream);
+    case 32: return launch_dkdv_t<32, 4>(q, k, v, dO, p, stream);
+    case 64: return launch_dkdv_t<64, 4>(q, k, v, dO, p, stream);
     case 128: return launch_dkdv_t<128, 1>(q, k, v, dO, p, stream);
     default: return cudaErrorInvalidValue;
     }

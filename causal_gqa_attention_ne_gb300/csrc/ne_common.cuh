@@ -143,6 +143,73 @@ __device__ __forceinline__ float rope_row_to_f16(uint8_t *tile, int r, uint32_t 
     return mx;
 }
 
+// ---- table-driven RoPE (no special-function unit work per element) ----
+//
+// A CTA keeps float2 tab[j][r] = (cos, sin)(r * theta_j) for the 128 rows r
+// of a tile and the D/2 frequencies j, and per rotated tile the 64 values
+// base[j] = (cos, sin)(p0 * theta_j) of the tile's first position p0.  The
+// angle of row r is p0*theta_j + r*theta_j; its cosine and sine come from the
+// angle-addition formulas (four multiply-adds).  Both tables come from the
+// hardware sine/cosine on the exactly reduced angle in [-pi, pi), where its
+// absolute error is below 4e-7 (far below the fp16 rounding of the result).
+
+__device__ __forceinline__ float2 rope_cs(uint32_t pos, uint32_t f)
+{
+    float s, c;
+    rope_sincos(pos, f, s, c);
+    return make_float2(c, s);
+}
+
+// Thread r (0..127) fills row r of the table.
+template <int D>
+__device__ __forceinline__ void rope_table_fill(float2 *tab, int r, const RopeFreqs &fr)
+{
+#pragma unroll 4
+    for (int j = 0; j < D / 2; ++j)
+        tab[j * kRows + r] = rope_cs(static_cast<uint32_t>(r), fr.turn[j]);
+}
+
+// Rotate row r of a bf16 tile in place to fp16 using the table and the
+// tile's base; returns the largest |x'| (fp16 range check).
+template <int D>
+__device__ __forceinline__ float rope_row_table(uint8_t *tile, int r, const float2 *tab,
+                                                const float2 *base)
+{
+    constexpr int HC = D / 16;
+    float mx = 0.f;
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        uint4 *pa = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c));
+        uint4 *pb = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c + HC));
+        const uint4 a = *pa, b = *pb;
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+        uint32_t ao[4], bo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float u[2], w[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = 8 * c + 2 * e + h;
+                const float2 t = tab[j * kRows + r];
+                const float2 bs = base[j];
+                const float cs = bs.x * t.x - bs.y * t.y;
+                const float sn = bs.y * t.x + bs.x * t.y;
+                const float x = h ? bf16_hi(av[e]) : bf16_lo(av[e]);
+                const float y = h ? bf16_hi(bv[e]) : bf16_lo(bv[e]);
+                u[h] = x * cs - y * sn;
+                w[h] = y * cs + x * sn;
+                mx = fmaxf(mx, fmaxf(fabsf(u[h]), fabsf(w[h])));
+            }
+            ao[e] = pack_f16x2(u[0], u[1]);
+            bo[e] = pack_f16x2(w[0], w[1]);
+        }
+        *pa = make_uint4(ao[0], ao[1], ao[2], ao[3]);
+        *pb = make_uint4(bo[0], bo[1], bo[2], bo[3]);
+    }
+    return mx;
+}
+
 // Inverse rotation (by -angle) of a pair of fp32 values held in registers.
 __device__ __forceinline__ void rope_inverse_pair(float &x, float &y, uint32_t pos, uint32_t f)
 {
@@ -172,6 +239,40 @@ inline cudaError_t ensure_smem_attr(Kernel kern, int bytes, bool (&done)[64])
     return e;
 }
 
+// Descriptor offsets (in the descriptor's 16-byte address units) of the K
+// step kk of a K-major D-wide tile, and of (N chunk nc, K step kk) of an
+// MN-major one, relative to the tile's base descriptor.  Compile-time
+// constants, so each MMA needs one add.
+template <int D>
+__host__ __device__ constexpr uint32_t kmajor_off(int kk)
+{
+    return static_cast<uint32_t>(((kk * 32) / Tile<D>::SWB * Tile<D>::BLOCK +
+                                  (kk * 32) % Tile<D>::SWB) >> 4);
+}
+template <int D>
+__host__ __device__ constexpr uint32_t mnmajor_off(int nc, int kk)
+{
+    return static_cast<uint32_t>((nc * Tile<D>::BLOCK + kk * 16 * Tile<D>::SWB) >> 4);
+}
+template <int D>
+__device__ __forceinline__ uint64_t desc_kmajor_base(uint32_t tile_addr)
+{
+    return smem_desc(tile_addr, 16, 8 * Tile<D>::SWB, Tile<D>::LAYOUT);
+}
+template <int D>
+__device__ __forceinline__ uint64_t desc_mnmajor_base(uint32_t tile_addr)
+{
+    return smem_desc(tile_addr, 8 * Tile<D>::SWB, 8 * Tile<D>::SWB, Tile<D>::LAYOUT);
+}
+
+// Persistent-CTA work order: CTA c of P takes units c, 2P-1-c, 2P+c, 4P-1-c,
+// ... (a snake over a list sorted by decreasing cost), which balances the
+// causal work across CTAs without any shared counter.
+__device__ __forceinline__ int snake_unit(int k, int c, int P)
+{
+    return (k & 1) ? k * P + (P - 1 - c) : k * P + c;
+}
+
 // Launch parameters (everything except the TMA descriptors).
 struct AttnParams {
     int B, T, Hq, Hkv, G, M;     // M = number of 128-row tiles along T
@@ -185,6 +286,7 @@ struct AttnParams {
     float *lse;                  // forward: written; backward: read
     float *Dws;                  // backward: D = rowsum(dO * O), [B][Hq][T]
     uint32_t *status;            // device status word
+    int num_units;               // persistent kernels: work units in the launch
     uint64_t wait_limit_ns;
     RopeFreqs rope;
 };

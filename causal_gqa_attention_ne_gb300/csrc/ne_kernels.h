@@ -12,15 +12,17 @@ namespace ne {
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const AttnParams &p, cudaStream_t stream);
 
-// Backward preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c].
-cudaError_t launch_bwd_pre(int d, const AttnParams &p, cudaStream_t stream);
+// Backward preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c], and the
+// rotated Q' = R(t) q, K' = R(s) k as fp16 (same layouts) into qrot / krot.
+cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot, const void *k,
+                           void *krot, cudaStream_t stream);
 
 // Backward dQ (query-tile major, recomputes S and dP).
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                           const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream);
 
 // Backward dK, dV (key-tile major; dK and dV summed over the query heads of
-// each KV head inside the CTA).
+// each KV head inside the CTA).  `q` and `k` are the fp16 rotated Q' / K' maps.
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,
                             const CUtensorMap &v, const CUtensorMap &dO, const AttnParams &p,
                             cudaStream_t stream);

@@ -78,8 +78,10 @@ int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse
                 int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
 
 /*
- * Bytes of device workspace ne_attn_bwd needs for this shape (the per-row
- * dO.O dot products D, fp32 [B][Hq][T], rounded up to 256 bytes).
+ * Bytes of device workspace ne_attn_bwd needs for this shape: the per-row
+ * dO.O dot products D (fp32 [B][Hq][T]), the rotated queries Q' = R(t) q
+ * (fp16 [B][T][Hq][d]) and the rotated keys K' = R(s) k (fp16
+ * [B][T][Hkv][d]), each rounded up to 256 bytes.
  * Returns 0 for a shape ne_attn_bwd would reject.
  */
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d);
@@ -106,16 +108,17 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
  * ne_attn_bwd; `workspace` carries D from the preprocess to the other two.
  *
  * ne_attn_bwd_preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c] in fp32
- *   (the row dot product the backward of a softmax needs), written into the
- *   workspace.
+ *   (the row dot product the backward of a softmax needs) and the rotated
+ *   Q' = R(t) q and K' = R(s) k in fp16, all written into the workspace.
  * ne_attn_bwd_dq: dq from q, k, v, lse, dO and D (query-tile major: recomputes
  *   the scores and dP = dO v^T per key tile; dq = R(t)^T sum_s dS k' / sqrt(d)).
- * ne_attn_bwd_dkdv: dk and dv from the same inputs (key-tile major: dk and dv
- *   summed over the query heads of each key/value head inside one CTA).
+ * ne_attn_bwd_dkdv: dk and dv from v, lse, dO and the workspace's D, Q', K'
+ *   (key-tile major: dk and dv summed over the query heads of each key/value
+ *   head inside one CTA); `q` and `k` are validated, the kernel reads Q', K'.
  */
-int ne_attn_bwd_preprocess(const void *o, const void *dO, void *workspace,
-                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
-                           void *stream);
+int ne_attn_bwd_preprocess(const void *q, const void *k, const void *o, const void *dO,
+                           void *workspace, size_t workspace_bytes, int B, int T, int Hq,
+                           int Hkv, int d, float rope_theta, void *stream);
 int ne_attn_bwd_dq(const void *q, const void *k, const void *v, const float *lse,
                    const void *dO, void *dq, const void *workspace, size_t workspace_bytes,
                    int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream);

@@ -155,7 +155,7 @@ def test_substeps_match_full_backward(d):
     ws = torch.empty(ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8,
                      device="cuda")
     dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
-    ne.ne_attn_bwd_preprocess(o, xd["do"], ws)
+    ne.ne_attn_bwd_preprocess(xd["q"], xd["k"], o, xd["do"], ws, THETA)
     ne.ne_attn_bwd_dkdv(xd["q"], xd["k"], xd["v"], lse, xd["do"], dk2, dv2, ws, THETA)
     ne.ne_attn_bwd_dq(xd["q"], xd["k"], xd["v"], lse, xd["do"], dq2, ws, THETA)
     torch.cuda.synchronize()
