@@ -17,12 +17,13 @@ from . import _build
 NE_STATUS = {
     0: "NE_OK", 1: "NE_ERR_NULL", 2: "NE_ERR_SHAPE", 3: "NE_ERR_UNSUPPORTED", 4: "NE_ERR_ALIGN",
     5: "NE_ERR_WORKSPACE", 6: "NE_ERR_CUDA", 7: "NE_ERR_TIMEOUT", 8: "NE_ERR_RANGE",
-    9: "NE_ERR_ARG",
+    9: "NE_ERR_ARG", 10: "NE_ERR_TOO_LARGE",
 }
 
 EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn_bwd_preprocess",
             "ne_attn_bwd_dq", "ne_attn_bwd_dkdv", "ne_attn_get_error", "ne_attn_status_string",
-            "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout")
+            "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout", "ne_attn_bwd_noalloc",
+            "ne_attn_bwd_noalloc_max_scratch")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,10 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_set_wait_limit_ns.restype = None
         lib.ne_attn_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.ne_attn_selftest_timeout.restype = i
+        lib.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_noalloc.restype = i
+        lib.ne_attn_bwd_noalloc_max_scratch.argtypes = []
+        lib.ne_attn_bwd_noalloc_max_scratch.restype = sz
         _lib = lib
         return lib
 
@@ -202,6 +207,29 @@ def ne_attn_bwd_dkdv(q, k, v, lse, do, dk, dv, workspace, rope_theta: float = 10
                                          Hkv, d, float(rope_theta), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd_dkdv")
+
+
+def ne_attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, rope_theta: float = 10000.0,
+                        stream=None) -> None:
+    """Backward into caller-allocated dq, dk, dv without any workspace: the
+    library's fixed scratch array stands in for it (see ne_attn.h for its size
+    limit and for why concurrent calls on one device must be serialised)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    rc = load_library().ne_attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, T, Hq,
+                                            Hkv, d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_noalloc")
+
+
+def ne_attn_bwd_noalloc_max_scratch() -> int:
+    return int(load_library().ne_attn_bwd_noalloc_max_scratch())
 
 
 def ne_attn_get_error(stream=None) -> int:

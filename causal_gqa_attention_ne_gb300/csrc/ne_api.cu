@@ -428,6 +428,8 @@ const char *ne_attn_status_string(int status)
     case NE_ERR_TIMEOUT: return "a device-side bounded wait ran out";
     case NE_ERR_RANGE: return "an fp16 tensor-core operand exceeded 65504";
     case NE_ERR_ARG: return "invalid argument (rope_theta must be finite and > 0)";
+    case NE_ERR_TOO_LARGE:
+        return "shape needs more scratch than ne_attn_bwd_noalloc's fixed buffer holds";
     default: return "unknown status";
     }
 }
@@ -446,6 +448,68 @@ int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream)
     cudaError_t e = ne::launch_timeout_selftest(status, limit_ns ? limit_ns : 1,
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // extern "C"
+
+// ------------------------------------------------------------------------
+// Backward without any allocation.  Its scratch (the D rows and the rotated
+// Q'/K' that ne_attn_bwd keeps in the caller's workspace) lives in one fixed
+// array that is part of this library's device image, so every GPU that
+// loads the library holds it until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;   // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (cudaGetSymbolAddress with that device current).
+int noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return NE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            return NE_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return NE_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+size_t ne_attn_bwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+int ne_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dO, void *dq, void *dk, void *dv, int B,
+                        int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
+    if (rc != NE_OK)
+        return rc;
+    if (ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d) > kNoAllocScratchBytes)
+        return NE_ERR_TOO_LARGE;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    void *scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != NE_OK)
+        return rc;
+    // Every part of the scratch the kernels read is written earlier in the same
+    // call, so nothing has to be cleared between calls.
+    return ne_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, scratch, kNoAllocScratchBytes, B, T, Hq,
+                       Hkv, d, rope_theta, stream);
 }
 
 } // extern "C"

@@ -65,7 +65,8 @@ typedef enum {
     NE_ERR_CUDA = 6,        /* a CUDA runtime / driver call or a launch failed */
     NE_ERR_TIMEOUT = 7,     /* a device-side bounded wait ran out (reported by get_error) */
     NE_ERR_RANGE = 8,       /* an fp16 tensor-core operand overflowed (reported by get_error) */
-    NE_ERR_ARG = 9          /* another invalid argument (rope_theta <= 0, NaN, ...) */
+    NE_ERR_ARG = 9,         /* another invalid argument (rope_theta <= 0, NaN, ...) */
+    NE_ERR_TOO_LARGE = 10   /* ne_attn_bwd_noalloc: shape exceeds its fixed scratch */
 } ne_status;
 
 /*
@@ -153,6 +154,38 @@ void ne_attn_set_wait_limit_ns(uint64_t limit_ns);
  * ne_attn_get_error(stream) must then report NE_ERR_TIMEOUT.
  */
 int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * Backward that allocates nothing and takes no workspace.  (This entry point
+ * has no counterpart on the pages; it exists for callers of this library.)
+ *
+ * Who needs it: callers that cannot call cudaMalloc -- code that runs with all
+ * device memory already claimed by another allocator (a framework's caching
+ * allocator, a fixed per-process memory budget) where a new allocation could
+ * fail or fragment, and callers whose own interface gives them no place to
+ * pass a workspace pointer through.
+ *
+ * Same arguments, results and errors as ne_attn_bwd, minus the workspace.
+ * The scratch ne_attn_bwd keeps in the workspace (D, Q', K') lives instead in
+ * one fixed device array of ne_attn_bwd_noalloc_max_scratch() bytes (32 MiB)
+ * compiled into the library: every GPU that loads the library holds it until
+ * the process exits.  Shapes whose ne_attn_bwd_workspace_size exceeds that
+ * return NE_ERR_TOO_LARGE and launch nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array: calls that can overlap on the GPU
+ * (different streams, or different host threads, on the same device) race on
+ * it and must be serialised by the caller.  The array keeps the last call's
+ * contents; every byte a call reads is written earlier in that same call, so
+ * nothing needs clearing.  No memory is allocated or freed by this call.
+ */
+int ne_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dO, void *dq, void *dk, void *dv, int B,
+                        int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+
+/* Size in bytes of ne_attn_bwd_noalloc's fixed scratch array. */
+size_t ne_attn_bwd_noalloc_max_scratch(void);
 
 #ifdef __cplusplus
 }
