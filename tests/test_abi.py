@@ -1,0 +1,92 @@
+"""The C-ABI library on the host: it loads, exports every entry point
+include/ne_attn.h declares, and rejects bad arguments before any device work
+(so these run without a GPU).  CPU only."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import causal_gqa_attention_ne_gb300 as ne
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ne_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ne_attn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ne.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size",
+                     "ne_attn_get_error", "ne_attn_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    exported = subprocess.run(["nm", "-D", "--defined-only", ne.lib_path()],
+                              capture_output=True, text=True, check=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}$", exported, re.M), f"{n} not exported"
+        assert hasattr(lib, n)
+    assert set(ne._binding.EXPORTED) == set(names)
+
+
+def test_status_strings(lib):
+    for code in range(11):
+        s = ne.ne_attn_status_string(code)
+        assert s and s != "unknown status"
+    assert ne.ne_attn_status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    # D (fp32 B*Hq*T) + Q' (fp16 B*T*Hq*d) + K' (fp16 B*T*Hkv*d), 256-aligned each
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for (B, T, Hq, Hkv, d) in ((1, 128, 4, 2, 32), (16, 512, 12, 4, 64), (4, 4096, 16, 4, 128),
+                               (3, 7, 5, 1, 64)):
+        want = r256(B * Hq * T * 4) + r256(B * T * Hq * d * 2) + r256(B * T * Hkv * d * 2)
+        assert ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d) == want
+    assert ne.ne_attn_bwd_workspace_size(1, 8, 3, 2, 64) == 0      # Hq % Hkv != 0
+    assert ne.ne_attn_bwd_workspace_size(1, 8, 2, 2, 48) == 0      # unsupported d
+
+
+def _fwd(lib, ptrs, B=1, T=8, Hq=2, Hkv=2, d=64, theta=10000.0):
+    return lib.ne_attn_fwd(*ptrs, B, T, Hq, Hkv, d, theta, None)
+
+
+def test_forward_argument_errors(lib):
+    buf = ctypes.create_string_buffer(4096 + 64)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    ok = [a, a, a, a, a]
+    assert _fwd(lib, [None, a, a, a, a]) == 1                       # NE_ERR_NULL
+    assert _fwd(lib, ok, B=0) == 2                                  # NE_ERR_SHAPE
+    assert _fwd(lib, ok, Hq=3, Hkv=2) == 2                          # Hq % Hkv
+    assert _fwd(lib, ok, d=48) == 3                                 # NE_ERR_UNSUPPORTED
+    assert _fwd(lib, ok, theta=0.0) == 9                            # NE_ERR_ARG
+    assert _fwd(lib, ok, theta=float("nan")) == 9
+    assert _fwd(lib, [a + 2, a, a, a, a]) == 4                      # NE_ERR_ALIGN
+
+
+def test_backward_argument_errors(lib):
+    buf = ctypes.create_string_buffer(4096)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    args = [a] * 9
+    # short workspace
+    assert lib.ne_attn_bwd(*args, a, 0, 1, 8, 2, 2, 64, 10000.0, None) == 5
+    # null gradient
+    assert lib.ne_attn_bwd(*args[:6], None, a, a, a, 1 << 20, 1, 8, 2, 2, 64, 10000.0,
+                           None) == 1
+    # no-allocation variant: shape whose scratch exceeds its fixed buffer
+    assert lib.ne_attn_bwd_noalloc(*args, 8, 4096, 8, 8, 128, 10000.0, None) == 10
+    assert lib.ne_attn_bwd_noalloc(*args, 1, 8, 3, 2, 64, 10000.0, None) == 2
