@@ -141,18 +141,6 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
     return cudaGetLastError();
 }
 
-// Stores 32 consecutive fp32 values as bf16 (64 bytes).
-__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16 *dst, const float *v)
-{
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        d4[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
-                           pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                           pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
-                           pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-}
-
 // Epilogue for a gradient of a rotated operand: reads the D fp32 columns of
 // this thread's TMEM row at `col`, multiplies by `scale`, rotates back by
 // -angle(pos) and stores bf16 to dst (when `store`).

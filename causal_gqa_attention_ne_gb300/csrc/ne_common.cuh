@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "sm103_ptx.cuh"
@@ -208,6 +209,68 @@ __device__ __forceinline__ float rope_row_table(uint8_t *tile, int r, const floa
         *pb = make_uint4(bo[0], bo[1], bo[2], bo[3]);
     }
     return mx;
+}
+
+// Rotate row r of a bf16 tile in place to fp16 with the hardware sine/cosine
+// per pair, loading a batch of up to four chunk pairs before computing so the
+// shared-memory and special-function latencies overlap.  Returns max |x'|.
+template <int D>
+__device__ __forceinline__ float rope_row_ilp(uint8_t *tile, int r, uint32_t pos,
+                                              const RopeFreqs &fr)
+{
+    constexpr int HC = D / 16;
+    constexpr int BATCH = HC < 4 ? HC : 4;
+    float mx = 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < HC; c0 += BATCH) {
+        uint4 a[BATCH], b[BATCH];
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            a[i] = *reinterpret_cast<const uint4 *>(tile + tile_chunk<D>(r, c0 + i));
+            b[i] = *reinterpret_cast<const uint4 *>(tile + tile_chunk<D>(r, c0 + i + HC));
+        }
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            uint32_t av[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+            uint32_t bv[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float u[2], w[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float sn, cs;
+                    rope_sincos(pos, fr.turn[8 * (c0 + i) + 2 * e + h], sn, cs);
+                    const float x = h ? bf16_hi(av[e]) : bf16_lo(av[e]);
+                    const float y = h ? bf16_hi(bv[e]) : bf16_lo(bv[e]);
+                    u[h] = x * cs - y * sn;
+                    w[h] = y * cs + x * sn;
+                    mx = fmaxf(mx, fmaxf(fabsf(u[h]), fabsf(w[h])));
+                }
+                av[e] = pack_f16x2(u[0], u[1]);
+                bv[e] = pack_f16x2(w[0], w[1]);
+            }
+            a[i] = make_uint4(av[0], av[1], av[2], av[3]);
+            b[i] = make_uint4(bv[0], bv[1], bv[2], bv[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            *reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c0 + i)) = a[i];
+            *reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c0 + i + HC)) = b[i];
+        }
+    }
+    return mx;
+}
+
+// Stores 32 consecutive fp32 values as bf16 (64 bytes).
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16 *dst, const float *v)
+{
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        d4[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
+                           pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                           pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
+                           pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
 }
 
 // Inverse rotation (by -angle) of a pair of fp32 values held in registers.
