@@ -193,7 +193,7 @@ __global__ void timeout_selftest_kernel(uint32_t *status, uint64_t limit_ns)
 
 namespace ne {
 
-int fwd_heads_per_cta(int d, int G) { return largest_divisor_at_most(G, d == 128 ? 2 : 4); }
+int fwd_heads_per_cta(int d, int G) { return largest_divisor_at_most(G, d == 32 ? 4 : d == 64 ? 3 : 2); }
 int dq_heads_per_cta(int d, int G)
 {
     return d == 128 ? 1 : largest_divisor_at_most(G, d == 64 ? 3 : 4);
@@ -227,11 +227,11 @@ int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse
     p.nchunks = p.G / p.GC;
     p.out0 = o;
     p.lse = lse;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
-        make_map(&mv, v, B, T, Hkv, d))
+        make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
         return NE_ERR_CUDA;
-    cudaError_t e = ne::launch_fwd(d, mq, mk, mv, p, static_cast<cudaStream_t>(stream));
+    cudaError_t e = ne::launch_fwd(d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 

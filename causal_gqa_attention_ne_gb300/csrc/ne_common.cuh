@@ -219,7 +219,7 @@ __device__ __forceinline__ float rope_row_ilp(uint8_t *tile, int r, uint32_t pos
                                               const RopeFreqs &fr)
 {
     constexpr int HC = D / 16;
-    constexpr int BATCH = HC < 4 ? HC : 4;
+    constexpr int BATCH = HC < 2 ? HC : 2;
     float mx = 0.f;
 #pragma unroll
     for (int c0 = 0; c0 < HC; c0 += BATCH) {

@@ -8,9 +8,10 @@
 
 namespace ne {
 
-// Forward: grid = M * B * Hkv * nchunks CTAs of 320 threads.
+// Forward: persistent CTAs of 512 threads over M * B * Hkv * nchunks units;
+// `o` is the tensor map of the output (same layout as q), used for its store.
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                       const AttnParams &p, cudaStream_t stream);
+                       const CUtensorMap &o, const AttnParams &p, cudaStream_t stream);
 
 // Backward preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c], and the
 // rotated Q' = R(t) q, K' = R(s) k as fp16 (same layouts) into qrot / krot.

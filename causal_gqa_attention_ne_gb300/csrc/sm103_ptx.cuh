@@ -168,6 +168,86 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 4-D tiled store from shared memory (bulk-group completion).  Elements
+// outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                             int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// This thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// This thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait0()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ------------------------------------------------- shared-memory counters ---
+// Monotonic per-CTA counters that order hand-offs between warps of different
+// roles without a CTA-wide barrier: a writer publishes with release, a reader
+// polls with acquire.
+
+__device__ __forceinline__ uint32_t ld_acquire_smem(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_smem(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void add_release_smem(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v)
+                 : "memory");
+}
+
+static __device__ __forceinline__ bool counter_wait_slow(const uint32_t *p, uint32_t target,
+                                                        WaitCtl w)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_smem(p) >= target)
+            return true;
+        if (*w.abort)
+            return false;
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1u;
+            atomicOr(w.status, kDevTimeout);
+            return false;
+        }
+    }
+}
+
+// Warp-uniform bounded wait until *p >= target (every lane polls the same
+// word with acquire, so each is ordered after the writer's release).
+__device__ __forceinline__ bool counter_wait_warp(const uint32_t *p, uint32_t target,
+                                                  const WaitCtl &w)
+{
+    bool ok = ld_acquire_smem(p) >= target;
+    if (!__all_sync(0xffffffffu, ok))
+        ok = counter_wait_slow(p, target, w);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ----------------------------------------------------------------- TMEM ---
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
@@ -371,6 +451,14 @@ __device__ __forceinline__ float ex2_approx(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Three-way maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
