@@ -9,7 +9,9 @@ backward on one stream, every layer with its own buffers (4.3 GB in all, so
 each layer's inputs are cold in the 129 MB L2).  Synthetic seeded N(0, 1)
 inputs (see ne_inputs.py).
 
-A step = 16 x (ne_attn_fwd, then the three backward steps) through the C ABI.
+A step = 16 x (ne_attn_fwd_save, then the three backward steps of
+ne_attn_bwd_saved) through the C ABI: the training pair, in which the forward
+leaves the rotated Q', K' in the workspace for the backward.
 The step is captured in a CUDA graph so Python call overhead does not leave
 the GPU idle; CUDA events inside the graph time every kernel.
 
@@ -67,10 +69,10 @@ def kernel_work(w=W):
     row = B * Hq * T * 4                           # lse or D
     return {
         # QK^T and PV: 2 GEMMs of 2d flops per pair; reads Q K V, writes O lse
-        "fwd": {"flops": 4.0 * d * pairs, "bytes": q + 2 * kv + q + row},
-        # D = rowsum(dO * O), Q' = R(t) q, K' = R(s) k: reads O, dO, q, k;
-        # writes D and fp16 Q', K'
-        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 4 * q + row + 2 * kv},
+        # and the fp16 Q', K' it rotated (for the backward)
+        "fwd": {"flops": 4.0 * d * pairs, "bytes": q + 2 * kv + q + row + q + kv},
+        # D = rowsum(dO * O): reads O, dO; writes D
+        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 2 * q + row},
         # dQ = dS K' (one GEMM; the S and dP recompute is not algorithmic work)
         "bwd_dq": {"flops": 2.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + q},
         # S, dP, dV, dK (four GEMMs); reads Q' K' (fp16) V dO lse D, writes dK dV
@@ -224,10 +226,10 @@ def run_ours(args, rank, world, local_rank):
         for li, (_, d, _) in enumerate(layers):
             if evs is not None:
                 evs[li][0].record()
-            ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], theta)
+            ne.ne_attn_fwd_save(d["q"], d["k"], d["v"], d["o"], d["lse"], d["ws"], theta)
             if evs is not None:
                 evs[li][1].record()
-            ne.ne_attn_bwd_preprocess(d["q"], d["k"], d["o"], d["do"], d["ws"], theta)
+            ne.ne_attn_bwd_preprocess_d(d["o"], d["do"], d["ws"], W.Hkv)
             if evs is not None:
                 evs[li][2].record()
             ne.ne_attn_bwd_dq(d["q"], d["k"], d["v"], d["lse"], d["do"], d["dq"], d["ws"], theta)
@@ -323,9 +325,9 @@ def run_ours(args, rank, world, local_rank):
         for host, d, oh in layers:
             for n in ("q", "k", "v", "do"):
                 d[n].copy_(host[n], non_blocking=True)
-            ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], theta)
-            ne.ne_attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"],
-                           d["dv"], d["ws"], theta)
+            ne.ne_attn_fwd_save(d["q"], d["k"], d["v"], d["o"], d["lse"], d["ws"], theta)
+            ne.ne_attn_bwd_saved(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"],
+                                 d["dk"], d["dv"], d["ws"], theta)
             for n in ("o", "lse", "dq", "dk", "dv"):
                 oh[n].copy_(d[n], non_blocking=True)
     e1.record(s)
@@ -393,9 +395,13 @@ def run_one_layer_for_profiler():
 
     import causal_gqa_attention_ne_gb300 as ne
     x = {n: t.cuda() for n, t in ne_inputs.make_inputs(W, 0).items()}
+    ws = torch.empty(ne.ne_attn_bwd_workspace_size(W.B, W.T, W.Hq, W.Hkv, W.d),
+                     dtype=torch.uint8, device="cuda")
+    o, lse = torch.empty_like(x["q"]), torch.empty(W.B, W.Hq, W.T, device="cuda")
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
     for _ in range(2):
-        o, lse = ne.attention_forward(x["q"], x["k"], x["v"], W.theta)
-        ne.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], W.theta)
+        ne.ne_attn_fwd_save(x["q"], x["k"], x["v"], o, lse, ws, W.theta)
+        ne.ne_attn_bwd_saved(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, ws, W.theta)
     torch.cuda.synchronize()
     st = ne.ne_attn_get_error()
     if st != 0:

@@ -23,7 +23,8 @@ NE_STATUS = {
 EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn_bwd_preprocess",
             "ne_attn_bwd_dq", "ne_attn_bwd_dkdv", "ne_attn_get_error", "ne_attn_status_string",
             "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout", "ne_attn_bwd_noalloc",
-            "ne_attn_bwd_noalloc_max_scratch")
+            "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save", "ne_attn_bwd_saved",
+            "ne_attn_bwd_preprocess_d")
 
 _lock = threading.Lock()
 _lib = None
@@ -57,6 +58,12 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_fwd.restype = i
         lib.ne_attn_bwd.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd.restype = i
+        lib.ne_attn_fwd_save.argtypes = [vp] * 6 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd_save.restype = i
+        lib.ne_attn_bwd_saved.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_saved.restype = i
+        lib.ne_attn_bwd_preprocess_d.argtypes = [vp] * 3 + [sz] + [i] * 5 + [vp]
+        lib.ne_attn_bwd_preprocess_d.restype = i
         lib.ne_attn_bwd_preprocess.argtypes = [vp] * 5 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd_preprocess.restype = i
         lib.ne_attn_bwd_dq.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
@@ -131,6 +138,61 @@ def ne_attn_fwd(q, k, v, o, lse, rope_theta: float = 10000.0, stream=None) -> No
                                     _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_fwd")
+
+
+def _workspace_ptr(workspace):
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def ne_attn_fwd_save(q, k, v, o, lse, workspace, rope_theta: float = 10000.0,
+                     stream=None) -> None:
+    """ne_attn_fwd that also leaves Q' and K' in `workspace` for ne_attn_bwd_saved."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (B, T, Hq, d), bf)
+    _check(k, "k", (B, T, Hkv, d), bf)
+    _check(v, "v", (B, T, Hkv, d), bf)
+    _check(o, "o", (B, T, Hq, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_fwd_save(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), wp, wbytes, B, T, Hq, Hkv, d,
+                                         float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd_save")
+
+
+def ne_attn_bwd_saved(q, k, v, o, lse, do, dq, dk, dv, workspace, rope_theta: float = 10000.0,
+                      stream=None) -> None:
+    """ne_attn_bwd on a workspace filled by ne_attn_fwd_save (D is recomputed, Q'/K' reused)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_saved(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), wp, wbytes,
+                                          B, T, Hq, Hkv, d, float(rope_theta),
+                                          _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_saved")
+
+
+def ne_attn_bwd_preprocess_d(o, do, workspace, Hkv: int, stream=None) -> None:
+    """D = rowsum(dO * O) into the workspace only (first step of ne_attn_bwd_saved)."""
+    B, T, Hq, d = o.shape
+    for x, n in ((o, "o"), (do, "do")):
+        _check(x, n, (B, T, Hq, d), torch.bfloat16)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_preprocess_d(o.data_ptr(), do.data_ptr(), wp, wbytes, B, T,
+                                                 Hq, Hkv, d, _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_preprocess_d")
 
 
 def ne_attn_bwd_workspace_size(B: int, T: int, Hq: int, Hkv: int, d: int) -> int:

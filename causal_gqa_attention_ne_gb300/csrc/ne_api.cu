@@ -101,7 +101,8 @@ int check_shape(int B, int T, int Hq, int Hkv, int d, float theta)
 
 // 4-D TMA descriptor over a contiguous [B][T][H][d] 16-bit tensor; box is
 // (one swizzle span of columns, 1 head, 128 rows, 1 batch).
-int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d, bool fp16 = false)
+int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d, bool fp16 = false,
+             int box_rows = 128)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
@@ -111,7 +112,7 @@ int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d, bool f
                           static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
                              static_cast<cuuint64_t>(T) * H * d * 2};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(swb / 2), 1, 128, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(swb / 2), 1, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                      4, const_cast<void *>(ptr), dims,
@@ -207,17 +208,23 @@ cudaError_t launch_timeout_selftest(uint32_t *status, uint64_t limit_ns, cudaStr
 
 } // namespace ne
 
-extern "C" {
+namespace {
 
-int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int T,
-                int Hq, int Hkv, int d, float rope_theta, void *stream)
+// The forward; with a workspace it also stores the rotated Q' and K' (fp16)
+// into the workspace's Q' and K' regions for ne_attn_bwd_saved.
+int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace,
+             size_t workspace_bytes, bool save, int B, int T, int Hq, int Hkv, int d,
+             float rope_theta, void *stream)
 {
-    if (!q || !k || !v || !o || !lse)
+    if (!q || !k || !v || !o || !lse || (save && !workspace))
         return NE_ERR_NULL;
     int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+    if (save && workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+        (save && !aligned16(workspace)))
         return NE_ERR_ALIGN;
     uint32_t *status = nullptr;
     if ((rc = device_state(&status)) != NE_OK)
@@ -227,12 +234,41 @@ int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse
     p.nchunks = p.G / p.GC;
     p.out0 = o;
     p.lse = lse;
-    CUtensorMap mq, mk, mv, mo;
+    p.save_rot = save ? 1 : 0;
+    CUtensorMap mq, mk, mv, mo, mqs, mks;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
         make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
         return NE_ERR_CUDA;
-    cudaError_t e = ne::launch_fwd(d, mq, mk, mv, mo, p, static_cast<cudaStream_t>(stream));
+    if (save) {
+        void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);
+        void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
+        if (make_map(&mqs, qrot, B, T, Hq, d, true) || make_map(&mks, krot, B, T, Hkv, d, true))
+            return NE_ERR_CUDA;
+    } else {
+        mqs = mq;   // not used
+        mks = mk;
+    }
+    cudaError_t e =
+        ne::launch_fwd(d, mq, mk, mv, mo, mqs, mks, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int T,
+                int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    return fwd_impl(q, k, v, o, lse, nullptr, 0, false, B, T, Hq, Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_fwd_save(const void *q, const void *k, const void *v, void *o, float *lse,
+                     void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                     float rope_theta, void *stream)
+{
+    return fwd_impl(q, k, v, o, lse, workspace, workspace_bytes, true, B, T, Hq, Hkv, d,
+                    rope_theta, stream);
 }
 
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
@@ -331,6 +367,32 @@ int ne_attn_bwd_preprocess(const void *q, const void *k, const void *o, const vo
                : NE_ERR_CUDA;
 }
 
+int ne_attn_bwd_preprocess_d(const void *o, const void *dO, void *workspace,
+                             size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                             void *stream)
+{
+    if (!o || !dO)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, 1.0f);
+    if (rc != NE_OK)
+        return rc;
+    if (!workspace || workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(o) || !aligned16(dO) || !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, 1.0f, status);
+    p.o_in = o;
+    p.do_in = dO;
+    p.Dws = static_cast<float *>(workspace);
+    return ne::launch_bwd_pre(d, p, nullptr, nullptr, nullptr, nullptr,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? NE_OK
+               : NE_ERR_CUDA;
+}
+
 int ne_attn_bwd_dq(const void *q, const void *k, const void *v, const float *lse,
                    const void *dO, void *dq, const void *workspace, size_t workspace_bytes,
                    int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
@@ -386,6 +448,31 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
     void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);
     void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
     if (ne::launch_bwd_pre(d, p, q, qrot, k, krot, st) != cudaSuccess)
+        return NE_ERR_CUDA;
+    if ((rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
+        return rc;
+    return run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st);
+}
+
+int ne_attn_bwd_saved(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                      void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                      int d, float rope_theta, void *stream)
+{
+    if (!o || !dq || !dk || !dv)
+        return NE_ERR_NULL;
+    if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return NE_ERR_ALIGN;
+    ne::AttnParams p;
+    CUtensorMap mq, mk, mv, mdo, mqr, mkr;
+    int rc = bwd_setup(q, k, v, lse, dO, workspace, workspace_bytes, B, T, Hq, Hkv, d,
+                       rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
+    if (rc != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.o_in = o;
+    // Q' and K' are already in the workspace: the preprocess computes D only
+    if (ne::launch_bwd_pre(d, p, q, nullptr, k, nullptr, st) != cudaSuccess)
         return NE_ERR_CUDA;
     if ((rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
         return rc;

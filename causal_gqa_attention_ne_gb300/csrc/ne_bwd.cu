@@ -28,7 +28,8 @@ namespace ne {
 //   Q'[b,t,h,:] = R(t) q[b,t,h,:] as fp16              (the score-side operands
 //   K'[b,s,j,:] = R(s) k[b,s,j,:] as fp16               of the backward, rotated
 //                once here instead of once per tile inside the loops)
-// Pure streaming over O, dO, q and k.
+// Pure streaming over O, dO, q and k.  With qrot == nullptr (Q' and K' already
+// in the workspace, stored by the forward's training path) only D is computed.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const uint4 *q,
                                                       uint4 *qrot, const uint4 *k, uint4 *krot)
@@ -49,16 +50,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
         if (idx < nthreads) {
             const size_t c0 = row * CPR + c, c1 = c0 + TPR;
             const uint4 oa = o[c0], ob = o[c1], ga = g[c0], gb = g[c1];
-            const uint4 qa = q[c0], qb = q[c1];
             const uint32_t oav[4] = {oa.x, oa.y, oa.z, oa.w}, obv[4] = {ob.x, ob.y, ob.z, ob.w};
             const uint32_t gav[4] = {ga.x, ga.y, ga.z, ga.w}, gbv[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc += bf16_lo(oav[e]) * bf16_lo(gav[e]) + bf16_hi(oav[e]) * bf16_hi(gav[e]);
+                acc += bf16_lo(obv[e]) * bf16_lo(gbv[e]) + bf16_hi(obv[e]) * bf16_hi(gbv[e]);
+            }
+        }
+        if (idx < nthreads && qrot != nullptr) {
+            const size_t c0 = row * CPR + c, c1 = c0 + TPR;
+            const uint4 qa = q[c0], qb = q[c1];
             const uint32_t qav[4] = {qa.x, qa.y, qa.z, qa.w}, qbv[4] = {qb.x, qb.y, qb.z, qb.w};
             const uint32_t t = static_cast<uint32_t>((row / p.Hq) % p.T);
             uint32_t ra[4], rb[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                acc += bf16_lo(oav[e]) * bf16_lo(gav[e]) + bf16_hi(oav[e]) * bf16_hi(gav[e]);
-                acc += bf16_lo(obv[e]) * bf16_lo(gbv[e]) + bf16_hi(obv[e]) * bf16_hi(gbv[e]);
                 float u[2], w[2];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -88,7 +95,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
         }
     }
     // K' = R(s) k as fp16, same layout as k.
-    const size_t krows = static_cast<size_t>(p.B) * p.T * p.Hkv;
+    const size_t krows = qrot != nullptr ? static_cast<size_t>(p.B) * p.T * p.Hkv : 0;
     for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
          idx < krows * TPR; idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const size_t row = idx / TPR;                // ((b*T + s)*Hkv + j)

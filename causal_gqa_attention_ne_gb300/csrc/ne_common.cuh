@@ -351,6 +351,7 @@ struct AttnParams {
     uint32_t *status;            // device status word
     int num_units;               // persistent kernels: work units in the launch
     uint64_t wait_limit_ns;
+    int save_rot;                // forward: also store Q' and K' (fp16) for the backward
     RopeFreqs rope;
 };
 

@@ -29,7 +29,10 @@
 //   warps 8-11  RoPE: rotate the unit's Q tiles and each K tile in place
 //               (bf16 in, fp16 out), in the order the MMAs first need them.
 //   warp 12     TMA producer.   warp 13  TMEM allocator + S issuer.
-//   warp 14     PV issuer.      warp 15  idle.
+//   warp 14     PV issuer.
+//   warp 15     training path only: stores each rotated Q' tile and each K'
+//               tile once into the backward's workspace, and tells the
+//               producer when a buffer it stored from may be reloaded.
 // TMEM: NSB S buffers of 64 columns (item gi uses gi % NSB), two P buffers
 // of 32 columns (bf16 pairs; group w uses P_w), then O of head g at
 // COL_O + g*D.
@@ -108,6 +111,7 @@ template <int D, int GC, int ST>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const __grid_constant__ CUtensorMap tmQs, const __grid_constant__ CUtensorMap tmKs,
                const AttnParams p)
 {
     using C = FwdCfg<D, GC, ST>;
@@ -128,6 +132,10 @@ __global__ void __launch_bounds__(512, 1)
     // partner waits for, so the parity of n / 3 is unambiguous)
     __shared__ uint64_t bar_hm[2][3], bar_hl[2][3];
     __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
+    // training path: warp 15 is done with a rotated tile (stored it, and the
+    // store has read the buffer; for K stages every tile, stored or not, so
+    // warp 15 never falls two phases behind a k_ready barrier)
+    __shared__ uint64_t bar_q_rd[QB][GC], bar_k_rd[ST];
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
     float *mrun = reinterpret_cast<float *>(smem + C::OFF_M);   // [g][row], log2 units
@@ -143,6 +151,7 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_init(smem_u32(&bar_q_full[qb][g]), 1);
                 mbar_init(smem_u32(&bar_q_ready[qb][g]), 4);
                 mbar_init(smem_u32(&bar_q_empty[qb][g]), 1);
+                mbar_init(smem_u32(&bar_q_rd[qb][g]), 1);
             }
             mbar_init(smem_u32(&bar_o_free[g]), 4);
         }
@@ -151,6 +160,7 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(smem_u32(&bar_k_ready[s]), 4);
             mbar_init(smem_u32(&bar_v_full[s]), 1);
             mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+            mbar_init(smem_u32(&bar_k_rd[s]), 1);
         }
         for (int b = 0; b < NSB; ++b) {
             mbar_init(smem_u32(&bar_s_full[b]), 1);
@@ -211,6 +221,10 @@ __global__ void __launch_bounds__(512, 1)
                 for (int g = 0; g < GC; ++g) {
                     if (use >= 1 && !mbar_wait(smem_u32(&bar_q_empty[qb][g]), (use - 1) & 1, wc))
                         return false;
+                    // training path: the previous tile of this slot was stored
+                    if (p.save_rot && use >= 1 &&
+                        !mbar_wait(smem_u32(&bar_q_rd[qb][g]), (use - 1) & 1, wc))
+                        return false;
                     const uint32_t bar = smem_u32(&bar_q_full[qb][g]);
                     mbar_arrive_expect_tx(bar, TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb)
@@ -224,6 +238,9 @@ __global__ void __launch_bounds__(512, 1)
             auto load_kv = [&](const FwdUnit &w, int jk) {
                 const int st = kt % ST, u2 = kt / ST;
                 if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc))
+                    return false;
+                if (p.save_rot && u2 >= 1 &&
+                    !mbar_wait(smem_u32(&bar_k_rd[st]), (u2 - 1) & 1, wc))
                     return false;
                 const uint32_t kb = smem_u32(&bar_k_full[st]), vb = smem_u32(&bar_v_full[st]);
                 mbar_arrive_expect_tx(kb, TL::BYTES);
@@ -263,6 +280,71 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_wait_drain(smem_u32(&bar_v_full[t % ST]), (t / ST) & 1, wc.limit_ns);
                 }
             }
+        } else if (warp == 15 && p.save_rot) {
+            // ------------------------------- stores of rotated tiles ---
+            // Same tile order as the RoPE warpgroup.  A tile marked ready is
+            // rotated (and fenced for the async proxy); its store reads the
+            // buffer while the MMAs read it too; the producer reloads the
+            // buffer only after bar_q_rd / bar_k_rd.
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQs);
+                tma_prefetch_desc(&tmKs);
+            }
+            bool ok = true;
+            int kt = 0;
+            for (int k = 0; ok; ++k) {
+                const int u = snake_unit(k, cta, P);
+                if (u >= p.num_units)
+                    break;
+                const FwdUnit w = fwd_unit(u, GC, p);
+                const int nq0 = (QB == 1 || k == 0) ? GC : 0;
+                const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
+                const int nq1 = has_next ? GC : 0;
+                for (int t = 0; t < nq0 + 1 + nq1 + w.m && ok; ++t) {
+                    const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
+                    const int qunit = t < nq0 ? k : k + 1;
+                    const int g = t < nq0 ? t : t - nq0 - 1;
+                    const int jk = t == nq0 ? 0 : t - nq0 - nq1;
+                    const int qb = qunit % QB, st = kt % ST;
+                    const uint32_t ready =
+                        isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]);
+                    const uint32_t par = isq ? ((qunit / QB) & 1) : ((kt / ST) & 1);
+                    if (!isq)
+                        ++kt;
+                    // every tile's ready phase, in order (exact parity)
+                    if (!mbar_wait_warp(ready, par, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!isq && !(jk == w.m && w.h0 == w.j * p.G)) {
+                        // this K' tile is stored by its diagonal unit
+                        if (lane == 0)
+                            mbar_arrive(smem_u32(&bar_k_rd[st]));
+                        __syncwarp();
+                        continue;
+                    }
+                    const uint8_t *tile = smem + (isq ? C::OFF_Q + (qb * GC + g) * TL::BYTES
+                                                      : C::OFF_K + st * TL::BYTES);
+                    if (lane == 0) {
+                        const FwdUnit wq =
+                            isq && qunit != k ? fwd_unit(snake_unit(qunit, cta, P), GC, p) : w;
+                        for (int cb = 0; cb < TL::NB; ++cb) {
+                            const uint32_t src = smem_u32(tile + cb * TL::BLOCK);
+                            if (isq)
+                                tma_store_4d(&tmQs, src, cb * TL::BOX_COLS, wq.h0 + g,
+                                             wq.m * kRows, wq.b);
+                            else
+                                tma_store_4d(&tmKs, src, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                        }
+                        bulk_commit();
+                        bulk_wait_read0();
+                        mbar_arrive(isq ? smem_u32(&bar_q_rd[qb][g]) : smem_u32(&bar_k_rd[st]));
+                    }
+                    __syncwarp();
+                }
+            }
+            if (lane == 0)
+                bulk_wait0();
         } else if (warp == 13 || warp == 14) {
             // -------------------------------------------------- MMA issuers ---
             constexpr uint32_t ID_S = idesc_f16(128, 64, false, false, false);
@@ -388,8 +470,10 @@ __global__ void __launch_bounds__(512, 1)
                                                p.rope));
                 fence_proxy_async_smem();
                 __syncwarp();
+                const uint32_t ready =
+                    isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]);
                 if (lane == 0)
-                    mbar_arrive(isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]));
+                    mbar_arrive(ready);
                 if (!isq)
                     ++kt;
             }
@@ -659,7 +743,8 @@ __global__ void __launch_bounds__(512, 1)
 
 template <int D, int GC, int ST>
 static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                const CUtensorMap &o, const AttnParams &p0, cudaStream_t stream)
+                                const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
+                                const AttnParams &p0, cudaStream_t stream)
 {
     using C = FwdCfg<D, GC, ST>;
     auto kern = fwd_kernel<D, GC, ST>;
@@ -674,42 +759,44 @@ static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, cons
     AttnParams p = p0;
     p.num_units = p.M * p.B * p.Hkv * p.nchunks;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
-    kern<<<grid, 512, C::SMEM_BYTES, stream>>>(q, k, v, o, p);
+    kern<<<grid, 512, C::SMEM_BYTES, stream>>>(q, k, v, o, qs, ks, p);
     return cudaGetLastError();
 }
 
 template <int D, int GC>
 static cudaError_t launch_fwd_p(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                const CUtensorMap &o, const AttnParams &p, cudaStream_t stream)
+                                const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
+                                const AttnParams &p, cudaStream_t stream)
 {
-    return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST>(q, k, v, o, p, stream);
+    return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST>(q, k, v, o, qs, ks, p, stream);
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                       const CUtensorMap &o, const AttnParams &p, cudaStream_t stream)
+                       const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
+                       const AttnParams &p, cudaStream_t stream)
 {
     switch (d) {
     case 32:
         switch (p.GC) {
-        case 1: return launch_fwd_p<32, 1>(q, k, v, o, p, stream);
-        case 2: return launch_fwd_p<32, 2>(q, k, v, o, p, stream);
-        case 3: return launch_fwd_p<32, 3>(q, k, v, o, p, stream);
-        case 4: return launch_fwd_p<32, 4>(q, k, v, o, p, stream);
+        case 1: return launch_fwd_p<32, 1>(q, k, v, o, qs, ks, p, stream);
+        case 2: return launch_fwd_p<32, 2>(q, k, v, o, qs, ks, p, stream);
+        case 3: return launch_fwd_p<32, 3>(q, k, v, o, qs, ks, p, stream);
+        case 4: return launch_fwd_p<32, 4>(q, k, v, o, qs, ks, p, stream);
         default: break;
         }
         break;
     case 64:
         switch (p.GC) {
-        case 1: return launch_fwd_p<64, 1>(q, k, v, o, p, stream);
-        case 2: return launch_fwd_p<64, 2>(q, k, v, o, p, stream);
-        case 3: return launch_fwd_p<64, 3>(q, k, v, o, p, stream);
+        case 1: return launch_fwd_p<64, 1>(q, k, v, o, qs, ks, p, stream);
+        case 2: return launch_fwd_p<64, 2>(q, k, v, o, qs, ks, p, stream);
+        case 3: return launch_fwd_p<64, 3>(q, k, v, o, qs, ks, p, stream);
         default: break;
         }
         break;
     case 128:
         switch (p.GC) {
-        case 1: return launch_fwd_p<128, 1>(q, k, v, o, p, stream);
-        case 2: return launch_fwd_p<128, 2>(q, k, v, o, p, stream);
+        case 1: return launch_fwd_p<128, 1>(q, k, v, o, qs, ks, p, stream);
+        case 2: return launch_fwd_p<128, 2>(q, k, v, o, qs, ks, p, stream);
         default: break;
         }
         break;

@@ -10,8 +10,11 @@ namespace ne {
 
 // Forward: persistent CTAs of 512 threads over M * B * Hkv * nchunks units;
 // `o` is the tensor map of the output (same layout as q), used for its store.
+// `qs` / `ks` map the fp16 Q' / K' regions of a backward workspace; they are
+// written only when p.save_rot is set.
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                       const CUtensorMap &o, const AttnParams &p, cudaStream_t stream);
+                       const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
+                       const AttnParams &p, cudaStream_t stream);
 
 // Backward preprocess: D[b][h][t] = sum_c dO[b,t,h,c] * O[b,t,h,c], and the
 // rotated Q' = R(t) q, K' = R(s) k as fp16 (same layouts) into qrot / krot.

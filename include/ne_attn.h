@@ -103,6 +103,36 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
                 float rope_theta, void *stream);
 
 /*
+ * Training pair.  ne_attn_fwd_save is ne_attn_fwd that also leaves the
+ * rotated Q' = R(t) q and K' = R(s) k (fp16) in `workspace` (at least
+ * ne_attn_bwd_workspace_size(...) bytes, 16-byte aligned, caller-owned), in
+ * the layout ne_attn_bwd uses; the forward rotates every Q and K tile in
+ * shared memory anyway, so this saves the backward from reading q and k and
+ * rotating them again.  ne_attn_bwd_saved is ne_attn_bwd for a workspace
+ * filled that way: its preprocess computes D only.  q and k are validated
+ * but not read by ne_attn_bwd_saved; the workspace must come from
+ * ne_attn_fwd_save on the same q, k, shape and rope_theta, unchanged since
+ * (the library cannot check this).  Results equal those of ne_attn_fwd
+ * followed by ne_attn_bwd, bit for bit.  Errors as for ne_attn_fwd and
+ * ne_attn_bwd (NE_ERR_WORKSPACE for a missing or short workspace).
+ */
+/*
+ * ne_attn_bwd_saved runs these three steps: ne_attn_bwd_preprocess_d (D only,
+ * into the workspace; no rope_theta needed), then ne_attn_bwd_dq and
+ * ne_attn_bwd_dkdv below, which read Q' and K' from the workspace.
+ */
+int ne_attn_bwd_preprocess_d(const void *o, const void *dO, void *workspace,
+                             size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                             void *stream);
+int ne_attn_fwd_save(const void *q, const void *k, const void *v, void *o, float *lse,
+                     void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                     int d, float rope_theta, void *stream);
+int ne_attn_bwd_saved(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                      void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                      int d, float rope_theta, void *stream);
+
+/*
  * The three steps ne_attn_bwd runs, in this order, exposed so a caller can
  * time them or run the two independent steps (dq, and dk/dv) on two streams
  * once the preprocess has finished.  Arguments mean what they mean for
