@@ -133,7 +133,10 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
 {
     const size_t nthreads = static_cast<size_t>(p.B) * p.T * p.Hq * (d / 16);
     size_t blocks = (nthreads + 255) / 256;
-    const size_t cap = 152 * 16;
+    // With the rotations, a grid-stride loop over a capped grid (the K'
+    // rows are covered by the same threads); D alone is one row chunk per
+    // thread, so the whole grid streams without a loop.
+    const size_t cap = qrot != nullptr ? 152 * 16 : 152 * 256;
     if (blocks > cap)
         blocks = cap;
     const uint4 *qi = static_cast<const uint4 *>(q), *ki = static_cast<const uint4 *>(k);

@@ -132,10 +132,11 @@ __global__ void __launch_bounds__(512, 1)
     // partner waits for, so the parity of n / 3 is unambiguous)
     __shared__ uint64_t bar_hm[2][3], bar_hl[2][3];
     __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
-    // training path: warp 15 is done with a rotated tile (stored it, and the
-    // store has read the buffer; for K stages every tile, stored or not, so
-    // warp 15 never falls two phases behind a k_ready barrier)
-    __shared__ uint64_t bar_q_rd[QB][GC], bar_k_rd[ST];
+    // training path: the RoPE warps finished the n-th tile to be stored
+    // (ring of 16: they are never 16 such tiles ahead of warp 15, which must
+    // release a Q slot or a stored K stage before it is reloaded), and warp
+    // 15's store has read a Q slot / K stage
+    __shared__ uint64_t bar_sv[16], bar_q_rd[QB][GC], bar_k_rd[ST];
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
     float *mrun = reinterpret_cast<float *>(smem + C::OFF_M);   // [g][row], log2 units
@@ -179,6 +180,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(smem_u32(&bar_stg_free[w]), 1);
         }
         mbar_init(smem_u32(&bar_drain), 2);
+        for (int i = 0; i < 16; ++i)
+            mbar_init(smem_u32(&bar_sv[i]), 4);
         fence_mbar_init();
     }
     if (warp == 13) {
@@ -235,13 +238,20 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 return true;
             };
+            // training path: K' tiles stored from each stage (count, and
+            // whether the stage's last tile was one)
+            int ksaved[ST] = {};
+            uint32_t last_saved = 0;
             auto load_kv = [&](const FwdUnit &w, int jk) {
                 const int st = kt % ST, u2 = kt / ST;
                 if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc))
                     return false;
-                if (p.save_rot && u2 >= 1 &&
-                    !mbar_wait(smem_u32(&bar_k_rd[st]), (u2 - 1) & 1, wc))
+                if (((last_saved >> st) & 1u) &&
+                    !mbar_wait(smem_u32(&bar_k_rd[st]), (ksaved[st] - 1) & 1, wc))
                     return false;
+                const bool saved = p.save_rot && jk == w.m && w.h0 == w.j * p.G;
+                last_saved = (last_saved & ~(1u << st)) | (saved ? 1u << st : 0u);
+                ksaved[st] += saved ? 1 : 0;
                 const uint32_t kb = smem_u32(&bar_k_full[st]), vb = smem_u32(&bar_v_full[st]);
                 mbar_arrive_expect_tx(kb, TL::BYTES);
                 for (int cb = 0; cb < TL::NB; ++cb)
@@ -282,16 +292,17 @@ __global__ void __launch_bounds__(512, 1)
             }
         } else if (warp == 15 && p.save_rot) {
             // ------------------------------- stores of rotated tiles ---
-            // Same tile order as the RoPE warpgroup.  A tile marked ready is
-            // rotated (and fenced for the async proxy); its store reads the
-            // buffer while the MMAs read it too; the producer reloads the
-            // buffer only after bar_q_rd / bar_k_rd.
+            // Same tile order as the RoPE warpgroup.  A tile handed over on
+            // bar_sv is rotated (and fenced for the async proxy); its store
+            // reads the buffer while the MMAs read it too; the producer
+            // reloads the buffer only after bar_q_rd / bar_k_rd.
             if (lane == 0) {
                 tma_prefetch_desc(&tmQs);
                 tma_prefetch_desc(&tmKs);
             }
             bool ok = true;
             int kt = 0;
+            uint32_t nsv = 0;
             for (int k = 0; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
@@ -306,23 +317,15 @@ __global__ void __launch_bounds__(512, 1)
                     const int g = t < nq0 ? t : t - nq0 - 1;
                     const int jk = t == nq0 ? 0 : t - nq0 - nq1;
                     const int qb = qunit % QB, st = kt % ST;
-                    const uint32_t ready =
-                        isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]);
-                    const uint32_t par = isq ? ((qunit / QB) & 1) : ((kt / ST) & 1);
                     if (!isq)
                         ++kt;
-                    // every tile's ready phase, in order (exact parity)
-                    if (!mbar_wait_warp(ready, par, wc)) {
+                    if (!isq && !(jk == w.m && w.h0 == w.j * p.G))
+                        continue;   // this K' tile is stored by its diagonal unit
+                    if (!mbar_wait_warp(smem_u32(&bar_sv[nsv % 16]), (nsv / 16) & 1, wc)) {
                         ok = false;
                         break;
                     }
-                    if (!isq && !(jk == w.m && w.h0 == w.j * p.G)) {
-                        // this K' tile is stored by its diagonal unit
-                        if (lane == 0)
-                            mbar_arrive(smem_u32(&bar_k_rd[st]));
-                        __syncwarp();
-                        continue;
-                    }
+                    ++nsv;
                     const uint8_t *tile = smem + (isq ? C::OFF_Q + (qb * GC + g) * TL::BYTES
                                                       : C::OFF_K + st * TL::BYTES);
                     if (lane == 0) {
@@ -439,6 +442,7 @@ __global__ void __launch_bounds__(512, 1)
         float mx = 0.f;
         bool ok = true;
         int kt = 0;
+        uint32_t nsv = 0;   // tiles handed to warp 15 (training path)
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
@@ -474,6 +478,11 @@ __global__ void __launch_bounds__(512, 1)
                     isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]);
                 if (lane == 0)
                     mbar_arrive(ready);
+                if (p.save_rot && (isq || (jk == w.m && w.h0 == w.j * p.G))) {
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&bar_sv[nsv % 16]));
+                    ++nsv;
+                }
                 if (!isq)
                     ++kt;
             }
