@@ -483,6 +483,33 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
     };
+    // A unit's epilogue (dq out of TMEM) runs after the next unit's first
+    // item has been handed to the dQ issuer: the wait for the unit's last dQ
+    // MMA then overlaps that item's softmax work, and the next unit's first
+    // dQ MMA waits for dq_free anyway.
+    int pend_k = -1;
+    DqUnit pend{};
+    auto epilogue = [&]() {
+        if (!mbar_wait_warp(smem_u32(&bar_dq_done), pend_k & 1, wc))
+            return false;
+        tc_fence_after();
+        const int t = pend.m * kRows + r;
+        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.out0);
+#pragma unroll
+        for (int g = 0; g < GC; ++g)
+            if ((g & 1) == w) {
+                __nv_bfloat16 *row =
+                    dq + ((static_cast<size_t>(pend.b) * p.T + t) * p.Hq + pend.h0 + g) * D;
+                epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
+                                         static_cast<uint32_t>(t), p.rope, row, t < p.T);
+            }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&bar_dq_free));
+        pend_k = -1;
+        return true;
+    };
     fetch(0, nl2, nD);
     for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, P);
@@ -569,30 +596,18 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&bar_ds_full));
+            if (it == 0 && pend_k >= 0 && !epilogue()) {
+                ok = false;
+                break;
+            }
         }
         if (!ok)
             break;
-        // ---- unit epilogue: dq = R(t)^T dQ' * scale, bf16 ----
-        if (!mbar_wait_warp(smem_u32(&bar_dq_done), k & 1, wc)) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        const int t = un.m * kRows + r;
-        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.out0);
-#pragma unroll
-        for (int g = 0; g < GC; ++g)
-            if ((g & 1) == w) {
-                __nv_bfloat16 *row =
-                    dq + ((static_cast<size_t>(un.b) * p.T + t) * p.Hq + un.h0 + g) * D;
-                epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
-                                         static_cast<uint32_t>(t), p.rope, row, t < p.T);
-            }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&bar_dq_free));
+        pend_k = k;          // dq = R(t)^T dQ' * scale of this unit: out at the next unit's first item
+        pend = un;
     }
+    if (ok && pend_k >= 0)
+        ok = epilogue();
     if (maxds > kFp16Max)
         atomicOr(p.status, kDevRange);
     teardown();
@@ -978,6 +993,44 @@ __global__ void __launch_bounds__(512, 1)
         float maxds = 0.f;
         bool ok = true;
         int gi = 0;
+        // The epilogue of a unit (dV, dK out of TMEM) runs after the next
+        // unit's first item has been handed to the dV/dK issuer, so the wait
+        // for the unit's last MMAs overlaps that item's softmax work; the
+        // first dV/dK of the next unit waits for acc_free anyway.
+        int pend_k = -1;
+        DkvUnit pend{};
+        auto epilogue = [&]() {
+            if (!mbar_wait_warp(smem_u32(&bar_acc_done), pend_k & 1, wc))
+                return false;
+            tc_fence_after();
+            const int s = pend.n * kRows + r;
+            const size_t rowoff = ((static_cast<size_t>(pend.b) * p.T + s) * p.Hkv + pend.j) * D;
+            if (w == 0) {
+                __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.out1) + rowoff;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t a[32];
+                    tmem_ld32(lane_base + C::COL_DV + cc * 32, a);
+                    tmem_ld_wait(a);
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        x[e] = __uint_as_float(a[e]);
+                    if (s < p.T)
+                        store_row32_bf16(dv + cc * 32, x);
+                }
+            } else {
+                __nv_bfloat16 *dkp = static_cast<__nv_bfloat16 *>(p.out0) + rowoff;
+                epilogue_inverse_rope<D>(lane_base + C::COL_DK, p.scale, static_cast<uint32_t>(s),
+                                         p.rope, dkp, s < p.T);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&bar_acc_free));
+            pend_k = -1;
+            return true;
+        };
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
@@ -1056,41 +1109,18 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_pds_full));
+                if (it == 0 && pend_k >= 0 && !epilogue()) {
+                    ok = false;
+                    break;
+                }
             }
             if (!ok)
                 break;
-            // ---- unit epilogue: dV (warpgroup 0) and dK (warpgroup 1) ----
-            if (!mbar_wait_warp(smem_u32(&bar_acc_done), k & 1, wc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int s = un.n * kRows + r;
-            const size_t rowoff = ((static_cast<size_t>(un.b) * p.T + s) * p.Hkv + un.j) * D;
-            if (w == 0) {
-                __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.out1) + rowoff;
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t a[32];
-                    tmem_ld32(lane_base + C::COL_DV + cc * 32, a);
-                    tmem_ld_wait(a);
-                    float x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        x[e] = __uint_as_float(a[e]);
-                    if (s < p.T)
-                        store_row32_bf16(dv + cc * 32, x);
-                }
-            } else {
-                __nv_bfloat16 *dkp = static_cast<__nv_bfloat16 *>(p.out0) + rowoff;
-                epilogue_inverse_rope<D>(lane_base + C::COL_DK, p.scale, static_cast<uint32_t>(s),
-                                         p.rope, dkp, s < p.T);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_acc_free));
+            pend_k = k;      // dV, dK of this unit: out at the next unit's first item
+            pend = un;
         }
+        if (ok && pend_k >= 0)
+            ok = epilogue();
         if (maxds > kFp16Max)
             atomicOr(p.status, kDevRange);
         teardown();
