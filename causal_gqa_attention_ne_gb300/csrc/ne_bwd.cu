@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
     const size_t nthreads = nrows * TPR;
     const uint4 *o = static_cast<const uint4 *>(p.o_in);
     const uint4 *g = static_cast<const uint4 *>(p.do_in);
+    // programmatic dependent launch: O comes from the previous grid
+    griddep_wait();
     float mx = 0.f;
     for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
          idx - (threadIdx.x % 32) < nthreads;   // whole warps stay in the loop for the shuffles
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
     }
     if (mx > kFp16Max)
         atomicOr(p.status, kDevRange);
+    griddep_launch_dependents();
 }
 
 cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot, const void *k,
@@ -143,12 +146,11 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
     uint4 *qo = static_cast<uint4 *>(qrot), *ko = static_cast<uint4 *>(krot);
     const unsigned nb = static_cast<unsigned>(blocks);
     switch (d) {
-    case 32: bwd_pre_kernel<32><<<nb, 256, 0, stream>>>(p, qi, qo, ki, ko); break;
-    case 64: bwd_pre_kernel<64><<<nb, 256, 0, stream>>>(p, qi, qo, ki, ko); break;
-    case 128: bwd_pre_kernel<128><<<nb, 256, 0, stream>>>(p, qi, qo, ki, ko); break;
+    case 32: return launch_pdl(bwd_pre_kernel<32>, nb, 256, 0, stream, p, qi, qo, ki, ko);
+    case 64: return launch_pdl(bwd_pre_kernel<64>, nb, 256, 0, stream, p, qi, qo, ki, ko);
+    case 128: return launch_pdl(bwd_pre_kernel<128>, nb, 256, 0, stream, p, qi, qo, ki, ko);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 // Epilogue for a gradient of a rotated operand: reads the D fp32 columns of
@@ -291,10 +293,15 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base_s;
+    // Only shared memory and TMEM were touched so far: from here on global
+    // memory is read and written, so wait for the previous grid in the stream
+    // (programmatic dependent launch).
+    griddep_wait();
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
     auto teardown = [&]() {
         tc_fence_before();
         __syncthreads();
+        griddep_launch_dependents();   // this CTA's work is done
         if (warp == 9) {
             tc_fence_after();
             tmem_dealloc(tbase, C::TMEM_COLS);
@@ -730,6 +737,10 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base_s;
+    // Only shared memory and TMEM were touched so far: from here on global
+    // memory is read and written, so wait for the previous grid in the stream
+    // (programmatic dependent launch).
+    griddep_wait();
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
     // Each role ends with its own copy of the teardown: warps run under
     // different register budgets after setmaxnreg, so their code paths never
@@ -737,6 +748,7 @@ __global__ void __launch_bounds__(512, 1)
     auto teardown = [&]() {
         tc_fence_before();
         __syncthreads();
+        griddep_launch_dependents();   // this CTA's work is done
         if (warp == 13) {
             tc_fence_after();
             tmem_dealloc(tbase, C::TMEM_COLS);
@@ -1146,8 +1158,7 @@ static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const
     AttnParams p = p0;
     p.num_units = p.M * p.B * p.Hkv * p.nchunks;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
-    kern<<<grid, 384, C::SMEM_BYTES, stream>>>(q, k, v, dO, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, 384, C::SMEM_BYTES, stream, q, k, v, dO, p);
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
@@ -1197,8 +1208,7 @@ static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, con
     AttnParams p = p0;
     p.num_units = p.M * p.B * p.Hkv;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
-    kern<<<grid, 512, C::SMEM_BYTES, stream>>>(q, k, v, dO, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, dO, p);
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,

@@ -302,6 +302,31 @@ inline cudaError_t ensure_smem_attr(Kernel kern, int bytes, bool (&done)[64])
     return e;
 }
 
+// Launches `kern` with programmatic stream serialization: the grid may be
+// scheduled while the previous kernel in the stream is still finishing (as
+// soon as every CTA of that kernel has run griddep_launch_dependents or
+// exited).  Every kernel of this library runs griddep_wait() after its
+// shared-memory / TMEM prologue and before its first global-memory access,
+// so only the prologue and the launch latency overlap the previous kernel.
+// After a kernel that never triggers early (any kernel not from this
+// library) the launch behaves like a plain one.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Descriptor offsets (in the descriptor's 16-byte address units) of the K
 // step kk of a K-major D-wide tile, and of (N chunk nc, K step kk) of an
 // MN-major one, relative to the tile's base descriptor.  Compile-time

@@ -192,12 +192,17 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base_s;
+    // Only shared memory and TMEM were touched so far: from here on global
+    // memory is read and written, so wait for the previous grid in the stream
+    // (programmatic dependent launch).
+    griddep_wait();
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
     // Each role ends with its own teardown: after setmaxnreg the warps run
     // under different register budgets, so their code paths never re-join.
     auto teardown = [&]() {
         tc_fence_before();
         __syncthreads();
+        griddep_launch_dependents();   // this CTA's work is done
         if (warp == 13) {
             tc_fence_after();
             tmem_dealloc(tbase, C::TMEM_COLS);
@@ -768,8 +773,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, cons
     AttnParams p = p0;
     p.num_units = p.M * p.B * p.Hkv * p.nchunks;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
-    kern<<<grid, 512, C::SMEM_BYTES, stream>>>(q, k, v, o, qs, ks, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, o, qs, ks, p);
 }
 
 template <int D, int GC>

@@ -34,6 +34,20 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: block until every grid this
+// one depends on has completed and its memory operations are visible (a
+// no-op when the launch had no such dependency).  griddep_launch_dependents:
+// allow the next grid in the stream to be scheduled once every CTA of this
+// grid has executed it or exited; it grants no memory visibility.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
