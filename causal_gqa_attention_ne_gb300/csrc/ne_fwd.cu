@@ -8,34 +8,31 @@
 // (b, kv head j, query tile m, chunk of GC query heads that share j),
 // heaviest (largest m) first.  Per unit the loop runs over the causal key
 // tiles jk <= m, each split into two halves of 64 keys, and the GC heads:
-// an "item" is (jk, half, g), numbered gi across the CTA's lifetime.  Each
-// K/V tile is loaded once by TMA, rotated once and used by all GC heads.
+// an "item" is one 128 x 64 score block (jk, head, half).  Each K/V tile is
+// loaded once by TMA, rotated once and used by all GC heads.
 // Warp roles (512 threads):
-//   warps 0-3, 4-7  two softmax warpgroups in ping-pong: warpgroup w takes
-//               the items with gi % 2 == w, thread r owns query row r (TMEM
-//               lane r) of the item's 128 x 64 score block.  S buffers are
-//               released as soon as the group has loaded them, so the S
-//               issuer runs up to NSB items ahead, and each group writes P
-//               into a P buffer of its own, so one group's exponentials
-//               overlap the other's TMEM traffic and the MMAs.  The running max and sum
-//               of (head g, row r) live in shared memory; when GC is odd a
-//               head's consecutive items belong to different groups and the
-//               two values pass between them through mbarriers.  The running
-//               max moves lazily (only when it grows by more than 2^8; the
-//               final division by l makes the result exact either way), and
-//               the group that raises it rescales that head's O row in TMEM.
-//               The group that finishes the last item of a head writes O / l
-//               (through shared memory and a TMA store) and lse.
+//   warps 0-3, 4-7  two softmax warpgroups.  The unit's 2*GC (head, key
+//               half) pairs are split between them: group w owns pairs
+//               w*GC .. w*GC+GC-1 (pair 2h + x = head h, keys [64x, 64x+64)
+//               of every key tile), so each group runs its own items with
+//               its running max and sum in registers; thread r owns query
+//               row r (TMEM lane r) of the item's 128 x 64 score block.  For
+//               odd GC one head is split between the groups: each keeps a
+//               partial O, max and sum, merged once at the end of the unit.
+//               The running max moves lazily (only when it grows by more
+//               than 2^8; the final division by l makes the result exact
+//               either way).  P (bf16) is written over its S in TMEM.
 //   warps 8-11  RoPE: rotate the unit's Q tiles and each K tile in place
 //               (bf16 in, fp16 out), in the order the MMAs first need them.
-//   warp 12     TMA producer.   warp 13  TMEM allocator + S issuer.
-//   warp 14     PV issuer.
+//   warp 12     TMA producer.
+//   warps 13, 14  MMA issuers of softmax groups 0 and 1 (warp 13 also
+//               allocates TMEM): S(n) into the group's S buffer n % 2, then
+//               PV(n - 1) reading P from TMEM.
 //   warp 15     training path only: stores each rotated Q' tile and each K'
 //               tile once into the backward's workspace, and tells the
 //               producer when a buffer it stored from may be reloaded.
-// TMEM: NSB S buffers of 64 columns (item gi uses gi % NSB), two P buffers
-// of 32 columns (bf16 pairs; group w uses P_w), then O of head g at
-// COL_O + g*D.
+// TMEM: two 64-column S/P buffers per group (columns 0-255), then the
+// groups' O accumulators (COL_O + (w*NSL + slot)*D).
 #include <cuda_bf16.h>
 
 #include "ne_common.cuh"
@@ -54,7 +51,7 @@ struct FwdPlan {
     static constexpr int QB = (D <= 64) ? 2 : 1;
     static constexpr int fixed_bytes()
     {
-        return QB * GC * TL::BYTES + (STAGE ? 2 * TL::BLOCK : 0) + 2 * GC * kRows * 4 + 1024;
+        return QB * GC * TL::BYTES + (STAGE ? 2 * TL::BLOCK : 0) + 2 * kRows * 4 + 1024;
     }
     static constexpr int stages()
     {
@@ -75,15 +72,15 @@ struct FwdCfg {
     static constexpr int OFF_K = OFF_Q + QB * GC * TL::BYTES;
     static constexpr int OFF_V = OFF_K + ST * TL::BYTES;
     static constexpr int OFF_O = OFF_V + ST * TL::BYTES;      // [2] staging blocks
-    static constexpr int OFF_M = OFF_O + (STAGE ? 2 * TL::BLOCK : 0);   // float [GC][128]
-    static constexpr int OFF_L = OFF_M + GC * kRows * 4;                // float [GC][128]
-    static constexpr int SMEM_BYTES = smem_one_cta(OFF_L + GC * kRows * 4 + 1024);
+    // group 1's running max and sum of the split head: float [2][128]
+    static constexpr int OFF_SPL = OFF_O + (STAGE ? 2 * TL::BLOCK : 0);
+    static constexpr int SMEM_BYTES = smem_one_cta(OFF_SPL + 2 * kRows * 4 + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NSB = (512 - 64 - GC * D) / 64 < 4 ? (512 - 64 - GC * D) / 64 : 4;
-    static constexpr uint32_t COL_P = 64 * NSB;
-    static constexpr uint32_t COL_O = COL_P + 64;
-    static_assert(NSB >= 2, "at least two S buffers");
-    static_assert(COL_O + GC * D <= 512, "TMEM budget");
+    static constexpr int NSL = (GC + 1) / 2;          // O accumulators per softmax group
+    static constexpr bool SPLIT = (GC & 1) != 0;      // one head's key halves in both groups
+    static constexpr uint32_t COL_S = 0;              // S/P buffer b of group w: 128 w + 64 b
+    static constexpr uint32_t COL_O = 256;            // O slot s of group w: COL_O + (w NSL + s) D
+    static_assert(COL_O + 2 * NSL * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448 - 1024, "shared memory budget");
     static_assert(ST >= 2, "K/V double buffering");
     static_assert(!STAGE || TL::NB == 1, "staged epilogue stores one column block per head");
@@ -116,21 +113,16 @@ __global__ void __launch_bounds__(512, 1)
 {
     using C = FwdCfg<D, GC, ST>;
     using TL = Tile<D>;
-    constexpr bool ODD = (GC & 1) != 0;   // a head's items alternate between the groups
-    constexpr int IPT = 2 * GC;           // items per key tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     constexpr int QB = C::QB;
     __shared__ uint64_t bar_q_full[QB][GC], bar_q_ready[QB][GC], bar_q_empty[QB][GC];
     __shared__ uint64_t bar_k_full[ST], bar_k_ready[ST], bar_v_full[ST], bar_kv_empty[ST];
-    constexpr int NSB = C::NSB;
-    __shared__ uint64_t bar_s_full[NSB], bar_s_empty[NSB], bar_p_full[2], bar_p_empty[2];
-    __shared__ uint64_t bar_o_free[GC], bar_drain;
-    // hand-off of the running max / sum: group w's n-th item arrives on
-    // [w][n % 3] (a group is never more than two items past the one its
-    // partner waits for, so the parity of n / 3 is unambiguous)
-    __shared__ uint64_t bar_hm[2][3], bar_hl[2][3];
+    // per softmax group w and S buffer b: S written (MMA commit), P written
+    // (the group's four warps), P read by the PV MMA (commit: buffer free)
+    __shared__ uint64_t bar_s_full[2][2], bar_p_full[2][2], bar_s_free[2][2];
+    __shared__ uint64_t bar_o_free[2][C::NSL], bar_split, bar_drain;
     __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
     // training path: the RoPE warps finished the n-th tile to be stored
     // (ring of 16: they are never 16 such tiles ahead of warp 15, which must
@@ -139,8 +131,6 @@ __global__ void __launch_bounds__(512, 1)
     __shared__ uint64_t bar_sv[16], bar_q_rd[QB][GC], bar_k_rd[ST];
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
-    float *mrun = reinterpret_cast<float *>(smem + C::OFF_M);   // [g][row], log2 units
-    float *lrun = reinterpret_cast<float *>(smem + C::OFF_L);   // [g][row]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cta = static_cast<int>(blockIdx.x), P = static_cast<int>(gridDim.x);
@@ -151,34 +141,29 @@ __global__ void __launch_bounds__(512, 1)
             for (int qb = 0; qb < QB; ++qb) {
                 mbar_init(smem_u32(&bar_q_full[qb][g]), 1);
                 mbar_init(smem_u32(&bar_q_ready[qb][g]), 4);
-                mbar_init(smem_u32(&bar_q_empty[qb][g]), 1);
+                mbar_init(smem_u32(&bar_q_empty[qb][g]), 2);
                 mbar_init(smem_u32(&bar_q_rd[qb][g]), 1);
             }
-            mbar_init(smem_u32(&bar_o_free[g]), 4);
         }
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&bar_k_full[s]), 1);
             mbar_init(smem_u32(&bar_k_ready[s]), 4);
             mbar_init(smem_u32(&bar_v_full[s]), 1);
-            mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+            mbar_init(smem_u32(&bar_kv_empty[s]), 2);
             mbar_init(smem_u32(&bar_k_rd[s]), 1);
         }
-        for (int b = 0; b < NSB; ++b) {
-            mbar_init(smem_u32(&bar_s_full[b]), 1);
-            mbar_init(smem_u32(&bar_s_empty[b]), 4);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bar_p_full[b]), 4);
-            mbar_init(smem_u32(&bar_p_empty[b]), 1);
-        }
         for (int w = 0; w < 2; ++w) {
-            for (int i = 0; i < 3; ++i) {
-                mbar_init(smem_u32(&bar_hm[w][i]), 4);
-                mbar_init(smem_u32(&bar_hl[w][i]), 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&bar_s_full[w][b]), 1);
+                mbar_init(smem_u32(&bar_p_full[w][b]), 4);
+                mbar_init(smem_u32(&bar_s_free[w][b]), 1);
             }
+            for (int sl = 0; sl < C::NSL; ++sl)
+                mbar_init(smem_u32(&bar_o_free[w][sl]), 4);
             mbar_init(smem_u32(&bar_stg_full[w]), 4);
             mbar_init(smem_u32(&bar_stg_free[w]), 1);
         }
+        mbar_init(smem_u32(&bar_split), 4);
         mbar_init(smem_u32(&bar_drain), 2);
         for (int i = 0; i < 16; ++i)
             mbar_init(smem_u32(&bar_sv[i]), 4);
@@ -355,6 +340,10 @@ __global__ void __launch_bounds__(512, 1)
                 bulk_wait0();
         } else if (warp == 13 || warp == 14) {
             // -------------------------------------------------- MMA issuers ---
+            // Warp 13 + w issues the MMAs of softmax group w, in the group's
+            // item order: S(n) into S buffer (w, n % 2), then PV(n - 1).  A
+            // buffer is refilled once PV(n - 2) has read the P written over it.
+            const int wg = warp - 13;
             constexpr uint32_t ID_S = idesc_f16(128, 64, false, false, false);
             constexpr uint32_t ID_PV = idesc_f16(128, TL::NPV, true, false, true);
             constexpr uint32_t TSTEP = TL::BYTES >> 4;
@@ -365,73 +354,90 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t dK0 = desc_kmajor_base<D>(sbase + C::OFF_K);
             const uint64_t dV0 = desc_mnmajor_base<D>(sbase + C::OFF_V);
             bool ok = true;
-            int gi = 0, kt = 0;
+            uint32_t n = 0;
+            int kt = 0;
+            // the previous item, whose PV is issued after the next S
+            struct Pend {
+                int k, st, kt, p;
+                bool first, last_in_tile;
+            } prev{};
+            bool have_prev = false;
+            auto issue_pv = [&](const Pend &x, uint32_t nx) {
+                const int pair = wg * GC + x.p, half = pair & 1;
+                const int slot = (pair >> 1) - ((wg * GC) >> 1);
+                const uint32_t b = nx & 1u;
+                if (!mbar_wait_warp(smem_u32(&bar_p_full[wg][b]), (nx >> 1) & 1, wc) ||
+                    !mbar_wait_warp(smem_u32(&bar_v_full[x.st]), (x.kt / ST) & 1, wc) ||
+                    (x.first && x.k >= 1 &&
+                     !mbar_wait_warp(smem_u32(&bar_o_free[wg][slot]), (x.k - 1) & 1, wc)))
+                    return false;
+                tc_fence_after();
+                const uint64_t vm = dV0 + x.st * TSTEP;
+                const uint32_t ocol = tb + C::COL_O + (wg * C::NSL + slot) * D;
+                const uint32_t pcol = tb + C::COL_S + 128u * wg + 64u * b;
+                if (elect_one()) {
+#pragma unroll
+                    for (int nc = 0; nc < D / TL::NPV; ++nc)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16_ts(ocol + nc * TL::NPV, pcol + 8 * kk,
+                                       vm + mnmajor_off<D>(nc, 4 * half + kk), ID_PV,
+                                       (kk > 0 || !x.first) ? 1u : 0u);
+                    mma_commit(smem_u32(&bar_s_free[wg][b]));
+                    if (x.last_in_tile)
+                        mma_commit(smem_u32(&bar_kv_empty[x.st]));
+                }
+                __syncwarp();
+                return true;
+            };
             for (int k = 0; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
                     break;
                 const FwdUnit w = fwd_unit(u, GC, p);
-                const int nitems = (w.m + 1) * IPT;
-                for (int it = 0; it < nitems; ++it, ++gi) {
-                    const int jk = it / IPT, half = (it / GC) & 1, g = it % GC, st = kt % ST;
-                    const int sb = gi % NSB, pw = gi & 1;
-                    if (warp == 13) {
-                        // S_sb = Q'_g K'[64 half, +64)^T once the operands are
-                        // rotated and buffer sb has been read by its last item
-                        if ((half == 0 && g == 0 &&
+                const int qb = k % QB;
+                for (int jk = 0; jk <= w.m && ok; ++jk, ++kt) {
+                    const int st = kt % ST;
+                    for (int pi = 0; pi < GC; ++pi, ++n) {
+                        const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
+                        const bool first = jk == 0 && (pi == 0 || ((pair - 1) >> 1) != hrel);
+                        const uint32_t b = n & 1u;
+                        // S(n) = Q'_hrel K'[64 half, +64)^T
+                        if ((pi == 0 &&
                              !mbar_wait_warp(smem_u32(&bar_k_ready[st]), (kt / ST) & 1, wc)) ||
-                            (it < GC && !mbar_wait_warp(smem_u32(&bar_q_ready[k % QB][g]),
+                            (jk == 0 && !mbar_wait_warp(smem_u32(&bar_q_ready[qb][hrel]),
                                                         (k / QB) & 1, wc)) ||
-                            (gi >= NSB && !mbar_wait_warp(smem_u32(&bar_s_empty[sb]),
-                                                          ((gi - NSB) / NSB) & 1, wc))) {
+                            (n >= 2 &&
+                             !mbar_wait_warp(smem_u32(&bar_s_free[wg][b]), ((n - 2) >> 1) & 1, wc))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t qd = dQ0 + ((k % QB) * GC + g) * TSTEP;
+                        const uint64_t qd = dQ0 + (qb * GC + hrel) * TSTEP;
                         const uint64_t kd = dK0 + st * TSTEP + half * KHALF;
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_f16_ss(tb + 64u * sb, qd + kmajor_off<D>(kk),
-                                           kd + kmajor_off<D>(kk), ID_S, kk > 0 ? 1u : 0u);
-                            mma_commit(smem_u32(&bar_s_full[sb]));
-                            if (jk == w.m && half == 1)   // last use of head g's Q'
-                                mma_commit(smem_u32(&bar_q_empty[k % QB][g]));
+                                mma_f16_ss(tb + C::COL_S + 128u * wg + 64u * b,
+                                           qd + kmajor_off<D>(kk), kd + kmajor_off<D>(kk), ID_S,
+                                           kk > 0 ? 1u : 0u);
+                            mma_commit(smem_u32(&bar_s_full[wg][b]));
+                            if (jk == w.m && pi == GC - 1)   // last S of the unit
+                                for (int g = 0; g < GC; ++g)
+                                    mma_commit(smem_u32(&bar_q_empty[qb][g]));
                         }
                         __syncwarp();
-                    } else {
-                        // O_g += P_pw V[64 half, +64) once the softmax has written P_pw
-                        if (!mbar_wait_warp(smem_u32(&bar_p_full[pw]), (gi >> 1) & 1, wc) ||
-                            (half == 0 && g == 0 &&
-                             !mbar_wait_warp(smem_u32(&bar_v_full[st]), (kt / ST) & 1, wc)) ||
-                            (it < GC && k >= 1 &&
-                             !mbar_wait_warp(smem_u32(&bar_o_free[g]), (k - 1) & 1, wc))) {
+                        if (have_prev && !issue_pv(prev, n - 1)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        const uint64_t vm = dV0 + st * TSTEP;
-                        const uint32_t first = (it >= GC) ? 1u : 0u;
-                        if (elect_one()) {
-#pragma unroll
-                            for (int nc = 0; nc < D / TL::NPV; ++nc)
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    mma_f16_ts(tb + C::COL_O + g * D + nc * TL::NPV,
-                                               tb + C::COL_P + 32u * pw + 8 * kk,
-                                               vm + mnmajor_off<D>(nc, 4 * half + kk), ID_PV,
-                                               kk > 0 ? 1u : first);
-                            mma_commit(smem_u32(&bar_p_empty[pw]));
-                            if (half == 1 && g == GC - 1)
-                                mma_commit(smem_u32(&bar_kv_empty[st]));
-                        }
-                        __syncwarp();
+                        prev = Pend{k, st, kt, pi, first, pi == GC - 1};
+                        have_prev = true;
                     }
-                    if (half == 1 && g == GC - 1)
-                        ++kt;
                 }
             }
+            if (ok && have_prev)
+                issue_pv(prev, n - 1);
             if (elect_one())
                 mma_commit(smem_u32(&bar_drain));
             __syncwarp();
@@ -499,251 +505,282 @@ __global__ void __launch_bounds__(512, 1)
     }
 
     // ----------------------------------------------------- softmax rows ---
+    // Group wg owns the (head, key half) pairs wg*GC .. wg*GC + GC - 1 of the
+    // unit (pair 2h + x = head h, keys [64x, 64x + 64) of every key tile), so
+    // the running max and sum of each of its heads stay in registers.  With
+    // GC odd one head's two halves belong to different groups; the groups
+    // merge it at the end of the unit (group 0 stores it).
     regs_claim<184>();
-    const int wg = warp >> 2;               // this group's item parity
+    const int wg = warp >> 2;               // softmax group
     const int q4 = warp & 3;                // TMEM lane quarter
     const int r = threadIdx.x & 127;        // query row == TMEM lane
     const uint32_t lane_base = tmem_addr(tbase, q4 * 32, 0);
     const float sl2 = p.scale_log2;
     uint8_t *stage = smem + C::OFF_O + wg * TL::BLOCK;
+    float *split_ml = reinterpret_cast<float *>(smem + C::OFF_SPL);   // [m | l][row]
     bool ok = true;
-    int gi = 0;
-    uint32_t nepi = 0;       // epilogues this group has run
+    uint32_t n = 0;          // this group's items so far
+    uint32_t nepi = 0;       // O stores this group has issued
+    float mr0 = 0.f, mr1 = 0.f, lr0 = 0.f, lr1 = 0.f;   // running max (log2 units) / sum per slot
+    // Writes O_slot / l of head h (rows of this thread) and its lse.  With a
+    // second accumulator (merge), O = (O_a * sa + O_b * sb) * inv_l.
+    auto store_head = [&](const FwdUnit &un, int h, uint32_t oa, bool merge, uint32_t ob, float sa,
+                          float sb, float inv_l, float lse2) -> bool {
+        const int t = un.m * kRows + r;
+        if constexpr (C::STAGE) {
+            // the staging block is free once this group's previous store
+            // has read it
+            if (nepi >= 1) {
+                if (warp == 4 * wg && lane == 0) {
+                    bulk_wait_read0();
+                    mbar_arrive(smem_u32(&bar_stg_free[wg]));
+                }
+                if (!mbar_wait_warp(smem_u32(&bar_stg_free[wg]), (nepi - 1) & 1, wc))
+                    return false;
+            }
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(oa + c, o);
+                tmem_ld_wait(o);
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    x[e] = __uint_as_float(o[e]) * sa;
+                if (merge) {
+                    tmem_ld32(ob + c, o);
+                    tmem_ld_wait(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        x[e] = fmaf(__uint_as_float(o[e]), sb, x[e]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c / 8 + q)) =
+                        make_uint4(pack_bf16x2(x[8 * q + 0] * inv_l, x[8 * q + 1] * inv_l),
+                                   pack_bf16x2(x[8 * q + 2] * inv_l, x[8 * q + 3] * inv_l),
+                                   pack_bf16x2(x[8 * q + 4] * inv_l, x[8 * q + 5] * inv_l),
+                                   pack_bf16x2(x[8 * q + 6] * inv_l, x[8 * q + 7] * inv_l));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&bar_stg_full[wg]));
+            if (warp == 4 * wg) {
+                if (!mbar_wait_warp(smem_u32(&bar_stg_full[wg]), nepi & 1, wc))
+                    return false;
+                if (lane == 0) {
+                    tma_store_4d(&tmO, smem_u32(stage), 0, h, un.m * kRows, un.b);
+                    bulk_commit();
+                }
+                __syncwarp();
+            }
+            ++nepi;
+        } else {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out0) +
+                                 ((static_cast<size_t>(un.b) * p.T + t) * p.Hq + h) * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(oa + c, o);
+                tmem_ld_wait(o);
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    x[e] = __uint_as_float(o[e]) * sa;
+                if (merge) {
+                    tmem_ld32(ob + c, o);
+                    tmem_ld_wait(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        x[e] = fmaf(__uint_as_float(o[e]), sb, x[e]);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    x[e] *= inv_l;
+                if (t < p.T)
+                    store_row32_bf16(dst + c, x);
+            }
+        }
+        if (t < p.T)
+            p.lse[(static_cast<size_t>(un.b) * p.Hq + h) * p.T + t] = lse2 * kLn2;
+        return true;
+    };
     for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, P);
         if (u >= p.num_units)
             break;
         const FwdUnit un = fwd_unit(u, GC, p);
-        const int nitems = (un.m + 1) * IPT;
-        for (int it = 0; it < nitems; ++it, ++gi) {
-            if ((gi & 1) != wg)
-                continue;
-            const uint32_t n = static_cast<uint32_t>(gi) >> 1;   // this group's item count
-            const int jk = it / IPT, half = (it / GC) & 1, g = it % GC;
-            const int pos = 2 * jk + half;                        // head g's item in the unit
-            const int sb = gi % NSB;
-            const uint32_t s_addr = lane_base + 64u * sb;
-            const uint32_t p_addr = lane_base + C::COL_P + 32u * wg;
-            // the previous item of head g ran on the other group (odd GC)
-            const int xprev = gi - GC;
-            const bool handoff = ODD && xprev >= 0;
-            const uint32_t xa = static_cast<uint32_t>(xprev) >> 1;   // its index there
-            if (!mbar_wait_warp(smem_u32(&bar_s_full[sb]), (gi / NSB) & 1, wc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t s[2][32];
-            tmem_ld32(s_addr, s[0]);
-            tmem_ld32(s_addr + 32, s[1]);
-            tmem_ld_wait_only();
-            tmem_tie(s[0]);
-            tmem_tie(s[1]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_s_empty[sb]));
-
-            // causal mask on the diagonal tile (key > query row)
-            if (jk == un.m) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (64 * half + 32 * c + e > r)
-                            s[c][e] = __float_as_uint(-INFINITY);
-            }
-            float mx;
-            {
-                float m2[2];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    m2[c] = fmaxf(__uint_as_float(s[c][0]), __uint_as_float(s[c][1]));
-#pragma unroll
-                    for (int e = 2; e < 32; e += 2)
-                        m2[c] = fmax3(m2[c], __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
-                }
-                mx = fmaxf(m2[0], m2[1]);
-            }
-            const float m_tile = mx * sl2;
-
-            // running max of (head g, row r): read, move lazily, publish
-            if (handoff &&
-                !mbar_wait_warp(smem_u32(&bar_hm[xprev & 1][xa % 3]), (xa / 3) & 1, wc)) {
-                ok = false;
-                break;
-            }
-            float m_use = m_tile, alpha = 1.f;
-            bool resc = false;
-            if (pos > 0) {
-                const float m_prev = mrun[g * kRows + r];
-                m_use = m_prev;
-                if (m_tile > m_prev + 8.f) {
-                    alpha = ex2_approx(m_prev - m_tile);
-                    m_use = m_tile;
-                    resc = true;
-                }
-            }
-            mrun[g * kRows + r] = m_use;
-            if (ODD) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&bar_hm[wg][n % 3]));
-            }
-
-            // P = 2^(S*scale*log2e - m) as bf16 pairs into P_wg
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-            {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][e]), sl2, -m_use));
-                        const float p1 =
-                            ex2_approx(fmaf(__uint_as_float(s[c][e + 1]), sl2, -m_use));
-                        sum4[(e >> 1) & 3] += p0 + p1;
-                        pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
-                    }
-                // P_wg is free once PV(gi - 2) has completed (this group's
-                // previous item; the one before was waited for then, so the
-                // parity is exact)
-                if (gi >= 2 &&
-                    !mbar_wait_warp(smem_u32(&bar_p_empty[wg]), ((gi - 2) >> 1) & 1, wc)) {
+        for (int jk = 0; jk <= un.m && ok; ++jk) {
+            for (int pi = 0; pi < GC; ++pi, ++n) {
+                const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
+                const int slot = hrel - ((wg * GC) >> 1);
+                const bool first = jk == 0 && (pi == 0 || ((pair - 1) >> 1) != hrel);
+                const uint32_t b = n & 1u;
+                const uint32_t s_addr = lane_base + C::COL_S + 128u * wg + 64u * b;
+                if (!mbar_wait_warp(smem_u32(&bar_s_full[wg][b]), (n >> 1) & 1, wc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                tmem_st32(p_addr, pk);
+                uint32_t s[2][32];
+                tmem_ld32(s_addr, s[0]);
+                tmem_ld32(s_addr + 32, s[1]);
+                tmem_ld_wait_only();
+                tmem_tie(s[0]);
+                tmem_tie(s[1]);
+
+                // causal mask on the diagonal tile (key > query row)
+                if (jk == un.m) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (64 * half + 32 * c + e > r)
+                                s[c][e] = __float_as_uint(-INFINITY);
+                }
+                float mx;
+                {
+                    float m2[2];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        m2[c] = fmaxf(__uint_as_float(s[c][0]), __uint_as_float(s[c][1]));
+#pragma unroll
+                        for (int e = 2; e < 32; e += 2)
+                            m2[c] = fmax3(m2[c], __uint_as_float(s[c][e]),
+                                          __uint_as_float(s[c][e + 1]));
+                    }
+                    mx = fmaxf(m2[0], m2[1]);
+                }
+                const float m_tile = mx * sl2;
+                // running max: moves lazily, only when it grows by more than
+                // 2^8 (the final division by l makes the result exact either
+                // way); a row with no visible key in its items so far keeps -inf
+                float m_use = m_tile, alpha = 1.f;
+                bool resc = false;
+                if (!first) {
+                    const float m_prev = slot ? mr1 : mr0;
+                    m_use = m_prev;
+                    if (m_tile > m_prev + 8.f) {
+                        alpha = ex2_approx(m_prev - m_tile);
+                        m_use = m_tile;
+                        resc = true;
+                    }
+                }
+                if (slot)
+                    mr1 = m_use;
+                else
+                    mr0 = m_use;
+                const float m_exp = m_use == -INFINITY ? 0.f : m_use;
+
+                // P = 2^(S*scale*log2e - m) as bf16 pairs, written over S
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][e]), sl2, -m_exp));
+                            const float p1 =
+                                ex2_approx(fmaf(__uint_as_float(s[c][e + 1]), sl2, -m_exp));
+                            sum4[(e >> 1) & 3] += p0 + p1;
+                            pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
+                        }
+                    tmem_st32(s_addr, pk);
+                }
+                const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O_slot must hold every earlier PV of this group before it
+                    // is rescaled: wait for PV(n - 1) (its commit covers all of
+                    // this issuer's earlier MMAs)
+                    if (!mbar_wait_warp(smem_u32(&bar_s_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1,
+                                        wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t oa = lane_base + C::COL_O + (wg * C::NSL + slot) * D;
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(oa + c, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(oa + c, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_p_full[wg][b]));
+                if (first) {
+                    if (slot)
+                        lr1 = sum;
+                    else
+                        lr0 = sum;
+                } else if (slot) {
+                    lr1 = fmaf(lr1, alpha, sum);
+                } else {
+                    lr0 = fmaf(lr0, alpha, sum);
+                }
             }
-            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-            if (__any_sync(0xffffffffu, resc)) {
-                // O_g must hold the previous item of head g (gi - GC) before it
-                // is rescaled.  PVs complete in order, so for GC >= 2 the wait
-                // for PV(gi - 2) above covers it; for GC == 1 it is the other
-                // group's PV(gi - 1) (PV(gi - 3) is complete, parity exact).
-                if (GC == 1 &&
-                    !mbar_wait_warp(smem_u32(&bar_p_empty[wg ^ 1]), ((gi - 1) >> 1) & 1, wc)) {
+        }
+        if (!ok)
+            break;
+
+        // ---- end of the unit: O / l and lse of this group's heads ----
+        // every PV of the unit has completed once PV(n - 1) has
+        if (!mbar_wait_warp(smem_u32(&bar_s_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1, wc)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        for (int slot = 0; slot < C::NSL && ok; ++slot) {
+            const int h = un.h0 + ((wg * GC) >> 1) + slot;
+            const float m_s = slot ? mr1 : mr0, l_s = slot ? lr1 : lr0;
+            const uint32_t oa = lane_base + C::COL_O + (wg * C::NSL + slot) * D;
+            const bool split = C::SPLIT && (wg == 0 ? slot == C::NSL - 1 : slot == 0);
+            if (split && wg == 1) {
+                // hand this half's max and sum to group 0, which merges and
+                // stores the head
+                split_ml[r] = m_s;
+                split_ml[kRows + r] = l_s;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_split));
+                continue;
+            }
+            float sa = 1.f, sb = 0.f, l_tot = l_s, m_tot = m_s;
+            uint32_t ob = 0u;
+            if (split) {
+                if (!mbar_wait_warp(smem_u32(&bar_split), k & 1, wc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t oa = lane_base + C::COL_O + g * D;
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(oa + c, o);
-                    tmem_ld_wait(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(oa + c, o);
-                }
+                const float m1 = split_ml[r], l1 = split_ml[kRows + r];
+                m_tot = fmaxf(m_s, m1);
+                sa = ex2_approx(m_s - m_tot);
+                sb = ex2_approx(m1 - m_tot);   // 0 when that half saw no key
+                l_tot = fmaf(l_s, sa, l1 * sb);
+                ob = lane_base + C::COL_O + (1 * C::NSL + 0) * D;
             }
-            tmem_st_wait();
+            const float inv_l = 1.f / l_tot;
+            if (!store_head(un, h, oa, split, ob, sa, sb, inv_l, m_tot + __log2f(l_tot))) {
+                ok = false;
+                break;
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_p_full[wg]));
-
-            // running sum of (head g, row r)
-            if (handoff &&
-                !mbar_wait_warp(smem_u32(&bar_hl[xprev & 1][xa % 3]), (xa / 3) & 1, wc)) {
-                ok = false;
-                break;
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&bar_o_free[wg][slot]));
+                if (split)
+                    mbar_arrive(smem_u32(&bar_o_free[1][0]));
             }
-            const float l_now = (pos > 0 ? lrun[g * kRows + r] * alpha : 0.f) + sum;
-            lrun[g * kRows + r] = l_now;
-            if (ODD) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&bar_hl[wg][n % 3]));
-            }
-            if (jk != un.m || half != 1)
-                continue;
-
-            // ---- last item of head g in this unit: O_g / l and lse ----
-            if (!mbar_wait_warp(smem_u32(&bar_p_empty[wg]), (gi >> 1) & 1, wc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float inv_l = 1.f / l_now;
-            const int h = un.h0 + g;
-            const int t = un.m * kRows + r;
-            const uint32_t oa = lane_base + C::COL_O + g * D;
-            if constexpr (C::STAGE) {
-                // the staging block is free once this group's previous
-                // store has read it
-                if (nepi >= 1) {
-                    if (warp == 4 * wg && lane == 0) {
-                        bulk_wait_read0();
-                        mbar_arrive(smem_u32(&bar_stg_free[wg]));
-                    }
-                    if (!mbar_wait_warp(smem_u32(&bar_stg_free[wg]), (nepi - 1) & 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(oa + c, o);
-                    tmem_ld_wait(o);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c / 8 + q)) =
-                            make_uint4(pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l,
-                                                   __uint_as_float(o[8 * q + 1]) * inv_l),
-                                       pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l,
-                                                   __uint_as_float(o[8 * q + 3]) * inv_l),
-                                       pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l,
-                                                   __uint_as_float(o[8 * q + 5]) * inv_l),
-                                       pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l,
-                                                   __uint_as_float(o[8 * q + 7]) * inv_l));
-                }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(smem_u32(&bar_o_free[g]));
-                    mbar_arrive(smem_u32(&bar_stg_full[wg]));
-                }
-                if (warp == 4 * wg) {
-                    if (!mbar_wait_warp(smem_u32(&bar_stg_full[wg]), nepi & 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        tma_store_4d(&tmO, smem_u32(stage), 0, h, un.m * kRows, un.b);
-                        bulk_commit();
-                    }
-                    __syncwarp();
-                }
-            } else {
-                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out0) +
-                                     ((static_cast<size_t>(un.b) * p.T + t) * p.Hq + h) * D;
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(oa + c, o);
-                    tmem_ld_wait(o);
-                    float x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        x[e] = __uint_as_float(o[e]) * inv_l;
-                    if (t < p.T)
-                        store_row32_bf16(dst + c, x);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&bar_o_free[g]));
-            }
-            if (t < p.T)
-                p.lse[(static_cast<size_t>(un.b) * p.Hq + h) * p.T + t] =
-                    (m_use + __log2f(l_now)) * kLn2;
-            ++nepi;
         }
     }
     if constexpr (C::STAGE) {
@@ -752,7 +789,6 @@ __global__ void __launch_bounds__(512, 1)
     }
     teardown();
 }
-
 // ------------------------------------------------------------- launch ---
 
 template <int D, int GC, int ST>
