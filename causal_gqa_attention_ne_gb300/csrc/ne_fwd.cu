@@ -21,18 +21,21 @@
 //               partial O, max and sum, merged once at the end of the unit.
 //               The running max moves lazily (only when it grows by more
 //               than 2^8; the final division by l makes the result exact
-//               either way).  P (bf16) is written over its S in TMEM.
+//               either way).  Each group has one S buffer, released as soon
+//               as the group has loaded it (so S(n+1) is computed while the
+//               group works on item n), and two P buffers.
 //   warps 8-11  RoPE: rotate the unit's Q tiles and each K tile in place
 //               (bf16 in, fp16 out), in the order the MMAs first need them.
 //   warp 12     TMA producer.
 //   warps 13, 14  MMA issuers of softmax groups 0 and 1 (warp 13 also
-//               allocates TMEM): S(n) into the group's S buffer n % 2, then
-//               PV(n - 1) reading P from TMEM.
+//               allocates TMEM): S(n) into the group's S buffer, then
+//               PV(n - 1) reading P from the group's P buffer (n - 1) % 2.
 //   warp 15     training path only: stores each rotated Q' tile and each K'
 //               tile once into the backward's workspace, and tells the
 //               producer when a buffer it stored from may be reloaded.
-// TMEM: two 64-column S/P buffers per group (columns 0-255), then the
-// groups' O accumulators (COL_O + (w*NSL + slot)*D).
+// TMEM: one 64-column S buffer per group (columns 0-127), two 32-column P
+// buffers per group (bf16 pairs, columns 128-255), then the groups' O
+// accumulators (COL_O + (w*NSL + slot)*D).
 #include <cuda_bf16.h>
 
 #include "ne_common.cuh"
@@ -78,7 +81,8 @@ struct FwdCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NSL = (GC + 1) / 2;          // O accumulators per softmax group
     static constexpr bool SPLIT = (GC & 1) != 0;      // one head's key halves in both groups
-    static constexpr uint32_t COL_S = 0;              // S/P buffer b of group w: 128 w + 64 b
+    static constexpr uint32_t COL_S = 0;              // S buffer of group w: 64 w
+    static constexpr uint32_t COL_P = 128;            // P buffer b of group w: COL_P + 64 w + 32 b
     static constexpr uint32_t COL_O = 256;            // O slot s of group w: COL_O + (w NSL + s) D
     static_assert(COL_O + 2 * NSL * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448 - 1024, "shared memory budget");
@@ -119,9 +123,10 @@ __global__ void __launch_bounds__(512, 1)
     constexpr int QB = C::QB;
     __shared__ uint64_t bar_q_full[QB][GC], bar_q_ready[QB][GC], bar_q_empty[QB][GC];
     __shared__ uint64_t bar_k_full[ST], bar_k_ready[ST], bar_v_full[ST], bar_kv_empty[ST];
-    // per softmax group w and S buffer b: S written (MMA commit), P written
-    // (the group's four warps), P read by the PV MMA (commit: buffer free)
-    __shared__ uint64_t bar_s_full[2][2], bar_p_full[2][2], bar_s_free[2][2];
+    // per softmax group w: S written (MMA commit), S loaded by the group (its
+    // four warps); per P buffer b: P written (four warps), P read by the PV
+    // MMA (commit)
+    __shared__ uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[2][2], bar_p_free[2][2];
     __shared__ uint64_t bar_o_free[2][C::NSL], bar_split, bar_drain;
     __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
     // training path: the RoPE warps finished the n-th tile to be stored
@@ -153,10 +158,11 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(smem_u32(&bar_k_rd[s]), 1);
         }
         for (int w = 0; w < 2; ++w) {
+            mbar_init(smem_u32(&bar_s_full[w]), 1);
+            mbar_init(smem_u32(&bar_s_empty[w]), 4);
             for (int b = 0; b < 2; ++b) {
-                mbar_init(smem_u32(&bar_s_full[w][b]), 1);
                 mbar_init(smem_u32(&bar_p_full[w][b]), 4);
-                mbar_init(smem_u32(&bar_s_free[w][b]), 1);
+                mbar_init(smem_u32(&bar_p_free[w][b]), 1);
             }
             for (int sl = 0; sl < C::NSL; ++sl)
                 mbar_init(smem_u32(&bar_o_free[w][sl]), 4);
@@ -198,11 +204,15 @@ __global__ void __launch_bounds__(512, 1)
     // softmax 184 x 256 + RoPE 80 x 128 + TMA/MMA 64 x 128 = 65536.
     if (warp >= 12) {
         regs_release<64>();
-        if (warp == 12 && lane == 0) {
+        if (warp == 12) {
             // ------------------------------------------------ TMA producer ---
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+            // The whole warp waits (a suspended warp leaves the issue slots to
+            // the softmax warps); lane 0 issues the copies.
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+            }
             bool ok = true;
             int kt = 0;
             int qloads[QB][GC] = {};   // loads issued per Q slot (for the abort drain)
@@ -212,18 +222,21 @@ __global__ void __launch_bounds__(512, 1)
                 const FwdUnit w = fwd_unit(snake_unit(kk, cta, P), GC, p);
                 const int qb = kk % QB, use = kk / QB;
                 for (int g = 0; g < GC; ++g) {
-                    if (use >= 1 && !mbar_wait(smem_u32(&bar_q_empty[qb][g]), (use - 1) & 1, wc))
+                    if (use >= 1 && !mbar_wait_warp(smem_u32(&bar_q_empty[qb][g]), (use - 1) & 1, wc))
                         return false;
                     // training path: the previous tile of this slot was stored
                     if (p.save_rot && use >= 1 &&
-                        !mbar_wait(smem_u32(&bar_q_rd[qb][g]), (use - 1) & 1, wc))
+                        !mbar_wait_warp(smem_u32(&bar_q_rd[qb][g]), (use - 1) & 1, wc))
                         return false;
                     const uint32_t bar = smem_u32(&bar_q_full[qb][g]);
-                    mbar_arrive_expect_tx(bar, TL::BYTES);
-                    for (int cb = 0; cb < TL::NB; ++cb)
-                        tma_load_4d(smem_u32(smem + C::OFF_Q + (qb * GC + g) * TL::BYTES +
-                                             cb * TL::BLOCK),
-                                    &tmQ, bar, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar, TL::BYTES);
+                        for (int cb = 0; cb < TL::NB; ++cb)
+                            tma_load_4d(smem_u32(smem + C::OFF_Q + (qb * GC + g) * TL::BYTES +
+                                                 cb * TL::BLOCK),
+                                        &tmQ, bar, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                    }
+                    __syncwarp();
                     ++qloads[qb][g];
                 }
                 return true;
@@ -234,23 +247,26 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t last_saved = 0;
             auto load_kv = [&](const FwdUnit &w, int jk) {
                 const int st = kt % ST, u2 = kt / ST;
-                if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc))
+                if (u2 >= 1 && !mbar_wait_warp(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc))
                     return false;
                 if (((last_saved >> st) & 1u) &&
-                    !mbar_wait(smem_u32(&bar_k_rd[st]), (ksaved[st] - 1) & 1, wc))
+                    !mbar_wait_warp(smem_u32(&bar_k_rd[st]), (ksaved[st] - 1) & 1, wc))
                     return false;
                 const bool saved = p.save_rot && jk == w.m && w.h0 == w.j * p.G;
                 last_saved = (last_saved & ~(1u << st)) | (saved ? 1u << st : 0u);
                 ksaved[st] += saved ? 1 : 0;
                 const uint32_t kb = smem_u32(&bar_k_full[st]), vb = smem_u32(&bar_v_full[st]);
-                mbar_arrive_expect_tx(kb, TL::BYTES);
-                for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK), &tmK,
-                                kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
-                mbar_arrive_expect_tx(vb, TL::BYTES);
-                for (int cb = 0; cb < TL::NB; ++cb)
-                    tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK), &tmV,
-                                vb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(kb, TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb)
+                        tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmK, kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                    mbar_arrive_expect_tx(vb, TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb)
+                        tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmV, vb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                }
+                __syncwarp();
                 ++kt;
                 return true;
             };
@@ -269,7 +285,7 @@ __global__ void __launch_bounds__(512, 1)
                 for (int jk = 1; jk <= w.m && ok; ++jk)
                     ok = load_kv(w, jk);
             }
-            if (*wc.abort) {
+            if (*wc.abort && lane == 0) {
                 for (int qb = 0; qb < QB; ++qb)
                     for (int g = 0; g < GC; ++g)
                         if (qloads[qb][g] > 0)
@@ -341,8 +357,10 @@ __global__ void __launch_bounds__(512, 1)
         } else if (warp == 13 || warp == 14) {
             // -------------------------------------------------- MMA issuers ---
             // Warp 13 + w issues the MMAs of softmax group w, in the group's
-            // item order: S(n) into S buffer (w, n % 2), then PV(n - 1).  A
-            // buffer is refilled once PV(n - 2) has read the P written over it.
+            // item order: S(n) into the group's S buffer once the group has
+            // loaded S(n - 1), then PV(n - 1) once P(n - 1) is written; at a
+            // unit boundary the previous unit's last PV goes first (its
+            // epilogue waits for it; S(n) waits for the new unit's tiles).
             const int wg = warp - 13;
             constexpr uint32_t ID_S = idesc_f16(128, 64, false, false, false);
             constexpr uint32_t ID_PV = idesc_f16(128, TL::NPV, true, false, true);
@@ -374,7 +392,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const uint64_t vm = dV0 + x.st * TSTEP;
                 const uint32_t ocol = tb + C::COL_O + (wg * C::NSL + slot) * D;
-                const uint32_t pcol = tb + C::COL_S + 128u * wg + 64u * b;
+                const uint32_t pcol = tb + C::COL_P + 64u * wg + 32u * b;
                 if (elect_one()) {
 #pragma unroll
                     for (int nc = 0; nc < D / TL::NPV; ++nc)
@@ -383,7 +401,7 @@ __global__ void __launch_bounds__(512, 1)
                             mma_f16_ts(ocol + nc * TL::NPV, pcol + 8 * kk,
                                        vm + mnmajor_off<D>(nc, 4 * half + kk), ID_PV,
                                        (kk > 0 || !x.first) ? 1u : 0u);
-                    mma_commit(smem_u32(&bar_s_free[wg][b]));
+                    mma_commit(smem_u32(&bar_p_free[wg][b]));
                     if (x.last_in_tile)
                         mma_commit(smem_u32(&bar_kv_empty[x.st]));
                 }
@@ -401,14 +419,20 @@ __global__ void __launch_bounds__(512, 1)
                     for (int pi = 0; pi < GC; ++pi, ++n) {
                         const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
                         const bool first = jk == 0 && (pi == 0 || ((pair - 1) >> 1) != hrel);
-                        const uint32_t b = n & 1u;
+                        if (jk == 0 && pi == 0 && have_prev) {
+                            if (!issue_pv(prev, n - 1)) {
+                                ok = false;
+                                break;
+                            }
+                            have_prev = false;
+                        }
                         // S(n) = Q'_hrel K'[64 half, +64)^T
                         if ((pi == 0 &&
                              !mbar_wait_warp(smem_u32(&bar_k_ready[st]), (kt / ST) & 1, wc)) ||
                             (jk == 0 && !mbar_wait_warp(smem_u32(&bar_q_ready[qb][hrel]),
                                                         (k / QB) & 1, wc)) ||
-                            (n >= 2 &&
-                             !mbar_wait_warp(smem_u32(&bar_s_free[wg][b]), ((n - 2) >> 1) & 1, wc))) {
+                            (n >= 1 &&
+                             !mbar_wait_warp(smem_u32(&bar_s_empty[wg]), (n - 1) & 1, wc))) {
                             ok = false;
                             break;
                         }
@@ -418,10 +442,10 @@ __global__ void __launch_bounds__(512, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_f16_ss(tb + C::COL_S + 128u * wg + 64u * b,
+                                mma_f16_ss(tb + C::COL_S + 64u * wg,
                                            qd + kmajor_off<D>(kk), kd + kmajor_off<D>(kk), ID_S,
                                            kk > 0 ? 1u : 0u);
-                            mma_commit(smem_u32(&bar_s_full[wg][b]));
+                            mma_commit(smem_u32(&bar_s_full[wg]));
                             if (jk == w.m && pi == GC - 1)   // last S of the unit
                                 for (int g = 0; g < GC; ++g)
                                     mma_commit(smem_u32(&bar_q_empty[qb][g]));
@@ -617,8 +641,9 @@ __global__ void __launch_bounds__(512, 1)
                 const int slot = hrel - ((wg * GC) >> 1);
                 const bool first = jk == 0 && (pi == 0 || ((pair - 1) >> 1) != hrel);
                 const uint32_t b = n & 1u;
-                const uint32_t s_addr = lane_base + C::COL_S + 128u * wg + 64u * b;
-                if (!mbar_wait_warp(smem_u32(&bar_s_full[wg][b]), (n >> 1) & 1, wc)) {
+                const uint32_t s_addr = lane_base + C::COL_S + 64u * wg;
+                const uint32_t p_addr = lane_base + C::COL_P + 64u * wg + 32u * b;
+                if (!mbar_wait_warp(smem_u32(&bar_s_full[wg]), n & 1, wc)) {
                     ok = false;
                     break;
                 }
@@ -629,6 +654,10 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_ld_wait_only();
                 tmem_tie(s[0]);
                 tmem_tie(s[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_s_empty[wg]));
 
                 // causal mask on the diagonal tile (key > query row)
                 if (jk == un.m) {
@@ -673,28 +702,47 @@ __global__ void __launch_bounds__(512, 1)
                     mr0 = m_use;
                 const float m_exp = m_use == -INFINITY ? 0.f : m_use;
 
-                // P = 2^(S*scale*log2e - m) as bf16 pairs, written over S
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                // P = 2^(S*scale*log2e - m) as bf16 pairs into P buffer b; the
+                // exponent arguments and the row sum run on packed fp32 pairs
+                uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
                 {
                     uint32_t pk[32];
+                    const uint64_t sl2x2 = f32x2(sl2, sl2), nm2 = f32x2(-m_exp, -m_exp);
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][e]), sl2, -m_exp));
-                            const float p1 =
-                                ex2_approx(fmaf(__uint_as_float(s[c][e + 1]), sl2, -m_exp));
-                            sum4[(e >> 1) & 3] += p0 + p1;
+                            const uint64_t x2 = fma_f32x2(
+                                f32x2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])),
+                                sl2x2, nm2);
+                            float x0, x1;
+                            f32x2_split(x2, x0, x1);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            sum2[(e >> 1) & 3] = add_f32x2(sum2[(e >> 1) & 3], f32x2(p0, p1));
                             pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
                         }
-                    tmem_st32(s_addr, pk);
+                    // buffer b is free once PV(n - 2) has read it
+                    if (n >= 2 &&
+                        !mbar_wait_warp(smem_u32(&bar_p_free[wg][b]), ((n - 2) >> 1) & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tmem_st32(p_addr, pk);
                 }
-                const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                float sum;
+                {
+                    const uint64_t s01 = add_f32x2(sum2[0], sum2[1]);
+                    const uint64_t s23 = add_f32x2(sum2[2], sum2[3]);
+                    float a0, a1;
+                    f32x2_split(add_f32x2(s01, s23), a0, a1);
+                    sum = a0 + a1;
+                }
                 if (__any_sync(0xffffffffu, resc)) {
                     // O_slot must hold every earlier PV of this group before it
                     // is rescaled: wait for PV(n - 1) (its commit covers all of
                     // this issuer's earlier MMAs)
-                    if (!mbar_wait_warp(smem_u32(&bar_s_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1,
+                    if (!mbar_wait_warp(smem_u32(&bar_p_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1,
                                         wc)) {
                         ok = false;
                         break;
@@ -734,7 +782,7 @@ __global__ void __launch_bounds__(512, 1)
 
         // ---- end of the unit: O / l and lse of this group's heads ----
         // every PV of the unit has completed once PV(n - 1) has
-        if (!mbar_wait_warp(smem_u32(&bar_s_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1, wc)) {
+        if (!mbar_wait_warp(smem_u32(&bar_p_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1, wc)) {
             ok = false;
             break;
         }
