@@ -131,9 +131,79 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
     griddep_launch_dependents();
 }
 
+// D alone (Q' and K' already in the workspace): a pure streaming pass over O
+// and dO.  A row of D/8 16-byte chunks is read by D/8 consecutive lanes, so
+// one warp-wide load covers 32 / (D/8) whole rows; RU such loads of O and of
+// dO are in flight per lane before the row sums are reduced with shuffles.
+// Persistent: the grid is a multiple of the SM count and strides over rows.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_d_kernel(const AttnParams p)
+{
+    constexpr int LPR = D / 8;                 // lanes per row (one 16-byte chunk each)
+    constexpr int RPW = 32 / LPR;              // rows per warp-wide load
+    constexpr int RU = 4;                      // loads of each tensor in flight per lane
+    const size_t nrows = static_cast<size_t>(p.B) * p.T * p.Hq;
+    const uint4 *o = static_cast<const uint4 *>(p.o_in);
+    const uint4 *g = static_cast<const uint4 *>(p.do_in);
+    const int lane = threadIdx.x % 32;
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const size_t nwarps = static_cast<size_t>(gridDim.x) * blockDim.x / 32;
+    griddep_wait();   // O comes from the previous grid
+    for (size_t r0 = warp * RPW * RU; r0 < nrows; r0 += nwarps * RPW * RU) {
+        uint4 ov[RU], gv[RU];
+#pragma unroll
+        for (int i = 0; i < RU; ++i) {
+            const size_t row = r0 + i * RPW + lane / LPR;
+            if (row < nrows) {
+                const size_t c = row * LPR + lane % LPR;
+                ov[i] = ld_stream(o + c);
+                gv[i] = ld_stream(g + c);
+            } else {
+                ov[i] = make_uint4(0u, 0u, 0u, 0u);
+                gv[i] = ov[i];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RU; ++i) {
+            const uint32_t oa[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
+            const uint32_t ga[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc = fmaf(bf16_hi(oa[e]), bf16_hi(ga[e]), fmaf(bf16_lo(oa[e]), bf16_lo(ga[e]), acc));
+#pragma unroll
+            for (int off = LPR / 2; off >= 1; off /= 2)
+                acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const size_t row = r0 + i * RPW + lane / LPR;   // ((b*T + t)*Hq + h)
+            if (lane % LPR == 0 && row < nrows) {
+                const int h = static_cast<int>(row % p.Hq);
+                const size_t bt = row / p.Hq;
+                const int t = static_cast<int>(bt % p.T);
+                const int b = static_cast<int>(bt / p.T);
+                p.Dws[(static_cast<size_t>(b) * p.Hq + h) * p.T + t] = acc;
+            }
+        }
+    }
+    griddep_launch_dependents();
+}
+
 cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot, const void *k,
                            void *krot, cudaStream_t stream)
 {
+    if (qrot == nullptr) {
+        int dev = 0, sms = 0;
+        cudaError_t e;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        const unsigned nb = static_cast<unsigned>(sms * 8);
+        switch (d) {
+        case 32: return launch_pdl(bwd_d_kernel<32>, nb, 256, 0, stream, p);
+        case 64: return launch_pdl(bwd_d_kernel<64>, nb, 256, 0, stream, p);
+        case 128: return launch_pdl(bwd_d_kernel<128>, nb, 256, 0, stream, p);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     const size_t nthreads = static_cast<size_t>(p.B) * p.T * p.Hq * (d / 16);
     size_t blocks = (nthreads + 255) / 256;
     // With the rotations, a grid-stride loop over a capped grid (the K'

@@ -165,6 +165,16 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 
 // ------------------------------------------------------------------ TMA ---
 
+// 16-byte read-only load that is not kept in L1 (a pure streaming pass).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
