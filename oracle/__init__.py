@@ -57,6 +57,9 @@ def _bind(path: str):
     lib.ne_oracle_bwd.restype = ctypes.c_int
     lib.ne_oracle_bwd.argtypes = [_DP] * 10 + [ctypes.c_int] * 5 + [
         ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_decode.restype = ctypes.c_int
+    lib.ne_oracle_decode.argtypes = [_DP] * 5 + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_long]
     lib.ne_oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -125,6 +128,24 @@ class Oracle:
         return {"dq": dq, "dk": dk, "dv": dv, "o": o, "lse": lse, "D": D}
 
 
+    def attn_decode(self, q1, k, v, theta: float, pos_offset: int = 0):
+        """One new token per sequence against a [B, Tk, Hkv, d] key/value cache whose
+        last row is the token's own: the last row of causal attention over Tk
+        positions.  q1 is [B, Hq, d].  Returns (o1 [B, Hq, d], lse1 [B, Hq])."""
+        q1, k, v = _c(q1), _c(k), _c(v)
+        B, Hq, d = q1.shape
+        Tk, Hkv = k.shape[1], k.shape[2]
+        if k.shape != (B, Tk, Hkv, d) or v.shape != k.shape:
+            raise ValueError("k and v must be [B, Tk, Hkv, d] matching q1")
+        o1 = np.empty_like(q1)
+        lse1 = np.empty((B, Hq), dtype=np.float64)
+        rc = self._lib.ne_oracle_decode(_p(q1), _p(k), _p(v), _p(o1), _p(lse1), B, Tk, Hq, Hkv,
+                                        d, float(theta), int(pos_offset))
+        if rc:
+            raise ValueError(f"ne_oracle_decode failed with code {rc}")
+        return o1, lse1
+
+
 def compile_source(src_path: str, lib_path: str) -> str:
     """Compile one copy of the oracle's C source into a shared library."""
     tmp = lib_path + f".tmp{os.getpid()}"
@@ -161,6 +182,10 @@ def attn_fwd(q, k, v, theta: float, pos_offset: int = 0, threads: int = 0):
 
 def attn_bwd(q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0):
     return default().attn_bwd(q, k, v, do, theta, pos_offset, threads)
+
+
+def attn_decode(q1, k, v, theta: float, pos_offset: int = 0):
+    return default().attn_decode(q1, k, v, theta, pos_offset)
 
 
 def group_slice(x: np.ndarray, b: int, j: int, heads_per_group: int):

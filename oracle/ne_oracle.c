@@ -270,6 +270,69 @@ int ne_oracle_bwd(const double *q, const double *k, const double *v, const doubl
     return err;
 }
 
+/*
+ * Decode against a key/value cache (one new token per sequence).  The new
+ * token is the last of Tk positions: its own key and value are the cache's
+ * last rows, so every cached key is visible to it.  By definition this is the
+ * last row (t = Tk - 1) of the causal attention above over the Tk positions:
+ *   q1 is [B][Hq][d] (pre-RoPE; rotated at position Tk - 1 + pos_offset),
+ *   k, v are [B][Tk][Hkv][d] (pre-RoPE keys, rotated at their positions),
+ *   S[s] = <q1'[b,h], k'[b,s,kv(h)]> / sqrt(d) for s = 0 .. Tk-1,
+ *   P = softmax(S), lse = ln sum_s exp S[s], o1[b,h] = sum_s P[s] v[b,s,kv(h)].
+ * o1 is [B][Hq][d], lse1 is [B][Hq].
+ */
+int ne_oracle_decode(const double *q1, const double *k, const double *v, double *o1,
+                     double *lse1, int B, int Tk, int Hq, int Hkv, int d, double theta,
+                     long pos_offset)
+{
+    if (check_shape(B, Tk, Hq, Hkv, d))
+        return 1;
+    int G = Hq / Hkv;
+    double scale = 1.0 / sqrt((double)d);
+    double *qr = malloc(sizeof(double) * d);
+    double *kr = malloc(sizeof(double) * d);
+    double *S = malloc(sizeof(double) * Tk);
+    if (!qr || !kr || !S) {
+        free(qr);
+        free(kr);
+        free(S);
+        return 2;
+    }
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) {
+            const int kvh = h / G;
+            rope_row(q1 + ((size_t)b * Hq + h) * d, qr, d, theta, (long)(Tk - 1) + pos_offset, 0);
+            double mx = -INFINITY;
+            for (int s = 0; s < Tk; ++s) {
+                rope_row(k + IDX(b, s, kvh, 0, Tk, Hkv, d), kr, d, theta, (long)s + pos_offset, 0);
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c)
+                    acc += qr[c] * kr[c];
+                S[s] = acc * scale;
+                if (S[s] > mx)
+                    mx = S[s];
+            }
+            double sum = 0.0;
+            for (int s = 0; s < Tk; ++s)
+                sum += exp(S[s] - mx);
+            const double lse_bh = mx + log(sum);
+            lse1[(size_t)b * Hq + h] = lse_bh;
+            double *orow = o1 + ((size_t)b * Hq + h) * d;
+            for (int c = 0; c < d; ++c)
+                orow[c] = 0.0;
+            for (int s = 0; s < Tk; ++s) {
+                double pr = exp(S[s] - lse_bh);
+                const double *vrow = v + IDX(b, s, kvh, 0, Tk, Hkv, d);
+                for (int c = 0; c < d; ++c)
+                    orow[c] += pr * vrow[c];
+            }
+        }
+    free(qr);
+    free(kr);
+    free(S);
+    return 0;
+}
+
 int ne_oracle_max_threads(void)
 {
 #ifdef _OPENMP

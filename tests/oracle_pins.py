@@ -282,6 +282,60 @@ def pin_gqa_is_repeated_mha(orc):
     assert _rel(r["dq"], r2["dq"]) < 1e-12
 
 
+# -------------------------------------------------------------- decode ----
+
+def pin_decode_torch_sdpa(orc):
+    """Decode against torch in float64: the query rotated at position Tk - 1 and
+    keys at 0 .. Tk-1 (complex-rotation RoPE), then scaled_dot_product_attention
+    of one query row over all keys (no mask), with GQA; to 1e-10."""
+    for (B, Tk, Hq, Hkv, d, seed) in ((2, 23, 6, 2, 16, 91), (1, 40, 4, 4, 8, 92),
+                                      (3, 1, 2, 1, 8, 93)):
+        q1 = _rand((B, Hq, d), seed)
+        k = _rand((B, Tk, Hkv, d), seed + 1)
+        v = _rand((B, Tk, Hkv, d), seed + 2)
+        qpad = np.zeros((B, Tk, Hq, d))
+        qpad[:, -1] = q1
+        qr = _torch_rope(torch.tensor(qpad), THETA)[:, -1:].transpose(1, 2)   # [B, Hq, 1, d]
+        kr = _torch_rope(torch.tensor(k), THETA).transpose(1, 2)             # [B, Hkv, Tk, d]
+        vv = torch.tensor(v).transpose(1, 2)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qr, kr, vv, scale=1.0 / math.sqrt(d), enable_gqa=True)[:, :, 0]
+        s = qr @ kr.repeat_interleave(Hq // Hkv, dim=1).transpose(-1, -2) / math.sqrt(d)
+        lse = torch.logsumexp(s[:, :, 0], dim=-1)
+        o1, lse1 = orc.attn_decode(q1, k, v, THETA)
+        assert _rel(o1, o.numpy()) < 1e-10, ("o", _rel(o1, o.numpy()))
+        assert np.abs(lse1 - lse.numpy()).max() < 1e-10, "lse"
+
+
+def pin_decode_is_last_causal_row(orc):
+    """Decode equals the last row of the (separately pinned) causal forward over
+    the same Tk positions, whatever the earlier query rows are."""
+    B, Tk, Hq, Hkv, d = 2, 29, 6, 3, 8
+    q = _rand((B, Tk, Hq, d), 95)
+    k = _rand((B, Tk, Hkv, d), 96)
+    v = _rand((B, Tk, Hkv, d), 97)
+    o, lse = orc.attn_fwd(q, k, v, THETA)
+    o1, lse1 = orc.attn_decode(q[:, -1], k, v, THETA)
+    assert _rel(o1, o[:, -1]) < 1e-13 and np.abs(lse1 - lse[:, :, -1]).max() < 1e-12
+
+
+def pin_decode_closed_forms(orc):
+    """q = 0: uniform weights, O = mean of v over the cache, lse = ln Tk.
+    Tk = 1: O = v[0] and lse = <q, k[0]> / sqrt(d) (position 0 rotates nothing)."""
+    B, Tk, Hq, Hkv, d = 1, 17, 4, 2, 8
+    v = _rand((B, Tk, Hkv, d), 98)
+    o1, lse1 = orc.attn_decode(np.zeros((B, Hq, d)), _rand((B, Tk, Hkv, d), 99), v, THETA)
+    mean = np.repeat(v.mean(axis=1), 2, axis=1)
+    assert _rel(o1, mean) < 1e-13 and np.abs(lse1 - math.log(Tk)).max() < 1e-13
+    q1 = _rand((2, 4, d), 100)
+    k = _rand((2, 1, 2, d), 101)
+    v = _rand((2, 1, 2, d), 102)
+    o1, lse1 = orc.attn_decode(q1, k, v, THETA)
+    kk = np.repeat(k[:, 0], 2, axis=1)
+    assert _rel(o1, np.repeat(v[:, 0], 2, axis=1)) < 1e-14
+    assert np.abs(lse1 - (q1 * kk).sum(-1) / math.sqrt(d)).max() < 1e-13
+
+
 ALL_PINS = [
     pin_rope_closed_form,
     pin_rope_identity_and_orthogonal,
@@ -295,4 +349,7 @@ ALL_PINS = [
     pin_finite_differences_tiny_workload,
     pin_torch_sdpa,
     pin_gqa_is_repeated_mha,
+    pin_decode_torch_sdpa,
+    pin_decode_is_last_causal_row,
+    pin_decode_closed_forms,
 ]
