@@ -399,6 +399,80 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def run_decode(args):
+    """Decode against a KV cache: 16 layers (own caches, 537 MB in all, so each
+    layer's cache is cold in L2) x ne_attn_decode of B=64 new tokens over 512
+    cached positions, 12/4 heads, d=64; one CUDA graph per step.  HBM-bound:
+    the metric is the algorithmic bytes (K and V caches, q, o, lse) per second."""
+    import torch
+
+    import causal_gqa_attention_ne_gb300 as ne
+    w = ne_inputs.DECODE_116M
+    ne.load_library()
+    dev = torch.device("cuda", 0)
+    layers = []
+    for layer in range(w.layers):
+        x = ne_inputs.make_inputs(w, layer)
+        q1 = x["q"][:, -1].contiguous().to(dev)
+        k, v = x["k"].to(dev), x["v"].to(dev)
+        o = torch.empty_like(q1)
+        lse = torch.empty(w.B, w.Hq, dtype=torch.float32, device=dev)
+        ws = torch.empty(ne.ne_attn_decode_workspace_size(w.B, w.T, w.Hq, w.Hkv, w.d),
+                         dtype=torch.uint8, device=dev)
+        layers.append((q1, k, v, o, lse, ws))
+
+    def step():
+        for q1, k, v, o, lse, ws in layers:
+            ne.ne_attn_decode(q1, k, v, o, lse, ws, w.theta)
+
+    step()
+    torch.cuda.synchronize()
+    st = ne.ne_attn_get_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)}")
+    cap = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        step()
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    e0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    kv = 2 * w.B * w.T * w.Hkv * w.d * 2
+    small = w.B * w.Hq * w.d * 2 * 2 + w.B * w.Hq * 4
+    nbytes = (kv + small) * w.layers
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    return {
+        "metric": "decode attention against a KV cache: GB/s of algorithmic HBM traffic "
+                  "(K, V caches, q, o, lse) at Tk=512, 12/4 heads, d=64",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16 in, fp32 math", "data": "synthetic (seeded N(0,1), see ne_inputs.py)",
+        "config": {"workload": w.name, "layers": w.layers, "B": w.B, "Tk": w.T, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "d": w.d,
+                   "l2": "16 layers x 33.6 MB of separate caches (537 MB > L2)"},
+        "tokens_per_s": w.B * args.steps / (e0.elapsed_time(e1) * 1e-3),
+        "gpu_launches": 2 * w.layers * args.steps,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"]},
+        "clocks": sampler.summary(),
+    }
+
+
 def run_one_layer_for_profiler():
     """One layer (B64 T512 12/4 d64, 270 MB of buffers), fwd then bwd, twice.
     The first pass warms up; a profiler captures the second (-s 4 -c 4)."""
@@ -489,9 +563,15 @@ def main():
     ap.add_argument("--ncu-layer", action="store_true",
                     help="profiler mode: run one layer of the workload (fwd, then the three "
                          "backward steps) twice, eagerly, and exit; no timing, no JSON")
+    ap.add_argument("--decode", action="store_true",
+                    help="time decode against a KV cache (16 layers of B64, Tk 512) instead "
+                         "of the training step; prints its own JSON line")
     args = ap.parse_args()
     if args.ncu_layer:
         run_one_layer_for_profiler()
+        return
+    if args.decode:
+        print(json.dumps(run_decode(args)), flush=True)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -24,7 +24,7 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn
             "ne_attn_bwd_dq", "ne_attn_bwd_dkdv", "ne_attn_get_error", "ne_attn_status_string",
             "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout", "ne_attn_bwd_noalloc",
             "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save", "ne_attn_bwd_saved",
-            "ne_attn_bwd_preprocess_d")
+            "ne_attn_bwd_preprocess_d", "ne_attn_decode", "ne_attn_decode_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +84,10 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_bwd_noalloc.restype = i
         lib.ne_attn_bwd_noalloc_max_scratch.argtypes = []
         lib.ne_attn_bwd_noalloc_max_scratch.restype = sz
+        lib.ne_attn_decode.argtypes = [vp] * 6 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_decode.restype = i
+        lib.ne_attn_decode_workspace_size.argtypes = [i] * 5
+        lib.ne_attn_decode_workspace_size.restype = sz
         _lib = lib
         return lib
 
@@ -314,6 +318,46 @@ def ne_attn_selftest_timeout(limit_ns: int, stream=None) -> None:
 
 
 # ---- conveniences that allocate outputs with torch (device memory only) ----
+
+def ne_attn_decode_workspace_size(B: int, Tk: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(load_library().ne_attn_decode_workspace_size(B, Tk, Hq, Hkv, d))
+
+
+def ne_attn_decode(q, k_cache, v_cache, o, lse, workspace, rope_theta: float = 10000.0,
+                   stream=None) -> None:
+    """Decode: q [B,Hq,d] (one new token per sequence, at position Tk-1) against
+    k_cache / v_cache [B,Tk,Hkv,d]; writes o [B,Hq,d] bf16 and lse [B,Hq] fp32."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, d] and k_cache [B, Tk, Hkv, d]")
+    B, Hq, d = q.shape
+    Tk, Hkv = k_cache.shape[1], k_cache.shape[2]
+    bf = torch.bfloat16
+    _check(q, "q", (B, Hq, d), bf)
+    _check(k_cache, "k_cache", (B, Tk, Hkv, d), bf)
+    _check(v_cache, "v_cache", (B, Tk, Hkv, d), bf)
+    _check(o, "o", (B, Hq, d), bf)
+    _check(lse, "lse", (B, Hq), torch.float32)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                       o.data_ptr(), lse.data_ptr(), wp, wbytes, B, Tk, Hq, Hkv,
+                                       d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_decode")
+
+
+def attention_decode(q, k_cache, v_cache, rope_theta: float = 10000.0, stream=None,
+                     workspace=None):
+    """Allocate o, lse (and a workspace if none is given) and run ne_attn_decode."""
+    B, Hq, d = q.shape
+    Tk, Hkv = k_cache.shape[1], k_cache.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(ne_attn_decode_workspace_size(B, Tk, Hq, Hkv, d), 16),
+                                dtype=torch.uint8, device=q.device)
+    ne_attn_decode(q, k_cache, v_cache, o, lse, workspace, rope_theta, stream)
+    return o, lse
+
 
 def attention_forward(q, k, v, rope_theta: float = 10000.0, stream=None):
     """Allocate o and lse on q's device and run ne_attn_fwd.  Returns (o, lse)."""

@@ -479,6 +479,62 @@ int ne_attn_bwd_saved(const void *q, const void *k, const void *v, const void *o
     return run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st);
 }
 
+size_t ne_attn_decode_workspace_size(int B, int Tk, int Hq, int Hkv, int d)
+{
+    if (check_shape(B, Tk, Hq, Hkv, d, 1.0f) != NE_OK)
+        return 0;
+    const size_t nchunks = (static_cast<size_t>(Tk) + ne::decode_chunk_keys() - 1) /
+                           ne::decode_chunk_keys();
+    const size_t rows = static_cast<size_t>(B) * Hq * nchunks;
+    const size_t part_o = (rows * d * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    const size_t part_ml = (rows * 2 * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    return part_o + part_ml;
+}
+
+int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                   void *workspace, size_t workspace_bytes, int B, int Tk, int Hq, int Hkv, int d,
+                   float rope_theta, void *stream)
+{
+    if (!q || !k_cache || !v_cache || !o || !lse)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, Tk, Hq, Hkv, d, rope_theta);
+    if (rc != NE_OK)
+        return rc;
+    if (Hq / Hkv > ne::kMaxDecodeGroup)
+        return NE_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < ne_attn_decode_workspace_size(B, Tk, Hq, Hkv, d))
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+        !aligned4(lse) || !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    ne::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = B;
+    p.Tk = Tk;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.nchunks = (Tk + ne::decode_chunk_keys() - 1) / ne::decode_chunk_keys();
+    p.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(d));
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.o = o;
+    p.lse = lse;
+    const size_t rows = static_cast<size_t>(B) * Hq * p.nchunks;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                          ((rows * d * sizeof(float) + 255) &
+                                           ~static_cast<size_t>(255)));
+    fill_rope(p.rope, d, rope_theta);
+    return ne::launch_decode(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? NE_OK
+               : NE_ERR_CUDA;
+}
+
 int ne_attn_get_error(void *stream)
 {
     uint32_t *status = nullptr;

@@ -35,6 +35,23 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,
 int fwd_heads_per_cta(int d, int G);
 int dq_heads_per_cta(int d, int G);
 
+// Decode against a key/value cache: one query row per (b, h) at position
+// Tk - 1 over Tk cached keys.  Split over chunks of decode_chunk_keys() keys;
+// part_o [B][Hq][nchunks][d] and part_ml [B][Hq][nchunks][2] (fp32) hold the
+// chunks' partial results, merged by a second kernel into o and lse.
+constexpr int kMaxDecodeGroup = 16;   // query heads per key/value head
+struct DecodeParams {
+    int B, Tk, Hq, Hkv, G, nchunks;
+    float scale_log2;
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    float *part_o, *part_ml;
+    RopeFreqs rope;
+};
+cudaError_t launch_decode(int d, const DecodeParams &p, cudaStream_t stream);
+int decode_chunk_keys();
+
 // One-block kernel whose wait can never complete (checks the timeout path).
 cudaError_t launch_timeout_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream);
 

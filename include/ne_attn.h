@@ -159,6 +159,32 @@ int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *l
                      float rope_theta, void *stream);
 
 /*
+ * Decode against a key/value cache (the chat loop of the NanoEuler README's
+ * KV-cache inference engine): one new token per sequence.  Its key and value
+ * are the cache's last rows, so it sits at position Tk - 1 and every cached
+ * key is visible to it; the result is, by definition, the last row of the
+ * causal attention ne_attn_fwd computes over those Tk positions.
+ *   q        bf16 [B][Hq][d]      the new tokens' queries, before RoPE
+ *   k_cache  bf16 [B][Tk][Hkv][d] keys before RoPE (rotated at their positions)
+ *   v_cache  bf16 [B][Tk][Hkv][d]
+ *   o        bf16 [B][Hq][d]      written
+ *   lse      fp32 [B][Hq]         written, natural log of the scaled scores
+ *   workspace, workspace_bytes    caller-owned scratch of at least
+ *                                 ne_attn_decode_workspace_size() bytes
+ *                                 (16-byte aligned; no initial contents)
+ * Preconditions as for ne_attn_fwd, and Hq / Hkv <= 16 (else
+ * NE_ERR_UNSUPPORTED).  Asynchronous on `stream`; two kernels (the keys are
+ * split into chunks of 128, each chunk's partial softmax is merged in chunk
+ * order, so the result is deterministic).  Calls that share a workspace must
+ * not overlap on the GPU.  ne_attn_decode_workspace_size returns 0 for an
+ * invalid shape.
+ */
+size_t ne_attn_decode_workspace_size(int B, int Tk, int Hq, int Hkv, int d);
+int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                   void *workspace, size_t workspace_bytes, int B, int Tk, int Hq, int Hkv, int d,
+                   float rope_theta, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side status of
  * the current device: NE_ERR_TIMEOUT or NE_ERR_RANGE if a kernel recorded
  * one since the last call, NE_ERR_CUDA if the stream reports a CUDA error,

@@ -75,6 +75,11 @@ WORKLOADS = {
         # NanoEuler 116M model, the attention of a full step: 16 layers of B=64.
         Workload("gpt116m_step_16x_b64_t512_h12x4_d64", B=64, T=512, Hq=12, Hkv=4, d=64,
                  seed=1004, layers=16),
+        # Decode against a KV cache at the 116M shape: one new token per sequence
+        # (its query is the last row of q), 512 cached positions, 16 layers
+        # with their own caches.
+        Workload("gpt116m_decode_16x_b64_tk512_h12x4_d64", B=64, T=512, Hq=12, Hkv=4, d=64,
+                 seed=1006, layers=16),
         # Long-context stress shape with one 8x row per (tensor, batch, head).
         Workload("stress_b4_t4096_h16x4_d128", B=4, T=4096, Hq=16, Hkv=4, d=128, seed=1005,
                  outlier_rows=True),
@@ -86,6 +91,7 @@ SMALL = WORKLOADS["small_b16_t128_h4x2_d32"]
 LAYER_116M = WORKLOADS["gpt116m_b16_t512_h12x4_d64"]
 STEP_116M = WORKLOADS["gpt116m_step_16x_b64_t512_h12x4_d64"]
 STRESS = WORKLOADS["stress_b4_t4096_h16x4_d128"]
+DECODE_116M = WORKLOADS["gpt116m_decode_16x_b64_tk512_h12x4_d64"]
 
 
 def make_inputs(w: Workload, layer: int = 0) -> dict[str, torch.Tensor]:

@@ -90,3 +90,23 @@ def test_backward_argument_errors(lib):
     # no-allocation variant: shape whose scratch exceeds its fixed buffer
     assert lib.ne_attn_bwd_noalloc(*args, 8, 4096, 8, 8, 128, 10000.0, None) == 10
     assert lib.ne_attn_bwd_noalloc(*args, 1, 8, 3, 2, 64, 10000.0, None) == 2
+
+
+def test_decode_workspace_size_and_argument_errors(lib):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for (B, Tk, Hq, Hkv, d) in ((1, 1, 4, 2, 32), (64, 512, 12, 4, 64), (3, 1000, 16, 4, 128)):
+        rows = B * Hq * ((Tk + 127) // 128)
+        assert ne.ne_attn_decode_workspace_size(B, Tk, Hq, Hkv, d) == r256(rows * d * 4) + \
+            r256(rows * 2 * 4)
+    assert ne.ne_attn_decode_workspace_size(1, 8, 3, 2, 64) == 0      # Hq % Hkv != 0
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    ws = 1 << 15
+    dec = lib.ne_attn_decode
+    assert dec(None, a, a, a, a, a, ws, 1, 8, 2, 2, 64, 10000.0, None) == 1    # NE_ERR_NULL
+    assert dec(a, a, a, a, a, a, ws, 1, 0, 2, 2, 64, 10000.0, None) == 2       # Tk = 0
+    assert dec(a, a, a, a, a, a, ws, 1, 8, 2, 2, 48, 10000.0, None) == 3       # d
+    assert dec(a, a, a, a, a, a, ws, 1, 8, 34, 2, 64, 10000.0, None) == 3      # group of 17
+    assert dec(a, a, a, a, a, a, 0, 1, 8, 2, 2, 64, 10000.0, None) == 5        # workspace
+    assert dec(a + 2, a, a, a, a, a, ws, 1, 8, 2, 2, 64, 10000.0, None) == 4   # alignment
