@@ -8,10 +8,12 @@
 // It reads every cached key and value once and does 4*d flops per key and
 // query head, so it is bound by HBM bandwidth: CUDA cores, no tensor cores.
 // Split over the keys: CTA (b, kv head j, chunk c) takes CH = 128 keys, stages
-// K and V of the chunk in shared memory with coalesced read-only loads,
-// rotates each key at its position (one thread per key), scores it against
-// the G query heads of the group (rotated once per CTA at Tk - 1), and writes
-// one partial (max, sum, O) per head.  A second kernel merges the partials of
+// the chunk's V in shared memory with coalesced read-only loads, and one
+// thread per key reads the key row, rotates it at its position pair by pair
+// straight into its scores against the G query heads of the group (rotated
+// once per CTA at Tk - 1); then one partial (max, sum, O) per head.  Small
+// enough (64 registers, 19 KB at d = 64) for eight CTAs per SM, so a layer's
+// chunks run in one wave.  A second kernel merges the partials of
 // each (b, h) in chunk order: deterministic, no atomics.
 #include <cuda_bf16.h>
 
@@ -25,23 +27,23 @@ constexpr int kDecThreads = 128;
 
 template <int D>
 struct DecCfg {
-    static constexpr int KSTR = D + 8;                                // padded bf16 row of K
-    static constexpr int OFF_K = 0;                                   // bf16 [CH][KSTR]
-    static constexpr int OFF_V = OFF_K + kDecCh * KSTR * 2;           // bf16 [CH][D]
+    static constexpr int OFF_V = 0;                                   // bf16 [CH][D]
     static constexpr int OFF_Q = OFF_V + kDecCh * D * 2;              // float [G][D]
     static __host__ __device__ constexpr int off_p(int G) { return OFF_Q + G * D * 4; }  // float [G][CH]
     static __host__ __device__ constexpr int off_ml(int G) { return off_p(G) + G * kDecCh * 4; }
     static __host__ __device__ constexpr int bytes(int G) { return off_ml(G) + 2 * G * 4; }
 };
 
-template <int D>
-__global__ void __launch_bounds__(kDecThreads)
+// GB = the group size G rounded up to a power of two (the kernel keeps GB
+// score accumulators per thread; heads g >= G are skipped).
+template <int D, int GB>
+__global__ void __launch_bounds__(kDecThreads, 8)
     decode_partial_kernel(const DecodeParams p)
 {
     using C = DecCfg<D>;
     constexpr int CPR = D / 8;     // 16-byte chunks per row
+    constexpr int HC = D / 16;     // chunks in the first half of a row
     extern __shared__ __align__(16) uint8_t smem[];
-    __nv_bfloat16 *ks = reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_K);
     __nv_bfloat16 *vs = reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_V);
     float *qs = reinterpret_cast<float *>(smem + C::OFF_Q);
     float *ps = reinterpret_cast<float *>(smem + C::off_p(p.G));
@@ -55,18 +57,15 @@ __global__ void __launch_bounds__(kDecThreads)
     const int G = p.G;
     griddep_wait();
 
-    // K and V rows s0 .. s0+127 of (b, j): coalesced 16-byte loads, zero past Tk
+    // V rows s0 .. s0+127 of (b, j) into shared memory (coalesced 16-byte
+    // loads, zero past Tk)
     const uint4 *kg = static_cast<const uint4 *>(p.k);
     const uint4 *vg = static_cast<const uint4 *>(p.v);
     for (int idx = t; idx < kDecCh * CPR; idx += kDecThreads) {
         const int r = idx / CPR, cc = idx % CPR, s = s0 + r;
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-        if (s < p.Tk) {
-            const size_t row = (static_cast<size_t>(b) * p.Tk + s) * p.Hkv + j;
-            kv = ld_stream(kg + row * CPR + cc);
-            vv = ld_stream(vg + row * CPR + cc);
-        }
-        *reinterpret_cast<uint4 *>(ks + r * C::KSTR + cc * 8) = kv;
+        uint4 vv = make_uint4(0u, 0u, 0u, 0u);
+        if (s < p.Tk)
+            vv = ld_stream(vg + ((static_cast<size_t>(b) * p.Tk + s) * p.Hkv + j) * CPR + cc);
         *reinterpret_cast<uint4 *>(vs + r * D + cc * 8) = vv;
     }
     // the group's G query rows, rotated at position Tk - 1, in fp32
@@ -83,29 +82,39 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     __syncthreads();
 
-    // one key per thread: rotate it, score it against the G heads (log2 units)
+    // one key per thread, read from global memory in rotate-half chunk pairs
+    // (c, c + D/16) and rotated pair by pair straight into the G scores
     {
         const int s = s0 + t;
-        float kr[D];
-        const __nv_bfloat16 *krow = ks + t * C::KSTR;
+        float acc[GB];
 #pragma unroll
-        for (int i = 0; i < D; ++i)
-            kr[i] = __bfloat162float(krow[i]);
+        for (int g = 0; g < GB; ++g)
+            acc[g] = 0.f;
+        if (s < p.Tk) {
+            const uint4 *krow = kg + ((static_cast<size_t>(b) * p.Tk + s) * p.Hkv + j) * CPR;
 #pragma unroll
-        for (int i = 0; i < D / 2; ++i) {
-            float sn, cs;
-            rope_sincos(static_cast<uint32_t>(s), p.rope.turn[i], sn, cs);
-            const float x = kr[i], y = kr[i + D / 2];
-            kr[i] = x * cs - y * sn;
-            kr[i + D / 2] = y * cs + x * sn;
+            for (int cc = 0; cc < HC; ++cc) {
+                const uint4 a4 = krow[cc], b4 = krow[cc + HC];
+                const uint32_t av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * cc + e;
+                    float sn, cs;
+                    rope_sincos(static_cast<uint32_t>(s), p.rope.turn[i], sn, cs);
+                    const float x = (e & 1) ? bf16_hi(av[e >> 1]) : bf16_lo(av[e >> 1]);
+                    const float y = (e & 1) ? bf16_hi(bv[e >> 1]) : bf16_lo(bv[e >> 1]);
+                    const float xr = x * cs - y * sn, yr = y * cs + x * sn;
+#pragma unroll
+                    for (int g = 0; g < GB; ++g)
+                        if (g < G)
+                            acc[g] = fmaf(qs[g * D + i + D / 2], yr, fmaf(qs[g * D + i], xr, acc[g]));
+                }
+            }
         }
-        for (int g = 0; g < G; ++g) {
-            float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < D; ++i)
-                acc = fmaf(qs[g * D + i], kr[i], acc);
-            ps[g * kDecCh + t] = s < p.Tk ? acc * p.scale_log2 : -INFINITY;
-        }
+        for (int g = 0; g < GB; ++g)
+            if (g < G)
+                ps[g * kDecCh + t] = s < p.Tk ? acc[g] * p.scale_log2 : -INFINITY;
     }
     __syncthreads();
 
@@ -135,16 +144,22 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     __syncthreads();
 
-    // O_g[e] = sum_r P_g[r] v[r][e]; partials to the workspace
+    // O_g[e..e+1] = sum_r P_g[r] v[r][e..e+1] (column pairs); partials to the
+    // workspace
     const size_t part0 = (static_cast<size_t>(b) * p.Hq + j * G) * p.nchunks + c;
-    for (int o = t; o < G * D; o += kDecThreads) {
-        const int g = o / D, e = o % D;
+    for (int o = t; o < G * (D / 2); o += kDecThreads) {
+        const int g = o / (D / 2), e = 2 * (o % (D / 2));
         const float *prow = ps + g * kDecCh;
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll 8
-        for (int r = 0; r < kDecCh; ++r)
-            acc = fmaf(prow[r], __bfloat162float(vs[r * D + e]), acc);
-        p.part_o[(part0 + static_cast<size_t>(g) * p.nchunks) * D + e] = acc;
+        for (int r = 0; r < kDecCh; ++r) {
+            const uint32_t v2 = *reinterpret_cast<const uint32_t *>(vs + r * D + e);
+            const float pr = prow[r];
+            a0 = fmaf(pr, bf16_lo(v2), a0);
+            a1 = fmaf(pr, bf16_hi(v2), a1);
+        }
+        float *dst = p.part_o + (part0 + static_cast<size_t>(g) * p.nchunks) * D + e;
+        *reinterpret_cast<float2 *>(dst) = make_float2(a0, a1);
     }
     if (t < G) {
         const size_t pi = part0 + static_cast<size_t>(t) * p.nchunks;
@@ -181,11 +196,11 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 
 int decode_chunk_keys() { return kDecCh; }
 
-template <int D>
+template <int D, int GB>
 static cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
 {
     const int smem = DecCfg<D>::bytes(p.G);
-    auto kern = decode_partial_kernel<D>;
+    auto kern = decode_partial_kernel<D, GB>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, DecCfg<D>::bytes(kMaxDecodeGroup), attr_done);
     if (e != cudaSuccess)
@@ -197,12 +212,26 @@ static cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
                       p);
 }
 
+template <int D>
+static cudaError_t launch_decode_d(const DecodeParams &p, cudaStream_t stream)
+{
+    if (p.G <= 1)
+        return launch_decode_t<D, 1>(p, stream);
+    if (p.G <= 2)
+        return launch_decode_t<D, 2>(p, stream);
+    if (p.G <= 4)
+        return launch_decode_t<D, 4>(p, stream);
+    if (p.G <= 8)
+        return launch_decode_t<D, 8>(p, stream);
+    return launch_decode_t<D, 16>(p, stream);
+}
+
 cudaError_t launch_decode(int d, const DecodeParams &p, cudaStream_t stream)
 {
     switch (d) {
-    case 32: return launch_decode_t<32>(p, stream);
-    case 64: return launch_decode_t<64>(p, stream);
-    case 128: return launch_decode_t<128>(p, stream);
+    case 32: return launch_decode_d<32>(p, stream);
+    case 64: return launch_decode_d<64>(p, stream);
+    case 128: return launch_decode_d<128>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
