@@ -53,10 +53,10 @@ def _bind(path: str):
         ctypes.c_double, ctypes.c_long, ctypes.c_int]
     lib.ne_oracle_fwd.restype = ctypes.c_int
     lib.ne_oracle_fwd.argtypes = [_DP] * 5 + [ctypes.c_int] * 5 + [
-        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+        ctypes.c_double, ctypes.c_long, ctypes.c_int, ctypes.c_int]
     lib.ne_oracle_bwd.restype = ctypes.c_int
     lib.ne_oracle_bwd.argtypes = [_DP] * 10 + [ctypes.c_int] * 5 + [
-        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+        ctypes.c_double, ctypes.c_long, ctypes.c_int, ctypes.c_int]
     lib.ne_oracle_decode.restype = ctypes.c_int
     lib.ne_oracle_decode.argtypes = [_DP] * 5 + [ctypes.c_int] * 5 + [
         ctypes.c_double, ctypes.c_long]
@@ -92,8 +92,10 @@ class Oracle:
             raise ValueError(f"ne_oracle_rope rejected shape {x.shape}")
         return y
 
-    def attn_fwd(self, q, k, v, theta: float, pos_offset: int = 0, threads: int = 0):
-        """Causal GQA attention with RoPE.  Returns (o [B,T,Hq,d], lse [B,Hq,T])."""
+    def attn_fwd(self, q, k, v, theta: float, pos_offset: int = 0, threads: int = 0,
+                 window: int = 0):
+        """Causal GQA attention with RoPE (window W > 0: query t sees keys t-W+1 .. t).
+        Returns (o [B,T,Hq,d], lse [B,Hq,T])."""
         q, k, v = _c(q), _c(k), _c(v)
         B, T, Hq, d = q.shape
         Hkv = k.shape[2]
@@ -102,12 +104,13 @@ class Oracle:
         o = np.empty_like(q)
         lse = np.empty((B, Hq, T), dtype=np.float64)
         rc = self._lib.ne_oracle_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, T, Hq, Hkv, d,
-                                     float(theta), int(pos_offset), int(threads))
+                                     float(theta), int(pos_offset), int(threads), int(window))
         if rc:
             raise ValueError(f"ne_oracle_fwd failed with code {rc}")
         return o, lse
 
-    def attn_bwd(self, q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0):
+    def attn_bwd(self, q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0,
+                 window: int = 0):
         """Gradients of sum(O * dO): dict with dq, dk, dv and the oracle's o, lse, D."""
         q, k, v, do = _c(q), _c(k), _c(v), _c(do)
         B, T, Hq, d = q.shape
@@ -122,7 +125,7 @@ class Oracle:
         D = np.empty((B, Hq, T), dtype=np.float64)
         rc = self._lib.ne_oracle_bwd(_p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv),
                                      _p(o), _p(lse), _p(D), B, T, Hq, Hkv, d, float(theta),
-                                     int(pos_offset), int(threads))
+                                     int(pos_offset), int(threads), int(window))
         if rc:
             raise ValueError(f"ne_oracle_bwd failed with code {rc}")
         return {"dq": dq, "dk": dk, "dv": dv, "o": o, "lse": lse, "D": D}
@@ -176,12 +179,13 @@ def rope(x, theta: float, pos_offset: int = 0, inverse: bool = False):
     return default().rope(x, theta, pos_offset, inverse)
 
 
-def attn_fwd(q, k, v, theta: float, pos_offset: int = 0, threads: int = 0):
-    return default().attn_fwd(q, k, v, theta, pos_offset, threads)
+def attn_fwd(q, k, v, theta: float, pos_offset: int = 0, threads: int = 0, window: int = 0):
+    return default().attn_fwd(q, k, v, theta, pos_offset, threads, window)
 
 
-def attn_bwd(q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0):
-    return default().attn_bwd(q, k, v, do, theta, pos_offset, threads)
+def attn_bwd(q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0,
+             window: int = 0):
+    return default().attn_bwd(q, k, v, do, theta, pos_offset, threads, window)
 
 
 def attn_decode(q1, k, v, theta: float, pos_offset: int = 0):

@@ -23,6 +23,9 @@
  *     x'_{i+d/2} = x_{i+d/2} cos a + x_i sin a
  *   GQA head map: query head h reads key/value head h / (Hq/Hkv).
  *   S[t,s] = <q'[t,h], k'[s,kv(h)]> / sqrt(d) for s <= t, -inf otherwise.
+ *   Sliding window (window = W > 0): also -inf for s <= t - W, so query t
+ *   sees the W keys t-W+1 .. t (the nanochat guide's per-layer window
+ *   pattern); window = 0 is the plain causal mask.
  *   P = row softmax of S;  lse[t] = ln sum_s exp S[t,s];  O[t] = sum_s P v[s].
  *
  *   Backward for the loss L = sum(O * dO):
@@ -37,6 +40,7 @@
  *
  * Layout: q, o, dO, dq are [B][T][Hq][d]; k, v, dk, dv are [B][T][Hkv][d];
  * lse and D are [B][Hq][T].  All arrays are contiguous float64.
+ * window: 0 for the causal mask alone, W > 0 for a sliding window of W keys.
  * pos_offset shifts every position by a constant (a test hook for the
  * relative-position property of RoPE); the library itself always uses 0.
  */
@@ -90,13 +94,18 @@ static int check_shape(int B, int T, int Hq, int Hkv, int d)
  * diagonal.  qr and kr are the rotated query / key rows of this head (T x d).
  * Writes lse[t] (natural log) as well.
  */
-static void probs(const double *qr, const double *kr, int T, int d, double *P, double *lse)
+static void probs(const double *qr, const double *kr, int T, int d, int window, double *P,
+                  double *lse)
 {
     double scale = 1.0 / sqrt((double)d);
     for (int t = 0; t < T; ++t) {
         double *S = P + (size_t)t * T;
         for (int s = 0; s < T; ++s) {
             if (s > t) {
+                S[s] = -INFINITY;
+                continue;
+            }
+            if (window > 0 && t - s >= window) {   /* outside the sliding window */
                 S[s] = -INFINITY;
                 continue;
             }
@@ -129,7 +138,7 @@ static void gather_rotated(const double *x, double *xr, int b, int h, int T, int
 
 int ne_oracle_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
                   int B, int T, int Hq, int Hkv, int d, double theta, long pos_offset,
-                  int nthreads)
+                  int nthreads, int window)
 {
     if (check_shape(B, T, Hq, Hkv, d))
         return 1;
@@ -151,7 +160,7 @@ int ne_oracle_fwd(const double *q, const double *k, const double *v, double *o, 
         } else {
             gather_rotated(q, qr, b, h, T, Hq, d, theta, pos_offset);
             gather_rotated(k, kr, b, j, T, Hkv, d, theta, pos_offset);
-            probs(qr, kr, T, d, P, lse + ((size_t)b * Hq + h) * T);
+            probs(qr, kr, T, d, window, P, lse + ((size_t)b * Hq + h) * T);
             for (int t = 0; t < T; ++t) {
                 double *orow = o + IDX(b, t, h, 0, T, Hq, d);
                 for (int c = 0; c < d; ++c)
@@ -179,7 +188,7 @@ int ne_oracle_fwd(const double *q, const double *k, const double *v, double *o, 
 int ne_oracle_bwd(const double *q, const double *k, const double *v, const double *dO,
                   double *dq, double *dk, double *dv, double *o_out, double *lse_out,
                   double *D_out, int B, int T, int Hq, int Hkv, int d, double theta,
-                  long pos_offset, int nthreads)
+                  long pos_offset, int nthreads, int window)
 {
     if (check_shape(B, T, Hq, Hkv, d))
         return 1;
@@ -212,7 +221,7 @@ int ne_oracle_bwd(const double *q, const double *k, const double *v, const doubl
             memset(dv + IDX(b, s, j, 0, T, Hkv, d), 0, sizeof(double) * d);
         for (int h = j * G; h < (j + 1) * G; ++h) {
             gather_rotated(q, qr, b, h, T, Hq, d, theta, pos_offset);
-            probs(qr, kr, T, d, P, lse);
+            probs(qr, kr, T, d, window, P, lse);
             memset(dqr, 0, sizeof(double) * Td);
             for (int t = 0; t < T; ++t) {
                 const double *dorow = dO + IDX(b, t, h, 0, T, Hq, d);

@@ -282,6 +282,56 @@ def pin_gqa_is_repeated_mha(orc):
     assert _rel(r["dq"], r2["dq"]) < 1e-12
 
 
+# ------------------------------------------------------- sliding window ----
+
+def pin_window_torch_band_mask(orc):
+    """Sliding window W against torch in float64: complex-rotation RoPE, then
+    scaled_dot_product_attention with the band mask t - W < s <= t and
+    autograd for the gradients of sum(O * dO); to 1e-10."""
+    for (B, T, Hq, Hkv, d, W, seed) in ((1, 37, 6, 2, 16, 5, 111), (2, 30, 4, 4, 8, 1, 112),
+                                        (1, 50, 4, 1, 8, 17, 113)):
+        x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=seed)
+        q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
+        tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+        t = torch.arange(T)
+        allowed = (t[None, :] <= t[:, None]) & (t[:, None] - t[None, :] < W)
+        qr = _torch_rope(tq, THETA).transpose(1, 2)
+        kr = _torch_rope(tk, THETA).transpose(1, 2)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qr, kr, tv.transpose(1, 2), attn_mask=allowed, scale=1.0 / math.sqrt(d),
+            enable_gqa=True)
+        (o * torch.tensor(do).transpose(1, 2)).sum().backward()
+        with torch.no_grad():
+            s = qr @ kr.repeat_interleave(Hq // Hkv, dim=1).transpose(-1, -2) / math.sqrt(d)
+            lse = torch.logsumexp(s.masked_fill(~allowed, float("-inf")), dim=-1)
+        o1, lse1 = orc.attn_fwd(q, k, v, THETA, window=W)
+        r = orc.attn_bwd(q, k, v, do, THETA, window=W)
+        assert _rel(o1, o.detach().transpose(1, 2).numpy()) < 1e-10, "o"
+        assert np.abs(lse1 - lse.numpy()).max() < 1e-10, "lse"
+        for n, g in (("dq", tq.grad), ("dk", tk.grad), ("dv", tv.grad)):
+            assert _rel(r[n], g.numpy()) < 1e-10, (n, _rel(r[n], g.numpy()))
+
+
+def pin_window_limits(orc):
+    """W >= T is the causal mask (bitwise); W = 1 lets query t see key t only:
+    O[t] = v[t], lse[t] = <q'_t, k'_t> / sqrt(d) (position t rotates both by
+    the same angle, which leaves their dot product unchanged)."""
+    x = ne_inputs.make_custom(B=2, T=23, Hq=4, Hkv=2, d=8, seed=115)
+    q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
+    o0, l0 = orc.attn_fwd(q, k, v, THETA)
+    o1, l1 = orc.attn_fwd(q, k, v, THETA, window=23)
+    assert (o0 == o1).all() and (l0 == l1).all()
+    r0 = orc.attn_bwd(q, k, v, do, THETA)
+    r1 = orc.attn_bwd(q, k, v, do, THETA, window=40)
+    for n in ("dq", "dk", "dv"):
+        assert (r0[n] == r1[n]).all()
+    o, lse = orc.attn_fwd(q, k, v, THETA, window=1)
+    kk = np.repeat(k, 2, axis=2)
+    assert _rel(o, np.repeat(v, 2, axis=2)) < 1e-13
+    want = (q * kk).sum(-1).transpose(0, 2, 1) / math.sqrt(8)
+    assert np.abs(lse - want).max() < 1e-12
+
+
 # -------------------------------------------------------------- decode ----
 
 def pin_decode_torch_sdpa(orc):
@@ -349,6 +399,8 @@ ALL_PINS = [
     pin_finite_differences_tiny_workload,
     pin_torch_sdpa,
     pin_gqa_is_repeated_mha,
+    pin_window_torch_band_mask,
+    pin_window_limits,
     pin_decode_torch_sdpa,
     pin_decode_is_last_causal_row,
     pin_decode_closed_forms,

@@ -38,6 +38,8 @@ MUTATIONS = [
     ("dq_forward_rotation", "rope_row(dqr + (size_t)t * d, dq + IDX(b, t, h, 0, T, Hq, d), d, theta,\n                         (long)t + pos_offset, 1);",
      "rope_row(dqr + (size_t)t * d, dq + IDX(b, t, h, 0, T, Hq, d), d, theta,\n                         (long)t + pos_offset, 0);"),
     ("dk_skips_inverse_rotation", "(long)s + pos_offset, 1);", "(long)s + pos_offset + 3, 1);"),
+    ("window_off_by_one", "if (window > 0 && t - s >= window) {",
+     "if (window > 0 && t - s > window) {"),
     ("decode_query_position", "(long)(Tk - 1) + pos_offset, 0);", "(long)Tk + pos_offset, 0);"),
     ("decode_kv_head_interleaved", "const int kvh = h / G;", "const int kvh = h % Hkv;"),
     ("decode_drops_normaliser", "double pr = exp(S[s] - lse_bh);", "double pr = exp(S[s] - mx);"),
