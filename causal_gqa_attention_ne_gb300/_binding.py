@@ -24,7 +24,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn
             "ne_attn_bwd_dq", "ne_attn_bwd_dkdv", "ne_attn_get_error", "ne_attn_status_string",
             "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout", "ne_attn_bwd_noalloc",
             "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save", "ne_attn_bwd_saved",
-            "ne_attn_bwd_preprocess_d", "ne_attn_decode", "ne_attn_decode_workspace_size")
+            "ne_attn_bwd_preprocess_d", "ne_attn_decode", "ne_attn_decode_workspace_size",
+            "ne_attn_fwd_window", "ne_attn_bwd_window")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +85,10 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_bwd_noalloc.restype = i
         lib.ne_attn_bwd_noalloc_max_scratch.argtypes = []
         lib.ne_attn_bwd_noalloc_max_scratch.restype = sz
+        lib.ne_attn_fwd_window.argtypes = [vp] * 5 + [i] * 5 + [f, i, vp]
+        lib.ne_attn_fwd_window.restype = i
+        lib.ne_attn_bwd_window.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, i, vp]
+        lib.ne_attn_bwd_window.restype = i
         lib.ne_attn_decode.argtypes = [vp] * 6 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_decode.restype = i
         lib.ne_attn_decode_workspace_size.argtypes = [i] * 5
@@ -318,6 +323,42 @@ def ne_attn_selftest_timeout(limit_ns: int, stream=None) -> None:
 
 
 # ---- conveniences that allocate outputs with torch (device memory only) ----
+
+def ne_attn_fwd_window(q, k, v, o, lse, window: int, rope_theta: float = 10000.0,
+                       stream=None) -> None:
+    """ne_attn_fwd with a sliding window: query t sees keys t-window+1 .. t (0: causal)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (B, T, Hq, d), bf)
+    _check(k, "k", (B, T, Hkv, d), bf)
+    _check(v, "v", (B, T, Hkv, d), bf)
+    _check(o, "o", (B, T, Hq, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    rc = load_library().ne_attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           lse.data_ptr(), B, T, Hq, Hkv, d, float(rope_theta),
+                                           int(window), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd_window")
+
+
+def ne_attn_bwd_window(q, k, v, o, lse, do, dq, dk, dv, workspace, window: int,
+                       rope_theta: float = 10000.0, stream=None) -> None:
+    """ne_attn_bwd with a sliding window (the forward's `window`)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                           o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), wp, wbytes,
+                                           B, T, Hq, Hkv, d, float(rope_theta), int(window),
+                                           _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_window")
+
 
 def ne_attn_decode_workspace_size(B: int, Tk: int, Hq: int, Hkv: int, d: int) -> int:
     return int(load_library().ne_attn_decode_workspace_size(B, Tk, Hq, Hkv, d))

@@ -214,13 +214,15 @@ namespace {
 // into the workspace's Q' and K' regions for ne_attn_bwd_saved.
 int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace,
              size_t workspace_bytes, bool save, int B, int T, int Hq, int Hkv, int d,
-             float rope_theta, void *stream)
+             float rope_theta, void *stream, int window = 0)
 {
     if (!q || !k || !v || !o || !lse || (save && !workspace))
         return NE_ERR_NULL;
     int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
+    if (window < 0)
+        return NE_ERR_ARG;
     if (save && workspace_bytes < ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d))
         return NE_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
@@ -235,6 +237,7 @@ int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, v
     p.out0 = o;
     p.lse = lse;
     p.save_rot = save ? 1 : 0;
+    p.window = window;
     CUtensorMap mq, mk, mv, mo, mqs, mks;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
         make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
@@ -276,6 +279,13 @@ size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
     if (check_shape(B, T, Hq, Hkv, d, 1.0f) != NE_OK)
         return 0;
     return ws_d_bytes(B, T, Hq) + ws_q_bytes(B, T, Hq, d) + ws_q_bytes(B, T, Hkv, d);
+}
+
+int ne_attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, int window, void *stream)
+{
+    return fwd_impl(q, k, v, o, lse, nullptr, 0, false, B, T, Hq, Hkv, d, rope_theta, stream,
+                    window);
 }
 
 } // extern "C"
@@ -428,11 +438,27 @@ int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *l
     return run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, static_cast<cudaStream_t>(stream));
 }
 
+int ne_attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                       int d, float rope_theta, int window, void *stream);
+
 int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                 const void *dO, void *dq, void *dk, void *dv, void *workspace,
                 size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, float rope_theta,
                 void *stream)
 {
+    return ne_attn_bwd_window(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, T,
+                              Hq, Hkv, d, rope_theta, 0, stream);
+}
+
+int ne_attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                       int d, float rope_theta, int window, void *stream)
+{
+    if (window < 0)
+        return NE_ERR_ARG;
     if (!o || !dq || !dk || !dv)
         return NE_ERR_NULL;
     if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -443,6 +469,7 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
                        rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
     if (rc != NE_OK)
         return rc;
+    p.window = window;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.o_in = o;
     void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);

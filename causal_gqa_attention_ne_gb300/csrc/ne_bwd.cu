@@ -298,7 +298,7 @@ struct DqCfg {
 };
 
 struct DqUnit {
-    int m, b, j, h0;
+    int m, b, j, h0, lo;   // lo: first key tile (sliding window; 0 otherwise)
 };
 
 __device__ __forceinline__ DqUnit dq_unit(int u, int GC, const AttnParams &p)
@@ -312,10 +312,12 @@ __device__ __forceinline__ DqUnit dq_unit(int u, int GC, const AttnParams &p)
     w.j = rem % p.Hkv;
     w.b = rem / p.Hkv;
     w.h0 = w.j * p.G + chunk * GC;
+    w.lo = key_tile_lo(w.m, p.window);
     return w;
 }
 
-template <int D, int GC, int ST>
+// WIN: a sliding window may mask keys off the diagonal tile.
+template <int D, int GC, int ST, bool WIN>
 __global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(384, 1)
                                     &tmDO, qb, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
                     }
                 }
-                for (int jk = 0; jk <= w.m && ok; ++jk, ++kt) {
+                for (int jk = w.lo; jk <= w.m && ok; ++jk, ++kt) {
                     const int st = kt % ST, u2 = kt / ST;
                     if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc)) {
                         ok = false;
@@ -451,12 +453,12 @@ __global__ void __launch_bounds__(384, 1)
                     if (u >= p.num_units)
                         break;
                     const DqUnit w = dq_unit(u, GC, p);
-                    const int nitems = (w.m + 1) * GC;
+                    const int nitems = (w.m - w.lo + 1) * GC;
                     for (int it = 0; it < nitems; ++it, ++gi) {
-                        const int jk = it / GC, g = it % GC;
+                        const int jk = w.lo + it / GC, g = it % GC;
                         const int st = kt % ST;
                         if ((g == 0 && !mbar_wait_warp(smem_u32(&bar_kv_full[st]), (kt / ST) & 1, wc)) ||
-                            (jk == 0 && !mbar_wait_warp(smem_u32(&bar_q_full[g]), k & 1, wc)) ||
+                            (jk == w.lo && !mbar_wait_warp(smem_u32(&bar_q_full[g]), k & 1, wc)) ||
                             (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_s_empty), (gi - 1) & 1, wc))) {
                             ok = false;
                             break;
@@ -489,9 +491,9 @@ __global__ void __launch_bounds__(384, 1)
                     if (u >= p.num_units)
                         break;
                     const DqUnit w = dq_unit(u, GC, p);
-                    const int nitems = (w.m + 1) * GC;
+                    const int nitems = (w.m - w.lo + 1) * GC;
                     for (int it = 0; it < nitems; ++it, ++gi) {
-                        const int jk = it / GC, g = it % GC;
+                        const int jk = w.lo + it / GC, g = it % GC;
                         const int st = kt % ST;
                         if (!mbar_wait_warp(smem_u32(&bar_ds_full), gi & 1, wc) ||
                             (it == 0 && k >= 1 &&
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         tc_fence_after();
                         const uint64_t km = dKm0 + st * TSTEP;
-                        const uint32_t first = (jk > 0) ? 1u : 0u;
+                        const uint32_t first = (jk > w.lo) ? 1u : 0u;
                         if (elect_one()) {
 #pragma unroll
                             for (int nc = 0; nc < D / TL::NPV; ++nc)
@@ -600,9 +602,9 @@ __global__ void __launch_bounds__(384, 1)
             dd[g] = nD[g];
         }
         fetch(k + 1, nl2, nD);              // next unit's row scalars, in flight meanwhile
-        const int nitems = (un.m + 1) * GC;
+        const int nitems = (un.m - un.lo + 1) * GC;
         for (int it = 0; it < nitems; ++it, ++gi) {
-            const int jk = it / GC, g = it % GC;
+            const int jk = un.lo + it / GC, g = it % GC;
             if (!mbar_wait_warp(smem_u32(&bar_s_full), gi & 1, wc)) {
                 ok = false;
                 break;
@@ -633,7 +635,11 @@ __global__ void __launch_bounds__(384, 1)
                 }
             const float sl2 = p.scale_log2;
             uint32_t dk[32];
-            if (jk != un.m) {
+            // sliding window: key columns c <= wlim (key <= row - W) are masked
+            int wlim = -1;
+            if constexpr (WIN)
+                wlim = un.m * kRows + r - p.window - jk * kRows;
+            if (jk != un.m && !(WIN && __any_sync(0xffffffffu, wlim >= 0))) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -646,7 +652,9 @@ __global__ void __launch_bounds__(384, 1)
                         dk[16 * h + e / 2] = pack_f16x2(d0, d1);
                     }
             } else {
-                // diagonal tile: key column c > query row r is masked
+                // diagonal tile: key column c > query row r is masked; window:
+                // columns c <= wlim
+                const int clim = (!WIN || jk == un.m) ? r : 1 << 30;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -654,8 +662,8 @@ __global__ void __launch_bounds__(384, 1)
                         const int c = 64 * w + 32 * h + e;
                         float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -lg));
                         float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -lg));
-                        p0 = (c > r) ? 0.f : p0;
-                        p1 = (c + 1 > r) ? 0.f : p1;
+                        p0 = (c > clim || (WIN && c <= wlim)) ? 0.f : p0;
+                        p1 = (c + 1 > clim || (WIN && c + 1 <= wlim)) ? 0.f : p1;
                         const float d0 = p0 * (__uint_as_float(pv[h][e]) - dg);
                         const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - dg);
                         maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
@@ -750,11 +758,12 @@ __device__ __forceinline__ DkvUnit dkv_unit(int u, const AttnParams &p)
     const int rem = u % per_n;
     w.j = rem % p.Hkv;
     w.b = rem / p.Hkv;
-    w.nitems = (p.M - w.n) * p.G;
+    w.nitems = (query_tile_hi(w.n, p.window, p.M) - w.n + 1) * p.G;
     return w;
 }
 
-template <int D, int ST>
+// WIN: a sliding window may mask queries off the diagonal tile.
+template <int D, int ST, bool WIN>
 __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -1145,7 +1154,12 @@ __global__ void __launch_bounds__(512, 1)
                 const float4 *ld4 = reinterpret_cast<const float4 *>(lsed + st * kRows + 64 * w);
                 uint32_t pp[32], dk[32];
                 const float sl2 = p.scale_log2;
-                if (mt != un.n) {
+                // sliding window: query columns c >= wmin (query >= key + W)
+                // are masked
+                int wmin = 1 << 30;
+                if constexpr (WIN)
+                    wmin = un.n * kRows + r + p.window - mt * kRows;
+                if (mt != un.n && !(WIN && __any_sync(0xffffffffu, wmin < kRows))) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -1161,7 +1175,9 @@ __global__ void __launch_bounds__(512, 1)
                             dk[16 * h + e / 2] = pack_f16x2(d0, d1);
                         }
                 } else {
-                    // diagonal tile: query column c < key row r is masked
+                    // diagonal tile: query column c < key row r is masked;
+                    // window: columns c >= wmin
+                    const int clo = (!WIN || mt == un.n) ? r : -1;
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -1170,8 +1186,8 @@ __global__ void __launch_bounds__(512, 1)
                             const float4 a = ld4[(32 * h + e) >> 1];
                             float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -a.x));
                             float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -a.z));
-                            p0 = (c < r) ? 0.f : p0;
-                            p1 = (c + 1 < r) ? 0.f : p1;
+                            p0 = (c < clo || (WIN && c >= wmin)) ? 0.f : p0;
+                            p1 = (c + 1 < clo || (WIN && c + 1 >= wmin)) ? 0.f : p1;
                             const float d0 = p0 * (__uint_as_float(pv[h][e]) - a.y);
                             const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - a.w);
                             maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
@@ -1211,12 +1227,12 @@ __global__ void __launch_bounds__(512, 1)
 
 // ------------------------------------------------------------- launch ---
 
-template <int D, int GC, int ST>
-static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+template <int D, int GC, int ST, bool WIN>
+static cudaError_t launch_dq_w(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                const CUtensorMap &dO, const AttnParams &p0, cudaStream_t stream)
 {
     using C = DqCfg<D, GC, ST>;
-    auto kern = dq_kernel<D, GC, ST>;
+    auto kern = dq_kernel<D, GC, ST, WIN>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
@@ -1229,6 +1245,15 @@ static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const
     p.num_units = p.M * p.B * p.Hkv * p.nchunks;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
     return launch_pdl(kern, grid, 384, C::SMEM_BYTES, stream, q, k, v, dO, p);
+}
+
+template <int D, int GC, int ST>
+static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
+{
+    if (p.window > 0)
+        return launch_dq_w<D, GC, ST, true>(q, k, v, dO, p, stream);
+    return launch_dq_w<D, GC, ST, false>(q, k, v, dO, p, stream);
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
@@ -1261,12 +1286,12 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, con
     return cudaErrorInvalidValue;
 }
 
-template <int D, int ST>
-static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+template <int D, int ST, bool WIN>
+static cudaError_t launch_dkdv_w(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                  const CUtensorMap &dO, const AttnParams &p0, cudaStream_t stream)
 {
     using C = DkvCfg<D, ST>;
-    auto kern = dkdv_kernel<D, ST>;
+    auto kern = dkdv_kernel<D, ST, WIN>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
@@ -1279,6 +1304,15 @@ static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, con
     p.num_units = p.M * p.B * p.Hkv;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
     return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, dO, p);
+}
+
+template <int D, int ST>
+static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                 const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
+{
+    if (p.window > 0)
+        return launch_dkdv_w<D, ST, true>(q, k, v, dO, p, stream);
+    return launch_dkdv_w<D, ST, false>(q, k, v, dO, p, stream);
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,

@@ -377,7 +377,26 @@ struct AttnParams {
     int num_units;               // persistent kernels: work units in the launch
     uint64_t wait_limit_ns;
     int save_rot;                // forward: also store Q' and K' (fp16) for the backward
+    int window;                  // 0: causal; W > 0: query t sees keys t-W+1 .. t
     RopeFreqs rope;
 };
+
+// Sliding window: the first key tile any row of query tile m sees (0 without
+// a window: its first row t = 128 m sees keys >= t - W + 1), and the last
+// query tile any key of key tile n is visible to (t <= 128 n + 127 + W - 1).
+__host__ __device__ inline int key_tile_lo(int m, int window)
+{
+    if (window <= 0)
+        return 0;
+    const int lo_key = m * kRows - window + 1;
+    return lo_key <= 0 ? 0 : lo_key / kRows;
+}
+__host__ __device__ inline int query_tile_hi(int n, int window, int M)
+{
+    if (window <= 0)
+        return M - 1;
+    const int hi = (n * kRows + kRows - 2 + window) / kRows;
+    return hi < M - 1 ? hi : M - 1;
+}
 
 } // namespace ne

@@ -91,7 +91,7 @@ struct FwdCfg {
 };
 
 struct FwdUnit {
-    int m, b, j, h0;
+    int m, b, j, h0, lo;   // lo: first key tile (sliding window; 0 otherwise)
 };
 
 __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
@@ -105,10 +105,13 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
     w.j = rem % p.Hkv;
     w.b = rem / p.Hkv;
     w.h0 = w.j * p.G + chunk * GC;
+    w.lo = key_tile_lo(w.m, p.window);
     return w;
 }
 
-template <int D, int GC, int ST>
+// WIN: a sliding window may mask keys off the diagonal tile (compiled out of
+// the causal instantiations).
+template <int D, int GC, int ST, bool WIN>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -275,14 +278,14 @@ __global__ void __launch_bounds__(512, 1)
                 if (u >= p.num_units)
                     break;
                 const FwdUnit w = fwd_unit(u, GC, p);
-                // order: [Q of this unit if not prefetched], K/V 0, [Q of the
-                // next unit], K/V 1..m
+                // order: [Q of this unit if not prefetched], K/V lo, [Q of the
+                // next unit], K/V lo+1..m
                 if (QB == 1 || k == 0)
                     ok = load_q(k);
-                ok = ok && load_kv(w, 0);
+                ok = ok && load_kv(w, w.lo);
                 if (QB == 2 && ok && snake_unit(k + 1, cta, P) < p.num_units)
                     ok = load_q(k + 1);
-                for (int jk = 1; jk <= w.m && ok; ++jk)
+                for (int jk = w.lo + 1; jk <= w.m && ok; ++jk)
                     ok = load_kv(w, jk);
             }
             if (*wc.abort && lane == 0) {
@@ -317,11 +320,11 @@ __global__ void __launch_bounds__(512, 1)
                 const int nq0 = (QB == 1 || k == 0) ? GC : 0;
                 const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
                 const int nq1 = has_next ? GC : 0;
-                for (int t = 0; t < nq0 + 1 + nq1 + w.m && ok; ++t) {
+                for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
                     const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
                     const int qunit = t < nq0 ? k : k + 1;
                     const int g = t < nq0 ? t : t - nq0 - 1;
-                    const int jk = t == nq0 ? 0 : t - nq0 - nq1;
+                    const int jk = w.lo + (t == nq0 ? 0 : t - nq0 - nq1);
                     const int qb = qunit % QB, st = kt % ST;
                     if (!isq)
                         ++kt;
@@ -414,12 +417,12 @@ __global__ void __launch_bounds__(512, 1)
                     break;
                 const FwdUnit w = fwd_unit(u, GC, p);
                 const int qb = k % QB;
-                for (int jk = 0; jk <= w.m && ok; ++jk, ++kt) {
+                for (int jk = w.lo; jk <= w.m && ok; ++jk, ++kt) {
                     const int st = kt % ST;
                     for (int pi = 0; pi < GC; ++pi, ++n) {
                         const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
-                        const bool first = jk == 0 && (pi == 0 || ((pair - 1) >> 1) != hrel);
-                        if (jk == 0 && pi == 0 && have_prev) {
+                        const bool first = jk == w.lo && (pi == 0 || ((pair - 1) >> 1) != hrel);
+                        if (jk == w.lo && pi == 0 && have_prev) {
                             if (!issue_pv(prev, n - 1)) {
                                 ok = false;
                                 break;
@@ -429,8 +432,8 @@ __global__ void __launch_bounds__(512, 1)
                         // S(n) = Q'_hrel K'[64 half, +64)^T
                         if ((pi == 0 &&
                              !mbar_wait_warp(smem_u32(&bar_k_ready[st]), (kt / ST) & 1, wc)) ||
-                            (jk == 0 && !mbar_wait_warp(smem_u32(&bar_q_ready[qb][hrel]),
-                                                        (k / QB) & 1, wc)) ||
+                            (jk == w.lo && !mbar_wait_warp(smem_u32(&bar_q_ready[qb][hrel]),
+                                                           (k / QB) & 1, wc)) ||
                             (n >= 1 &&
                              !mbar_wait_warp(smem_u32(&bar_s_empty[wg]), (n - 1) & 1, wc))) {
                             ok = false;
@@ -490,11 +493,11 @@ __global__ void __launch_bounds__(512, 1)
             const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
             const int nq1 = has_next ? GC : 0;
             const int mnext = has_next ? fwd_unit(snake_unit(k + 1, cta, P), GC, p).m : 0;
-            for (int t = 0; t < nq0 + 1 + nq1 + w.m && ok; ++t) {
+            for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
                 const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
                 const int qunit = t < nq0 ? k : k + 1;
                 const int g = t < nq0 ? t : t - nq0 - 1;
-                const int jk = t == nq0 ? 0 : t - nq0 - nq1;
+                const int jk = w.lo + (t == nq0 ? 0 : t - nq0 - nq1);
                 const int qb = qunit % QB, st = kt % ST;
                 const uint32_t full = isq ? smem_u32(&bar_q_full[qb][g]) : smem_u32(&bar_k_full[st]);
                 const uint32_t par = isq ? ((qunit / QB) & 1) : ((kt / ST) & 1);
@@ -635,11 +638,11 @@ __global__ void __launch_bounds__(512, 1)
         if (u >= p.num_units)
             break;
         const FwdUnit un = fwd_unit(u, GC, p);
-        for (int jk = 0; jk <= un.m && ok; ++jk) {
+        for (int jk = un.lo; jk <= un.m && ok; ++jk) {
             for (int pi = 0; pi < GC; ++pi, ++n) {
                 const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
                 const int slot = hrel - ((wg * GC) >> 1);
-                const bool first = jk == 0 && (pi == 0 || ((pair - 1) >> 1) != hrel);
+                const bool first = jk == un.lo && (pi == 0 || ((pair - 1) >> 1) != hrel);
                 const uint32_t b = n & 1u;
                 const uint32_t s_addr = lane_base + C::COL_S + 64u * wg;
                 const uint32_t p_addr = lane_base + C::COL_P + 64u * wg + 32u * b;
@@ -659,13 +662,19 @@ __global__ void __launch_bounds__(512, 1)
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_s_empty[wg]));
 
-                // causal mask on the diagonal tile (key > query row)
-                if (jk == un.m) {
+                // causal mask on the diagonal tile (key > query row); with a
+                // sliding window also keys at or below row - W (local index
+                // <= wlim) on the tiles the window edge crosses
+                int wlim = -1;
+                if constexpr (WIN)
+                    wlim = un.m * kRows + r - p.window - (jk * kRows + 64 * half);
+                if (jk == un.m || (WIN && __any_sync(0xffffffffu, wlim >= 0))) {
+                    const int clim = (!WIN || jk == un.m) ? r - 64 * half : 1 << 30;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (64 * half + 32 * c + e > r)
+                            if (32 * c + e > clim || (WIN && 32 * c + e <= wlim))
                                 s[c][e] = __float_as_uint(-INFINITY);
                 }
                 float mx;
@@ -839,13 +848,13 @@ __global__ void __launch_bounds__(512, 1)
 }
 // ------------------------------------------------------------- launch ---
 
-template <int D, int GC, int ST>
+template <int D, int GC, int ST, bool WIN>
 static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                 const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
                                 const AttnParams &p0, cudaStream_t stream)
 {
     using C = FwdCfg<D, GC, ST>;
-    auto kern = fwd_kernel<D, GC, ST>;
+    auto kern = fwd_kernel<D, GC, ST, WIN>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
@@ -865,7 +874,9 @@ static cudaError_t launch_fwd_p(const CUtensorMap &q, const CUtensorMap &k, cons
                                 const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
                                 const AttnParams &p, cudaStream_t stream)
 {
-    return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST>(q, k, v, o, qs, ks, p, stream);
+    if (p.window > 0)
+        return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, true>(q, k, v, o, qs, ks, p, stream);
+    return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, false>(q, k, v, o, qs, ks, p, stream);
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

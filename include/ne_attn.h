@@ -159,6 +159,21 @@ int ne_attn_bwd_dkdv(const void *q, const void *k, const void *v, const float *l
                      float rope_theta, void *stream);
 
 /*
+ * Sliding-window variants (the per-layer window pattern of the nanochat
+ * guide): query t attends to keys t-W+1 .. t only, W = `window` >= 1; W = 0
+ * is the causal mask of ne_attn_fwd / ne_attn_bwd (W >= T gives the same
+ * result).  Everything else (arguments, layouts, workspace, errors) as for
+ * ne_attn_fwd and ne_attn_bwd; a negative window returns NE_ERR_ARG.  Key
+ * tiles entirely outside every row's window are skipped.
+ */
+int ne_attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, int window, void *stream);
+int ne_attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                       int d, float rope_theta, int window, void *stream);
+
+/*
  * Decode against a key/value cache (the chat loop of the NanoEuler README's
  * KV-cache inference engine): one new token per sequence.  Its key and value
  * are the cache's last rows, so it sits at position Tk - 1 and every cached

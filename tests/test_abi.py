@@ -110,3 +110,10 @@ def test_decode_workspace_size_and_argument_errors(lib):
     assert dec(a, a, a, a, a, a, ws, 1, 8, 34, 2, 64, 10000.0, None) == 3      # group of 17
     assert dec(a, a, a, a, a, a, 0, 1, 8, 2, 2, 64, 10000.0, None) == 5        # workspace
     assert dec(a + 2, a, a, a, a, a, ws, 1, 8, 2, 2, 64, 10000.0, None) == 4   # alignment
+
+
+def test_window_argument_errors(lib):
+    buf = ctypes.create_string_buffer(4096 + 64)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.ne_attn_fwd_window(a, a, a, a, a, 1, 8, 2, 2, 64, 10000.0, -1, None) == 9
+    assert lib.ne_attn_bwd_window(*([a] * 10), 1 << 20, 1, 8, 2, 2, 64, 10000.0, -3, None) == 9
