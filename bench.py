@@ -473,6 +473,79 @@ def run_decode(args):
     }
 
 
+def run_window(args):
+    """The training step's workload (16 layers x B64 T512 12/4 d64, own buffers)
+    with a sliding window of args.window keys: the training pair
+    (ne_attn_fwd_save, ne_attn_bwd_saved) with `window`, one CUDA graph per step.  Algorithmic flops
+    count the pairs inside the window only (t - W < s <= t)."""
+    import torch
+
+    import causal_gqa_attention_ne_gb300 as ne
+    Wn = args.window
+    ne.load_library()
+    dev = torch.device("cuda", 0)
+    layers = []
+    for layer in range(W.layers):
+        x = {n: t.to(dev) for n, t in ne_inputs.make_inputs(W, layer).items()}
+        x["o"] = torch.empty_like(x["q"])
+        x["lse"] = torch.empty(W.B, W.Hq, W.T, dtype=torch.float32, device=dev)
+        x["dq"], x["dk"], x["dv"] = (torch.empty_like(x["q"]), torch.empty_like(x["k"]),
+                                     torch.empty_like(x["v"]))
+        x["ws"] = torch.empty(ne.ne_attn_bwd_workspace_size(W.B, W.T, W.Hq, W.Hkv, W.d),
+                              dtype=torch.uint8, device=dev)
+        layers.append(x)
+
+    def step():
+        for d in layers:
+            ne.ne_attn_fwd_save(d["q"], d["k"], d["v"], d["o"], d["lse"], d["ws"], W.theta,
+                                window=Wn)
+            ne.ne_attn_bwd_saved(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"],
+                                 d["dk"], d["dv"], d["ws"], W.theta, window=Wn)
+
+    step()
+    torch.cuda.synchronize()
+    st = ne.ne_attn_get_error()
+    if st != 0:
+        raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)}")
+    cap = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        step()
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    e0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    pairs = sum(min(t + 1, Wn) for t in range(W.T))
+    flops = 14.0 * W.d * pairs * W.B * W.Hq * W.layers
+    peaks = load_peaks()
+    value = flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": f"sliding-window (W={Wn}) GQA attn fwd+bwd TFLOP/s at T=512 12/4 heads",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), see ne_inputs.py)",
+        "config": {"workload": W.name, "window": Wn, "pairs_per_head": pairs,
+                   "causal_pairs_per_head": W.pairs,
+                   "path": "ne_attn_fwd_save + ne_attn_bwd_saved with window"},
+        "tokens_per_s": W.tokens() * args.steps / (e0.elapsed_time(e1) * 1e-3),
+        "pct_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
+        "gpu_launches": 4 * W.layers * args.steps,
+        "clocks": sampler.summary(),
+    }
+
+
 def run_one_layer_for_profiler():
     """One layer (B64 T512 12/4 d64, 270 MB of buffers), fwd then bwd, twice.
     The first pass warms up; a profiler captures the second (-s 4 -c 4)."""
@@ -566,7 +639,13 @@ def main():
     ap.add_argument("--decode", action="store_true",
                     help="time decode against a KV cache (16 layers of B64, Tk 512) instead "
                          "of the training step; prints its own JSON line")
+    ap.add_argument("--window", type=int, default=0,
+                    help="time the training step with a sliding window of this many keys "
+                         "(the window entry points) instead; prints its own JSON line")
     args = ap.parse_args()
+    if args.window > 0:
+        print(json.dumps(run_window(args)), flush=True)
+        return
     if args.ncu_layer:
         run_one_layer_for_profiler()
         return

@@ -59,9 +59,9 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_fwd.restype = i
         lib.ne_attn_bwd.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd.restype = i
-        lib.ne_attn_fwd_save.argtypes = [vp] * 6 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd_save.argtypes = [vp] * 6 + [sz] + [i] * 5 + [f, i, vp]
         lib.ne_attn_fwd_save.restype = i
-        lib.ne_attn_bwd_saved.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_saved.argtypes = [vp] * 10 + [sz] + [i] * 5 + [f, i, vp]
         lib.ne_attn_bwd_saved.restype = i
         lib.ne_attn_bwd_preprocess_d.argtypes = [vp] * 3 + [sz] + [i] * 5 + [vp]
         lib.ne_attn_bwd_preprocess_d.restype = i
@@ -156,7 +156,7 @@ def _workspace_ptr(workspace):
 
 
 def ne_attn_fwd_save(q, k, v, o, lse, workspace, rope_theta: float = 10000.0,
-                     stream=None) -> None:
+                     stream=None, window: int = 0) -> None:
     """ne_attn_fwd that also leaves Q' and K' in `workspace` for ne_attn_bwd_saved."""
     B, T, Hq, Hkv, d = _dims(q, k)
     bf = torch.bfloat16
@@ -168,13 +168,13 @@ def ne_attn_fwd_save(q, k, v, o, lse, workspace, rope_theta: float = 10000.0,
     wp, wbytes = _workspace_ptr(workspace)
     rc = load_library().ne_attn_fwd_save(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          lse.data_ptr(), wp, wbytes, B, T, Hq, Hkv, d,
-                                         float(rope_theta), _stream_ptr(stream))
+                                         float(rope_theta), int(window), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_fwd_save")
 
 
 def ne_attn_bwd_saved(q, k, v, o, lse, do, dq, dk, dv, workspace, rope_theta: float = 10000.0,
-                      stream=None) -> None:
+                      stream=None, window: int = 0) -> None:
     """ne_attn_bwd on a workspace filled by ne_attn_fwd_save (D is recomputed, Q'/K' reused)."""
     B, T, Hq, Hkv, d = _dims(q, k)
     bf = torch.bfloat16
@@ -186,7 +186,7 @@ def ne_attn_bwd_saved(q, k, v, o, lse, do, dq, dk, dv, workspace, rope_theta: fl
     rc = load_library().ne_attn_bwd_saved(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                           o.data_ptr(), lse.data_ptr(), do.data_ptr(),
                                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), wp, wbytes,
-                                          B, T, Hq, Hkv, d, float(rope_theta),
+                                          B, T, Hq, Hkv, d, float(rope_theta), int(window),
                                           _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd_saved")

@@ -268,10 +268,10 @@ int ne_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse
 
 int ne_attn_fwd_save(const void *q, const void *k, const void *v, void *o, float *lse,
                      void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
-                     float rope_theta, void *stream)
+                     float rope_theta, int window, void *stream)
 {
     return fwd_impl(q, k, v, o, lse, workspace, workspace_bytes, true, B, T, Hq, Hkv, d,
-                    rope_theta, stream);
+                    rope_theta, stream, window);
 }
 
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int d)
@@ -484,8 +484,10 @@ int ne_attn_bwd_window(const void *q, const void *k, const void *v, const void *
 int ne_attn_bwd_saved(const void *q, const void *k, const void *v, const void *o,
                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
                       void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
-                      int d, float rope_theta, void *stream)
+                      int d, float rope_theta, int window, void *stream)
 {
+    if (window < 0)
+        return NE_ERR_ARG;
     if (!o || !dq || !dk || !dv)
         return NE_ERR_NULL;
     if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -496,6 +498,7 @@ int ne_attn_bwd_saved(const void *q, const void *k, const void *v, const void *o
                        rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
     if (rc != NE_OK)
         return rc;
+    p.window = window;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.o_in = o;
     // Q' and K' are already in the workspace: the preprocess computes D only

@@ -115,6 +115,8 @@ int ne_attn_bwd(const void *q, const void *k, const void *v, const void *o, cons
  * (the library cannot check this).  Results equal those of ne_attn_fwd
  * followed by ne_attn_bwd, bit for bit.  Errors as for ne_attn_fwd and
  * ne_attn_bwd (NE_ERR_WORKSPACE for a missing or short workspace).
+ * `window` is the sliding window of ne_attn_fwd_window (0: causal); both
+ * calls of a pair take the same value.
  */
 /*
  * ne_attn_bwd_saved runs these three steps: ne_attn_bwd_preprocess_d (D only,
@@ -126,11 +128,11 @@ int ne_attn_bwd_preprocess_d(const void *o, const void *dO, void *workspace,
                              void *stream);
 int ne_attn_fwd_save(const void *q, const void *k, const void *v, void *o, float *lse,
                      void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
-                     int d, float rope_theta, void *stream);
+                     int d, float rope_theta, int window, void *stream);
 int ne_attn_bwd_saved(const void *q, const void *k, const void *v, const void *o,
                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
                       void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
-                      int d, float rope_theta, void *stream);
+                      int d, float rope_theta, int window, void *stream);
 
 /*
  * The three steps ne_attn_bwd runs, in this order, exposed so a caller can

@@ -51,6 +51,25 @@ def test_window_matches_oracle(ne, B, T, Hq, Hkv, d, W):
     compare(got, ref, q, k)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,W", [(1, 384, 12, 4, 64, 129), (2, 300, 4, 2, 32, 64)])
+def test_window_training_pair_matches_oracle(ne, B, T, Hq, Hkv, d, W):
+    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1650 + T + W)
+    xd = to_dev(x)
+    q, k, v, do = xd["q"], xd["k"], xd["v"], xd["do"]
+    ws = torch.zeros(ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8,
+                     device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device="cuda")
+    ne.ne_attn_fwd_save(q, k, v, o, lse, ws, THETA, window=W)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ne.ne_attn_bwd_saved(q, k, v, o, lse, do, dq, dk, dv, ws, THETA, window=W)
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 0
+    q64, k64, v64, do64 = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
+    ref = oracle.attn_bwd(q64, k64, v64, do64, THETA, window=W)
+    compare({"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}, ref, q64, k64)
+
+
 def test_window_zero_is_the_causal_path(ne):
     x = to_dev(ne_inputs.make_custom(B=2, T=300, Hq=6, Hkv=2, d=64, seed=1700))
     got = _run(ne, x, 0)
