@@ -135,9 +135,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
 // and dO.  A row of D/8 16-byte chunks is read by D/8 consecutive lanes, so
 // one warp-wide load covers 32 / (D/8) whole rows; RU such loads of O and of
 // dO are in flight per lane before the row sums are reduced with shuffles.
-// Persistent: the grid is a multiple of the SM count and strides over rows.
+// Persistent: four CTAs per SM (the register budget of RU loads in flight),
+// all resident at once, striding over the rows.
+constexpr int kDCtasPerSm = 4;
 template <int D>
-__global__ void __launch_bounds__(256) bwd_d_kernel(const AttnParams p)
+__global__ void __launch_bounds__(256, kDCtasPerSm) bwd_d_kernel(const AttnParams p)
 {
     constexpr int LPR = D / 8;                 // lanes per row (one 16-byte chunk each)
     constexpr int RPW = 32 / LPR;              // rows per warp-wide load
@@ -196,7 +198,7 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
         if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return e;
-        const unsigned nb = static_cast<unsigned>(sms * 8);
+        const unsigned nb = static_cast<unsigned>(sms * kDCtasPerSm);
         switch (d) {
         case 32: return launch_pdl(bwd_d_kernel<32>, nb, 256, 0, stream, p);
         case 64: return launch_pdl(bwd_d_kernel<64>, nb, 256, 0, stream, p);
@@ -734,7 +736,8 @@ struct DkvCfg {
     static constexpr int OFF_V = KB * TL::BYTES;
     static constexpr int OFF_Q = 2 * KB * TL::BYTES;
     static constexpr int OFF_DO = OFF_Q + ST * TL::BYTES;
-    static constexpr int OFF_LSED = OFF_DO + ST * TL::BYTES;          // float2 [ST][128]
+    // float [ST][64 column pairs][-l2_c, -l2_c+1, -D_c, -D_c+1]
+    static constexpr int OFF_LSED = OFF_DO + ST * TL::BYTES;
     static constexpr int SMEM_BYTES = smem_one_cta(OFF_LSED + ST * kRows * 8 + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128;
@@ -781,7 +784,7 @@ __global__ void __launch_bounds__(512, 1)
     __shared__ uint64_t bar_acc_done, bar_acc_free, bar_drain;
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
-    float2 *lsed = reinterpret_cast<float2 *>(smem + C::OFF_LSED);
+    float *lsed = reinterpret_cast<float *>(smem + C::OFF_LSED);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cta = static_cast<int>(blockIdx.x), P = static_cast<int>(gridDim.x);
@@ -834,10 +837,16 @@ __global__ void __launch_bounds__(512, 1)
         }
     };
 
-    // Register budgets after the split (launched with 128 per thread x 512):
-    // rows 184 x 256 + RoPE 56 x 128 + TMA/MMA 80 x 128 <= 65536.
+    // Register budgets after the split (launched with 128 per thread x 512,
+    // four warps per sub-partition: 2 rows + lse/D + TMA/MMA <= 4 x 128):
+    // d <= 64: rows 192 + 56 + 72 = 512 / 2; d = 128 (wider issue loops):
+    // rows 184 + 56 + 80 = 504 / 2.
+    constexpr int kRowRegs = D == 128 ? 184 : 192;
     if (warp >= 12) {
-        regs_release<80>();
+        if constexpr (D == 128)
+            regs_release<80>();
+        else
+            regs_release<72>();
         if (warp == 12 && lane == 0) {
             // ------------------------------------------------ TMA producer ---
             tma_prefetch_desc(&tmQ);
@@ -1065,7 +1074,10 @@ __global__ void __launch_bounds__(512, 1)
                     ok = false;
                     break;
                 }
-                lsed[st * kRows + r] = make_float2(l2, dd);
+                // negated, paired by columns: one 16-byte load gives the row
+                // warps two columns' (-lse, -D) as packed fp32 pairs
+                lsed[st * 2 * kRows + (r >> 1) * 4 + (r & 1)] = -l2;
+                lsed[st * 2 * kRows + (r >> 1) * 4 + 2 + (r & 1)] = -dd;
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_q_ready[st]));
@@ -1077,7 +1089,7 @@ __global__ void __launch_bounds__(512, 1)
         return;
     } else {
         // ---------------------------------------------- row warpgroups ---
-        regs_claim<184>();
+        regs_claim<kRowRegs>();
         const int w = warp >> 2;                // column half of the score tile
         const int r = threadIdx.x & 127;        // key row == TMEM lane
         const uint32_t lane_base = tmem_addr(tbase, (warp & 3) * 32, 0);
@@ -1151,50 +1163,47 @@ __global__ void __launch_bounds__(512, 1)
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_s_empty));
 
-                const float4 *ld4 = reinterpret_cast<const float4 *>(lsed + st * kRows + 64 * w);
+                const float4 *ld4 =
+                    reinterpret_cast<const float4 *>(lsed + st * 2 * kRows + 2 * 64 * w);
                 uint32_t pp[32], dk[32];
-                const float sl2 = p.scale_log2;
+                const uint64_t sl2x2 = f32x2(p.scale_log2, p.scale_log2);
                 // sliding window: query columns c >= wmin (query >= key + W)
                 // are masked
                 int wmin = 1 << 30;
                 if constexpr (WIN)
                     wmin = un.n * kRows + r + p.window - mt * kRows;
-                if (mt != un.n && !(WIN && __any_sync(0xffffffffu, wmin < kRows))) {
+                // column pair (c, c+1): P = 2^(S sl2 - l2), dS = P (dP - D) on
+                // packed fp32 pairs; masked entries (query column c before key
+                // row r on the diagonal tile, or outside the window) get P = 0
+                const bool masked = mt == un.n || (WIN && __any_sync(0xffffffffu, wmin < kRows));
+                const int clo = (!WIN || mt == un.n) ? r : -1;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float4 a = ld4[(32 * h + e) >> 1];   // (l2, D) of 2 columns
-                            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -a.x));
-                            const float p1 =
-                                ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -a.z));
-                            const float d0 = p0 * (__uint_as_float(pv[h][e]) - a.y);
-                            const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - a.w);
-                            maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
-                            pp[16 * h + e / 2] = pack_bf16x2(p0, p1);
-                            dk[16 * h + e / 2] = pack_f16x2(d0, d1);
-                        }
-                } else {
-                    // diagonal tile: query column c < key row r is masked;
-                    // window: columns c >= wmin
-                    const int clo = (!WIN || mt == un.n) ? r : -1;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 32; e += 2) {
+                        const float4 a = ld4[(32 * h + e) >> 1];   // -l2, -l2', -D, -D'
+                        const uint64_t x2 = fma_f32x2(
+                            f32x2(__uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1])), sl2x2,
+                            f32x2(a.x, a.y));
+                        float x0, x1;
+                        f32x2_split(x2, x0, x1);
+                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        if (masked) {
                             const int c = 64 * w + 32 * h + e;
-                            const float4 a = ld4[(32 * h + e) >> 1];
-                            float p0 = ex2_approx(fmaf(__uint_as_float(sv[h][e]), sl2, -a.x));
-                            float p1 = ex2_approx(fmaf(__uint_as_float(sv[h][e + 1]), sl2, -a.z));
                             p0 = (c < clo || (WIN && c >= wmin)) ? 0.f : p0;
                             p1 = (c + 1 < clo || (WIN && c + 1 >= wmin)) ? 0.f : p1;
-                            const float d0 = p0 * (__uint_as_float(pv[h][e]) - a.y);
-                            const float d1 = p1 * (__uint_as_float(pv[h][e + 1]) - a.w);
-                            maxds = fmaxf(maxds, fmaxf(fabsf(d0), fabsf(d1)));
-                            pp[16 * h + e / 2] = pack_bf16x2(p0, p1);
-                            dk[16 * h + e / 2] = pack_f16x2(d0, d1);
                         }
-                }
+                        const uint64_t pr2 = f32x2(p0, p1);
+                        const uint64_t ds2 = mul_f32x2(
+                            pr2, add_f32x2(f32x2(__uint_as_float(pv[h][e]),
+                                                 __uint_as_float(pv[h][e + 1])),
+                                           f32x2(a.z, a.w)));
+                        float d0, d1;
+                        f32x2_split(ds2, d0, d1);
+                        maxds = fmax3(maxds, fabsf(d0), fabsf(d1));
+                        pp[16 * h + e / 2] = pack_bf16x2(p0, p1);
+                        dk[16 * h + e / 2] = pack_f16x2(d0, d1);
+                    }
                 if (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_pds_empty), (gi - 1) & 1, wc)) {
                     ok = false;
                     break;
