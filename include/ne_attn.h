@@ -18,6 +18,10 @@
  *
  * and the backward of L = sum(O * dO) with respect to the pre-RoPE q, k and
  * v; dk and dv are summed over the G query heads sharing each key/value head.
+ * Variants below: a training pair that hands the rotated Q' and K' from the
+ * forward to the backward, a sliding window (keys t-W+1 .. t), decode of one
+ * new token per sequence against a key/value cache, and a backward that
+ * allocates nothing.
  *
  * Layouts (all row-major, contiguous, no padding):
  *   q, o, dO, dq : bf16 [B][T][Hq][d]
