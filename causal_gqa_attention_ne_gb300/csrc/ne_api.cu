@@ -331,7 +331,10 @@ int run_dq(int d, const ne::AttnParams &base, void *dq, const CUtensorMap &mq,
     p.GC = ne::dq_heads_per_cta(d, p.G);
     p.nchunks = p.G / p.GC;
     p.out0 = dq;
-    return ne::launch_bwd_dq(d, mq, mk, mv, mdo, p, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+    CUtensorMap mdq;
+    if (make_map(&mdq, dq, p.B, p.T, p.Hq, d))
+        return NE_ERR_CUDA;
+    return ne::launch_bwd_dq(d, mq, mk, mv, mdo, mdq, p, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
 int run_dkdv(int d, const ne::AttnParams &base, void *dk, void *dv, const CUtensorMap &mq,

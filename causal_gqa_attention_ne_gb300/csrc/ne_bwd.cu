@@ -225,6 +225,44 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
     }
 }
 
+// The same for a D <= 64 tile leaving through shared memory: the row is
+// written as bf16 into this thread's row r of a 128-byte or 64-byte swizzled
+// staging block (the layout the TMA store of the output tensor reads).
+template <int D>
+__device__ __forceinline__ void epilogue_inverse_rope_stage(uint32_t taddr, float scale,
+                                                            uint32_t pos, const RopeFreqs &fr,
+                                                            uint8_t *stage, int r)
+{
+    static_assert(D <= 64, "one column block");
+    uint32_t a[32];
+    float x[D];
+    tmem_ld32(taddr, a);
+    if constexpr (D == 64) {
+        uint32_t b[32];
+        tmem_ld32(taddr + 32, b);
+        tmem_ld_wait(a);
+        tmem_tie(b);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(a[e]) * scale;
+            x[e + 32] = __uint_as_float(b[e]) * scale;
+        }
+    } else {
+        tmem_ld_wait(a);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            x[e] = __uint_as_float(a[e]) * scale;
+    }
+#pragma unroll
+    for (int e = 0; e < D / 2; ++e)
+        rope_inverse_pair(x[e], x[e + D / 2], pos, fr.turn[e]);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+        *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c)) =
+            make_uint4(pack_bf16x2(x[8 * c + 0], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                       pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+}
+
 // Epilogue for a gradient of a rotated operand: reads the D fp32 columns of
 // this thread's TMEM row at `col`, multiplies by `scale`, rotates back by
 // -angle(pos) and stores bf16 to dst (when `store`).
@@ -292,9 +330,15 @@ struct DqCfg {
     static constexpr int OFF_DO = OFF_Q + GC * TL::BYTES;
     static constexpr int OFF_K = OFF_DO + GC * TL::BYTES;
     static constexpr int OFF_V = OFF_K + ST * TL::BYTES;
-    static constexpr int SMEM_BYTES = smem_one_cta(OFF_V + ST * TL::BYTES + 1024);
+    // d <= 64: dq leaves through one shared-memory staging block per row
+    // warpgroup and a TMA store (a thread's own row would be 16-byte stores
+    // Hq*d*2 bytes apart, 32 transactions per warp store)
+    static constexpr bool STAGE = (D <= 64);
+    static constexpr int OFF_STG = OFF_V + ST * TL::BYTES;
+    static constexpr int SMEM_BYTES = smem_one_cta(OFF_STG + (STAGE ? 2 * TL::BLOCK : 0) + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DS = 256, COL_DQ = 320;
+    static_assert(!STAGE || TL::NB == 1, "staged epilogue stores one column block per head");
     static_assert(COL_DQ + GC * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -323,7 +367,7 @@ template <int D, int GC, int ST, bool WIN>
 __global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const AttnParams p)
+              const __grid_constant__ CUtensorMap tmDQ, const AttnParams p)
 {
     using C = DqCfg<D, GC, ST>;
     using TL = Tile<D>;
@@ -334,6 +378,7 @@ __global__ void __launch_bounds__(384, 1)
     __shared__ uint64_t bar_kv_full[ST], bar_kv_empty[ST];
     __shared__ uint64_t bar_s_full, bar_s_empty, bar_ds_full, bar_ds_empty;
     __shared__ uint64_t bar_dq_done, bar_dq_free, bar_drain;
+    __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
 
@@ -356,6 +401,10 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(smem_u32(&bar_ds_empty), 1);
         mbar_init(smem_u32(&bar_dq_done), 1);
         mbar_init(smem_u32(&bar_dq_free), 8);
+        for (int w2 = 0; w2 < 2; ++w2) {
+            mbar_init(smem_u32(&bar_stg_full[w2]), 4);
+            mbar_init(smem_u32(&bar_stg_free[w2]), 1);
+        }
         mbar_init(smem_u32(&bar_drain), 2);
         fence_mbar_init();
     }
@@ -570,6 +619,8 @@ __global__ void __launch_bounds__(384, 1)
     // dQ MMA waits for dq_free anyway.
     int pend_k = -1;
     DqUnit pend{};
+    uint8_t *stage = smem + C::OFF_STG + w * TL::BLOCK;   // this warpgroup's staging block
+    uint32_t nepi = 0;                                   // dq tiles this warpgroup has stored
     auto epilogue = [&]() {
         if (!mbar_wait_warp(smem_u32(&bar_dq_done), pend_k & 1, wc))
             return false;
@@ -579,10 +630,40 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int g = 0; g < GC; ++g)
             if ((g & 1) == w) {
-                __nv_bfloat16 *row =
-                    dq + ((static_cast<size_t>(pend.b) * p.T + t) * p.Hq + pend.h0 + g) * D;
-                epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
-                                         static_cast<uint32_t>(t), p.rope, row, t < p.T);
+                if constexpr (C::STAGE) {
+                    // the staging block is free once this group's previous
+                    // store has read it
+                    if (nepi >= 1) {
+                        if (warp == 4 * w && lane == 0) {
+                            bulk_wait_read0();
+                            mbar_arrive(smem_u32(&bar_stg_free[w]));
+                        }
+                        if (!mbar_wait_warp(smem_u32(&bar_stg_free[w]), (nepi - 1) & 1, wc))
+                            return false;
+                    }
+                    epilogue_inverse_rope_stage<D>(lane_base + C::COL_DQ + g * D, p.scale,
+                                                   static_cast<uint32_t>(t), p.rope, stage, r);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&bar_stg_full[w]));
+                    if (warp == 4 * w) {
+                        if (!mbar_wait_warp(smem_u32(&bar_stg_full[w]), nepi & 1, wc))
+                            return false;
+                        if (lane == 0) {
+                            tma_store_4d(&tmDQ, smem_u32(stage), 0, pend.h0 + g, pend.m * kRows,
+                                         pend.b);
+                            bulk_commit();
+                        }
+                        __syncwarp();
+                    }
+                    ++nepi;
+                } else {
+                    __nv_bfloat16 *row =
+                        dq + ((static_cast<size_t>(pend.b) * p.T + t) * p.Hq + pend.h0 + g) * D;
+                    epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
+                                             static_cast<uint32_t>(t), p.rope, row, t < p.T);
+                }
             }
         tc_fence_before();
         __syncwarp();
@@ -695,6 +776,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (ok && pend_k >= 0)
         ok = epilogue();
+    if constexpr (C::STAGE) {
+        if (warp == 4 * w && lane == 0)
+            bulk_wait0();
+    }
     if (maxds > kFp16Max)
         atomicOr(p.status, kDevRange);
     teardown();
@@ -1238,7 +1323,8 @@ __global__ void __launch_bounds__(512, 1)
 
 template <int D, int GC, int ST, bool WIN>
 static cudaError_t launch_dq_w(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &dO, const AttnParams &p0, cudaStream_t stream)
+                               const CUtensorMap &dO, const CUtensorMap &dq,
+                               const AttnParams &p0, cudaStream_t stream)
 {
     using C = DqCfg<D, GC, ST>;
     auto kern = dq_kernel<D, GC, ST, WIN>;
@@ -1253,42 +1339,44 @@ static cudaError_t launch_dq_w(const CUtensorMap &q, const CUtensorMap &k, const
     AttnParams p = p0;
     p.num_units = p.M * p.B * p.Hkv * p.nchunks;
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
-    return launch_pdl(kern, grid, 384, C::SMEM_BYTES, stream, q, k, v, dO, p);
+    return launch_pdl(kern, grid, 384, C::SMEM_BYTES, stream, q, k, v, dO, dq, p);
 }
 
 template <int D, int GC, int ST>
 static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
+                               const CUtensorMap &dO, const CUtensorMap &dq, const AttnParams &p,
+                               cudaStream_t stream)
 {
     if (p.window > 0)
-        return launch_dq_w<D, GC, ST, true>(q, k, v, dO, p, stream);
-    return launch_dq_w<D, GC, ST, false>(q, k, v, dO, p, stream);
+        return launch_dq_w<D, GC, ST, true>(q, k, v, dO, dq, p, stream);
+    return launch_dq_w<D, GC, ST, false>(q, k, v, dO, dq, p, stream);
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                          const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
+                          const CUtensorMap &dO, const CUtensorMap &dq, const AttnParams &p,
+                          cudaStream_t stream)
 {
     switch (d) {
     case 32:
         switch (p.GC) {
-        case 1: return launch_dq_t<32, 1, 4>(q, k, v, dO, p, stream);
-        case 2: return launch_dq_t<32, 2, 4>(q, k, v, dO, p, stream);
-        case 3: return launch_dq_t<32, 3, 4>(q, k, v, dO, p, stream);
-        case 4: return launch_dq_t<32, 4, 4>(q, k, v, dO, p, stream);
+        case 1: return launch_dq_t<32, 1, 4>(q, k, v, dO, dq, p, stream);
+        case 2: return launch_dq_t<32, 2, 4>(q, k, v, dO, dq, p, stream);
+        case 3: return launch_dq_t<32, 3, 4>(q, k, v, dO, dq, p, stream);
+        case 4: return launch_dq_t<32, 4, 4>(q, k, v, dO, dq, p, stream);
         default: break;
         }
         break;
     case 64:
         switch (p.GC) {
-        case 1: return launch_dq_t<64, 1, 3>(q, k, v, dO, p, stream);
-        case 2: return launch_dq_t<64, 2, 3>(q, k, v, dO, p, stream);
-        case 3: return launch_dq_t<64, 3, 3>(q, k, v, dO, p, stream);
+        case 1: return launch_dq_t<64, 1, 3>(q, k, v, dO, dq, p, stream);
+        case 2: return launch_dq_t<64, 2, 3>(q, k, v, dO, dq, p, stream);
+        case 3: return launch_dq_t<64, 3, 3>(q, k, v, dO, dq, p, stream);
         default: break;
         }
         break;
     case 128:
         if (p.GC == 1)
-            return launch_dq_t<128, 1, 2>(q, k, v, dO, p, stream);
+            return launch_dq_t<128, 1, 2>(q, k, v, dO, dq, p, stream);
         break;
     default: break;
     }

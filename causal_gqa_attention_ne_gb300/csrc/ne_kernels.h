@@ -21,9 +21,11 @@ cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const 
 cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot, const void *k,
                            void *krot, cudaStream_t stream);
 
-// Backward dQ (query-tile major, recomputes S and dP).
+// Backward dQ (query-tile major, recomputes S and dP); `dq` is the tensor
+// map of the output (same layout as q), used by its TMA store (d <= 64).
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                          const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream);
+                          const CUtensorMap &dO, const CUtensorMap &dq, const AttnParams &p,
+                          cudaStream_t stream);
 
 // Backward dK, dV (key-tile major; dK and dV summed over the query heads of
 // each KV head inside the CTA).  `q` and `k` are the fp16 rotated Q' / K' maps.
