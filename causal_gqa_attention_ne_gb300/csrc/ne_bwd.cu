@@ -230,7 +230,8 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
 // staging block (the layout the TMA store of the output tensor reads).
 template <int D>
 __device__ __forceinline__ void epilogue_inverse_rope_stage(uint32_t taddr, float scale,
-                                                            uint32_t pos, const RopeFreqs &fr,
+                                                            const float (&sn)[D / 2],
+                                                            const float (&cs)[D / 2],
                                                             uint8_t *stage, int r)
 {
     static_assert(D <= 64, "one column block");
@@ -253,9 +254,14 @@ __device__ __forceinline__ void epilogue_inverse_rope_stage(uint32_t taddr, floa
         for (int e = 0; e < 32; ++e)
             x[e] = __uint_as_float(a[e]) * scale;
     }
+    // rotation by -angle: (x, y) -> (x cos + y sin, y cos - x sin)
 #pragma unroll
-    for (int e = 0; e < D / 2; ++e)
-        rope_inverse_pair(x[e], x[e + D / 2], pos, fr.turn[e]);
+    for (int e = 0; e < D / 2; ++e) {
+        const float u = x[e] * cs[e] + x[e + D / 2] * sn[e];
+        const float w = x[e + D / 2] * cs[e] - x[e] * sn[e];
+        x[e] = u;
+        x[e + D / 2] = w;
+    }
 #pragma unroll
     for (int c = 0; c < D / 8; ++c)
         *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c)) =
@@ -627,6 +633,13 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         const int t = pend.m * kRows + r;
         __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(p.out0);
+        // the row's sines and cosines, shared by the warpgroup's heads
+        float sn[D <= 64 ? D / 2 : 1], cs[D <= 64 ? D / 2 : 1];
+        if constexpr (C::STAGE) {
+#pragma unroll
+            for (int e = 0; e < D / 2; ++e)
+                rope_sincos(static_cast<uint32_t>(t), p.rope.turn[e], sn[e], cs[e]);
+        }
 #pragma unroll
         for (int g = 0; g < GC; ++g)
             if ((g & 1) == w) {
@@ -641,8 +654,8 @@ __global__ void __launch_bounds__(384, 1)
                         if (!mbar_wait_warp(smem_u32(&bar_stg_free[w]), (nepi - 1) & 1, wc))
                             return false;
                     }
-                    epilogue_inverse_rope_stage<D>(lane_base + C::COL_DQ + g * D, p.scale,
-                                                   static_cast<uint32_t>(t), p.rope, stage, r);
+                    epilogue_inverse_rope_stage<D>(lane_base + C::COL_DQ + g * D, p.scale, sn, cs,
+                                                   stage, r);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0)
