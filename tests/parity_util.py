@@ -2,7 +2,7 @@
 binding, run the oracle on the same seeded inputs, compare with the stated
 tolerances.
 
-Tolerances (the spec contract for bf16 inputs and tensor-core operands):
+Tolerances (the stated bounds for bf16 inputs and tensor-core operands):
   O           norm-wise max relative error <= 1e-2
   dq, dk, dv  norm-wise max relative error <= 2e-2
   lse         absolute error <= 1e-3 * max(1, |q_t| max_s |k_s| / d)
