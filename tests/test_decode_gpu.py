@@ -66,3 +66,14 @@ def test_decode_at_the_116m_chat_shape_sampled(ne):
     ro, rl = oracle.attn_decode(*(ne_inputs.as_f64(t[rows]) for t in (q1, k, v)), THETA)
     assert rel_err(o[rows].float().cpu().numpy(), ro) <= TOL_O
     assert float(np.abs(lse[rows].cpu().double().numpy() - rl).max()) <= TOL_LSE
+
+
+def test_decode_long_cache(ne):
+    # 4096 cached positions: 32 chunks merged per (b, h)
+    q1, k, v = _case(2, 4096, 16, 4, 128, 1502)
+    o, lse = ne.attention_decode(q1.cuda(), k.cuda(), v.cuda(), THETA)
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 0
+    ro, rl = oracle.attn_decode(*(ne_inputs.as_f64(t) for t in (q1, k, v)), THETA)
+    assert rel_err(o.float().cpu().numpy(), ro) <= TOL_O
+    assert float(np.abs(lse.cpu().double().numpy() - rl).max()) <= TOL_LSE

@@ -78,3 +78,20 @@ def test_window_zero_is_the_causal_path(ne):
     torch.cuda.synchronize()
     for n, ref in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
         assert torch.equal(got[n], ref), n
+
+
+def test_window_long_context_sampled(ne):
+    """T = 2048 with W = 300: most key tiles of a query tile lie outside the
+    window and are skipped; the oracle checks two (batch, kv head) groups."""
+    from parity_util import slice_gpu
+    B, T, Hq, Hkv, d, W = 2, 2048, 8, 2, 128, 300
+    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1800)
+    got = _run(ne, to_dev(x), W)
+    q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
+    G = Hq // Hkv
+    for (b, j) in ((0, 0), (1, 1)):
+        ref = oracle.attn_bwd(oracle.group_slice(q, b, j, G), oracle.group_slice(k, b, j, 1),
+                              oracle.group_slice(v, b, j, 1), oracle.group_slice(do, b, j, G),
+                              THETA, window=W)
+        compare(slice_gpu(got, b, j, G), ref, oracle.group_slice(q, b, j, G),
+                oracle.group_slice(k, b, j, 1))
