@@ -18,7 +18,8 @@
 //               its running max and sum in registers; thread r owns query
 //               row r (TMEM lane r) of the item's 128 x 64 score block.  For
 //               odd GC one head is split between the groups: each keeps a
-//               partial O, max and sum, merged once at the end of the unit.
+//               partial O, max and sum, merged once at the end of the unit
+//               (by group 0 in even units, group 1 in odd ones).
 //               The running max moves lazily (only when it grows by more
 //               than 2^8; the final division by l makes the result exact
 //               either way).  Each group has one S buffer, released as soon
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(512, 1)
     // unit (pair 2h + x = head h, keys [64x, 64x + 64) of every key tile), so
     // the running max and sum of each of its heads stay in registers.  With
     // GC odd one head's two halves belong to different groups; the groups
-    // merge it at the end of the unit (group 0 stores it).
+    // merge it at the end of the unit.
     regs_claim<184>();
     const int wg = warp >> 2;               // softmax group
     const int q4 = warp & 3;                // TMEM lane quarter
@@ -796,14 +797,23 @@ __global__ void __launch_bounds__(512, 1)
             break;
         }
         tc_fence_after();
-        for (int slot = 0; slot < C::NSL && ok; ++slot) {
+        // The split head (odd GC) is merged and stored by group k % 2, so the
+        // two groups' epilogues carry the same work over consecutive units;
+        // the merging group stores its own head first, the other group
+        // publishes its half first.
+        const int ss = wg == 0 ? C::NSL - 1 : 0;            // this group's split slot
+        const int og = 1 - wg, oss = og == 0 ? C::NSL - 1 : 0;
+        const bool merging = !C::SPLIT || (k & 1) == wg;
+        for (int i = 0; i < C::NSL && ok; ++i) {
+            int slot = i;
+            if constexpr (C::SPLIT && C::NSL == 2)
+                slot = (merging == (i == 1)) ? ss : 1 - ss;
             const int h = un.h0 + ((wg * GC) >> 1) + slot;
             const float m_s = slot ? mr1 : mr0, l_s = slot ? lr1 : lr0;
             const uint32_t oa = lane_base + C::COL_O + (wg * C::NSL + slot) * D;
-            const bool split = C::SPLIT && (wg == 0 ? slot == C::NSL - 1 : slot == 0);
-            if (split && wg == 1) {
-                // hand this half's max and sum to group 0, which merges and
-                // stores the head
+            const bool split = C::SPLIT && slot == ss;
+            if (split && !merging) {
+                // hand this half's max and sum to the merging group
                 split_ml[r] = m_s;
                 split_ml[kRows + r] = l_s;
                 __syncwarp();
@@ -824,7 +834,7 @@ __global__ void __launch_bounds__(512, 1)
                 sa = ex2_approx(m_s - m_tot);
                 sb = ex2_approx(m1 - m_tot);   // 0 when that half saw no key
                 l_tot = fmaf(l_s, sa, l1 * sb);
-                ob = lane_base + C::COL_O + (1 * C::NSL + 0) * D;
+                ob = lane_base + C::COL_O + (og * C::NSL + oss) * D;
             }
             const float inv_l = 1.f / l_tot;
             if (!store_head(un, h, oa, split, ob, sa, sb, inv_l, m_tot + __log2f(l_tot))) {
@@ -836,7 +846,7 @@ __global__ void __launch_bounds__(512, 1)
             if (lane == 0) {
                 mbar_arrive(smem_u32(&bar_o_free[wg][slot]));
                 if (split)
-                    mbar_arrive(smem_u32(&bar_o_free[1][0]));
+                    mbar_arrive(smem_u32(&bar_o_free[og][oss]));
             }
         }
     }
