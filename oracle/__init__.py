@@ -60,6 +60,13 @@ def _bind(path: str):
     lib.ne_oracle_decode.restype = ctypes.c_int
     lib.ne_oracle_decode.argtypes = [_DP] * 5 + [ctypes.c_int] * 5 + [
         ctypes.c_double, ctypes.c_long]
+    _IP = ctypes.POINTER(ctypes.c_int)
+    lib.ne_oracle_fwd_varlen.restype = ctypes.c_int
+    lib.ne_oracle_fwd_varlen.argtypes = [_DP] * 5 + [_IP] + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_bwd_varlen.restype = ctypes.c_int
+    lib.ne_oracle_bwd_varlen.argtypes = [_DP] * 7 + [_IP] + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
     lib.ne_oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -149,6 +156,54 @@ class Oracle:
         return o1, lse1
 
 
+    def _seqlens(self, seqlens, B: int):
+        sl = np.ascontiguousarray(np.asarray(seqlens).reshape(-1), dtype=np.intc)
+        if sl.shape != (B,):
+            raise ValueError(f"seqlens must hold {B} lengths")
+        return sl
+
+    def attn_fwd_varlen(self, q, k, v, seqlens, theta: float, pos_offset: int = 0,
+                        threads: int = 0):
+        """Padded variable-length batch: sequence b is its first seqlens[b] rows, a
+        causal problem of its own; padding rows get O = 0 and lse = -inf.
+        Returns (o [B,T,Hq,d], lse [B,Hq,T])."""
+        q, k, v = _c(q), _c(k), _c(v)
+        B, T, Hq, d = q.shape
+        Hkv = k.shape[2]
+        if k.shape != (B, T, Hkv, d) or v.shape != k.shape:
+            raise ValueError("k and v must be [B, T, Hkv, d] matching q")
+        sl = self._seqlens(seqlens, B)
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, T), dtype=np.float64)
+        rc = self._lib.ne_oracle_fwd_varlen(
+            _p(q), _p(k), _p(v), _p(o), _p(lse), sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+            B, T, Hq, Hkv, d, float(theta), int(pos_offset), int(threads))
+        if rc:
+            raise ValueError(f"ne_oracle_fwd_varlen failed with code {rc}")
+        return o, lse
+
+    def attn_bwd_varlen(self, q, k, v, do, seqlens, theta: float, pos_offset: int = 0,
+                        threads: int = 0):
+        """Gradients of the sum of O * dO over the valid rows of a padded
+        variable-length batch; 0 on padding positions.  Dict with dq, dk, dv."""
+        q, k, v, do = _c(q), _c(k), _c(v), _c(do)
+        B, T, Hq, d = q.shape
+        Hkv = k.shape[2]
+        if do.shape != q.shape or k.shape != (B, T, Hkv, d) or v.shape != k.shape:
+            raise ValueError("shape mismatch")
+        sl = self._seqlens(seqlens, B)
+        dq = np.empty_like(q)
+        dk = np.empty_like(k)
+        dv = np.empty_like(v)
+        rc = self._lib.ne_oracle_bwd_varlen(
+            _p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv),
+            sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), B, T, Hq, Hkv, d, float(theta),
+            int(pos_offset), int(threads))
+        if rc:
+            raise ValueError(f"ne_oracle_bwd_varlen failed with code {rc}")
+        return {"dq": dq, "dk": dk, "dv": dv}
+
+
 def compile_source(src_path: str, lib_path: str) -> str:
     """Compile one copy of the oracle's C source into a shared library."""
     tmp = lib_path + f".tmp{os.getpid()}"
@@ -190,6 +245,14 @@ def attn_bwd(q, k, v, do, theta: float, pos_offset: int = 0, threads: int = 0,
 
 def attn_decode(q1, k, v, theta: float, pos_offset: int = 0):
     return default().attn_decode(q1, k, v, theta, pos_offset)
+
+
+def attn_fwd_varlen(q, k, v, seqlens, theta: float, pos_offset: int = 0, threads: int = 0):
+    return default().attn_fwd_varlen(q, k, v, seqlens, theta, pos_offset, threads)
+
+
+def attn_bwd_varlen(q, k, v, do, seqlens, theta: float, pos_offset: int = 0, threads: int = 0):
+    return default().attn_bwd_varlen(q, k, v, do, seqlens, theta, pos_offset, threads)
 
 
 def group_slice(x: np.ndarray, b: int, j: int, heads_per_group: int):

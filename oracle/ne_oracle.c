@@ -280,6 +280,81 @@ int ne_oracle_bwd(const double *q, const double *k, const double *v, const doubl
 }
 
 /*
+ * Variable-length (padded) batches: sequence b holds its first seqlen[b]
+ * tokens, 0 <= seqlen[b] <= T, and the rows after them are padding.  The
+ * NanoEuler SFT stage pads every instruction/response pair to the context
+ * and masks the loss on prompt and padding ("Rebuilding GPT-2 in one 100KB
+ * C/CUDA file" section 3.2, SFT stage; "NanoEuler: a GPT-2-scale LLM"
+ * two-stage training, SFT).  Each sequence is its own causal problem over
+ * its L = seqlen[b] tokens (positions 0 .. L-1), so the definition is the
+ * attention above applied to every sequence's prefix; a padding row attends
+ * to nothing: O = 0, lse = -inf.  In the backward only the valid rows carry
+ * a loss, so dq, dk, dv are the prefix problem's gradients and 0 on padding
+ * positions (dO of padding rows is never read).  A sequence's prefix rows are
+ * contiguous in the [B][T][H][d] layout, so each call below is the B = 1,
+ * T = L problem on a pointer into batch b.
+ */
+int ne_oracle_fwd_varlen(const double *q, const double *k, const double *v, double *o,
+                         double *lse, const int *seqlen, int B, int T, int Hq, int Hkv, int d,
+                         double theta, long pos_offset, int nthreads)
+{
+    if (check_shape(B, T, Hq, Hkv, d) || !seqlen)
+        return 1;
+    for (int b = 0; b < B; ++b)
+        if (seqlen[b] < 0 || seqlen[b] > T)
+            return 1;
+    double *lse1 = malloc(sizeof(double) * (size_t)Hq * T);
+    if (!lse1)
+        return 2;
+    int err = 0;
+    for (int b = 0; b < B && !err; ++b) {
+        int L = seqlen[b];
+        for (int t = L; t < T; ++t)
+            memset(o + IDX(b, t, 0, 0, T, Hq, d), 0, sizeof(double) * Hq * d);
+        for (int h = 0; h < Hq; ++h)
+            for (int t = L; t < T; ++t)
+                lse[((size_t)b * Hq + h) * T + t] = -INFINITY;
+        if (L == 0)
+            continue;
+        err = ne_oracle_fwd(q + IDX(b, 0, 0, 0, T, Hq, d), k + IDX(b, 0, 0, 0, T, Hkv, d),
+                            v + IDX(b, 0, 0, 0, T, Hkv, d), o + IDX(b, 0, 0, 0, T, Hq, d), lse1,
+                            1, L, Hq, Hkv, d, theta, pos_offset, nthreads, 0);
+        for (int h = 0; h < Hq; ++h)
+            memcpy(lse + ((size_t)b * Hq + h) * T, lse1 + (size_t)h * L, sizeof(double) * L);
+    }
+    free(lse1);
+    return err;
+}
+
+int ne_oracle_bwd_varlen(const double *q, const double *k, const double *v, const double *dO,
+                         double *dq, double *dk, double *dv, const int *seqlen, int B, int T,
+                         int Hq, int Hkv, int d, double theta, long pos_offset, int nthreads)
+{
+    if (check_shape(B, T, Hq, Hkv, d) || !seqlen)
+        return 1;
+    for (int b = 0; b < B; ++b)
+        if (seqlen[b] < 0 || seqlen[b] > T)
+            return 1;
+    int err = 0;
+    for (int b = 0; b < B && !err; ++b) {
+        int L = seqlen[b];
+        for (int t = L; t < T; ++t) {
+            memset(dq + IDX(b, t, 0, 0, T, Hq, d), 0, sizeof(double) * Hq * d);
+            memset(dk + IDX(b, t, 0, 0, T, Hkv, d), 0, sizeof(double) * Hkv * d);
+            memset(dv + IDX(b, t, 0, 0, T, Hkv, d), 0, sizeof(double) * Hkv * d);
+        }
+        if (L == 0)
+            continue;
+        err = ne_oracle_bwd(q + IDX(b, 0, 0, 0, T, Hq, d), k + IDX(b, 0, 0, 0, T, Hkv, d),
+                            v + IDX(b, 0, 0, 0, T, Hkv, d), dO + IDX(b, 0, 0, 0, T, Hq, d),
+                            dq + IDX(b, 0, 0, 0, T, Hq, d), dk + IDX(b, 0, 0, 0, T, Hkv, d),
+                            dv + IDX(b, 0, 0, 0, T, Hkv, d), NULL, NULL, NULL, 1, L, Hq, Hkv, d,
+                            theta, pos_offset, nthreads, 0);
+    }
+    return err;
+}
+
+/*
  * Decode against a key/value cache (one new token per sequence).  The new
  * token is the last of Tk positions: its own key and value are the cache's
  * last rows, so every cached key is visible to it.  By definition this is the

@@ -386,6 +386,78 @@ def pin_decode_closed_forms(orc):
     assert np.abs(lse1 - (q1 * kk).sum(-1) / math.sqrt(d)).max() < 1e-13
 
 
+def pin_varlen_torch_sdpa(orc):
+    """Padded variable-length batches against torch in float64: complex-rotation
+    RoPE, scaled_dot_product_attention with a per-sequence mask (valid row t of
+    sequence b sees keys s <= t; a padding row sees only itself, so torch stays
+    finite there) and autograd of the sum of O * dO over valid rows only.  Valid
+    rows of O and lse, and every gradient element, to 1e-10; padding rows of O
+    exactly 0 and of lse exactly -inf; padding gradients exactly 0."""
+    for (B, T, Hq, Hkv, d, lens, seed) in ((3, 37, 6, 2, 16, (37, 0, 20), 121),
+                                           (4, 30, 4, 4, 8, (1, 29, 13, 30), 122),
+                                           (2, 50, 4, 1, 8, (7, 33), 123)):
+        x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=seed)
+        q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
+        L = torch.tensor(lens)
+        t = torch.arange(T)
+        valid = t[None, :] < L[:, None]                                   # [B, T]
+        allowed = (t[None, None, :] <= t[None, :, None]) & valid[:, :, None]
+        allowed = allowed | torch.eye(T, dtype=torch.bool)[None]         # padding: itself
+        tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+        qr = _torch_rope(tq, THETA).transpose(1, 2)
+        kr = _torch_rope(tk, THETA).transpose(1, 2)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qr, kr, tv.transpose(1, 2), attn_mask=allowed[:, None], scale=1.0 / math.sqrt(d),
+            enable_gqa=True)
+        dmask = valid[:, None, :, None].to(torch.float64)
+        (o * torch.tensor(do).transpose(1, 2) * dmask).sum().backward()
+        with torch.no_grad():
+            sc = qr @ kr.repeat_interleave(Hq // Hkv, dim=1).transpose(-1, -2) / math.sqrt(d)
+            lse = torch.logsumexp(sc.masked_fill(~allowed[:, None], float("-inf")), dim=-1)
+        o1, lse1 = orc.attn_fwd_varlen(q, k, v, lens, THETA)
+        r = orc.attn_bwd_varlen(q, k, v, do, lens, THETA)
+        vm = valid.numpy()
+        ot = o.detach().transpose(1, 2).numpy()
+        assert _rel(o1[vm], ot[vm]) < 1e-10, "o"
+        assert (o1[~vm] == 0).all(), "padding rows of O"
+        lm = np.broadcast_to(vm[:, None, :], lse1.shape)
+        assert np.abs(lse1[lm] - lse.numpy()[lm]).max() < 1e-10, "lse"
+        assert np.isneginf(lse1[~lm]).all(), "padding rows of lse"
+        for n, g in (("dq", tq.grad), ("dk", tk.grad), ("dv", tv.grad)):
+            assert _rel(r[n], g.numpy()) < 1e-10, (n, _rel(r[n], g.numpy()))
+            assert (r[n][~vm] == 0).all(), (n, "padding positions")
+
+
+def pin_varlen_prefix_and_closed_forms(orc):
+    """A causal row never sees a later key, so the valid rows of a padded batch
+    equal the same rows of the plain causal forward over all T rows; a length
+    of T is the causal forward, bit for bit.  L = 0: everything is padding
+    (O = 0, lse = -inf, gradients 0).  L = 1: O[0] = v[0] of the head's group,
+    lse[0] = <q_0, k_0> / sqrt(d) (position 0 rotates nothing), dq = dk = 0
+    (the one probability is 1 whatever the score) and dv[0] = the sum of dO[0]
+    over the group's query heads."""
+    B, T, Hq, Hkv, d = 4, 21, 6, 2, 8
+    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=125)
+    q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
+    lens = (21, 0, 1, 9)
+    o, lse = orc.attn_fwd_varlen(q, k, v, lens, THETA)
+    oc, lc = orc.attn_fwd(q, k, v, THETA)
+    assert (o[0] == oc[0]).all() and (lse[0] == lc[0]).all()
+    assert _rel(o[3, :9], oc[3, :9]) < 1e-13 and np.abs(lse[3, :, :9] - lc[3, :, :9]).max() < 1e-12
+    assert (o[1] == 0).all() and np.isneginf(lse[1]).all()
+    G = Hq // Hkv
+    assert _rel(o[2, 0], np.repeat(v[2, 0], G, axis=0)) < 1e-14
+    want = (q[2, 0] * np.repeat(k[2, 0], G, axis=0)).sum(-1) / math.sqrt(d)
+    assert np.abs(lse[2, :, 0] - want).max() < 1e-13
+    r = orc.attn_bwd_varlen(q, k, v, do, lens, THETA)
+    rc = orc.attn_bwd(q[:1], k[:1], v[:1], do[:1], THETA)
+    for n in ("dq", "dk", "dv"):
+        assert (r[n][0] == rc[n][0]).all(), n
+        assert (r[n][1] == 0).all(), n
+    assert np.abs(r["dq"][2, 0]).max() < 1e-14 and np.abs(r["dk"][2, 0]).max() < 1e-14
+    assert _rel(r["dv"][2, 0], do[2, 0].reshape(Hkv, G, d).sum(axis=1)) < 1e-14
+
+
 ALL_PINS = [
     pin_rope_closed_form,
     pin_rope_identity_and_orthogonal,
@@ -404,4 +476,6 @@ ALL_PINS = [
     pin_decode_torch_sdpa,
     pin_decode_is_last_causal_row,
     pin_decode_closed_forms,
+    pin_varlen_torch_sdpa,
+    pin_varlen_prefix_and_closed_forms,
 ]

@@ -43,6 +43,16 @@ MUTATIONS = [
     ("decode_query_position", "(long)(Tk - 1) + pos_offset, 0);", "(long)Tk + pos_offset, 0);"),
     ("decode_kv_head_interleaved", "const int kvh = h / G;", "const int kvh = h % Hkv;"),
     ("decode_drops_normaliser", "double pr = exp(S[s] - lse_bh);", "double pr = exp(S[s] - mx);"),
+    ("varlen_lse_padding_zero", "lse[((size_t)b * Hq + h) * T + t] = -INFINITY;",
+     "lse[((size_t)b * Hq + h) * T + t] = 0.0;"),
+    ("varlen_fwd_full_length", "1, L, Hq, Hkv, d, theta, pos_offset, nthreads, 0);",
+     "1, T, Hq, Hkv, d, theta, pos_offset, nthreads, 0);"),
+    ("varlen_bwd_reads_padding_dO", "NULL, NULL, NULL, 1, L, Hq, Hkv, d,",
+     "NULL, NULL, NULL, 1, T, Hq, Hkv, d,"),
+    ("varlen_batch_stride", "err = ne_oracle_fwd(q + IDX(b, 0, 0, 0, T, Hq, d),",
+     "err = ne_oracle_fwd(q + IDX(b, 0, 0, 0, L, Hq, d),"),
+    ("varlen_lse_row_stride", "lse1 + (size_t)h * L, sizeof(double) * L);",
+     "lse1 + (size_t)h * T, sizeof(double) * L);"),
 ]
 
 
