@@ -546,6 +546,95 @@ def run_window(args):
     }
 
 
+def run_varlen(args):
+    """The 116M SFT step: 16 layers of B64 sequences padded to T=512 (12/4
+    heads, d64), each sequence with its own seeded valid length (ne_inputs:
+    uniform on [16, 512]); per layer ne_attn_fwd_varlen then ne_attn_bwd_varlen,
+    launched eagerly (the calls copy their unit tables from host memory, which
+    a CUDA graph cannot capture).  Algorithmic flops count the causal pairs of
+    the valid rows only.  The padded causal step (ne_attn_fwd + ne_attn_bwd on
+    the same buffers, also eager) is timed beside it."""
+    import numpy as np
+    import torch
+
+    import causal_gqa_attention_ne_gb300 as ne
+    w = ne_inputs.SFT_116M
+    lens = w.seqlens()
+    ne.load_library()
+    dev = torch.device("cuda", 0)
+    layers = []
+    for layer in range(w.layers):
+        x = {n: t.to(dev) for n, t in ne_inputs.make_inputs(w, layer).items()}
+        x["o"] = torch.empty_like(x["q"])
+        x["lse"] = torch.empty(w.B, w.Hq, w.T, dtype=torch.float32, device=dev)
+        x["dq"], x["dk"], x["dv"] = (torch.empty_like(x["q"]), torch.empty_like(x["k"]),
+                                     torch.empty_like(x["v"]))
+        x["ws"] = torch.empty(ne.ne_attn_varlen_workspace_size(w.B, w.T, w.Hq, w.Hkv, w.d),
+                              dtype=torch.uint8, device=dev)
+        layers.append(x)
+    sl = np.asarray(lens, dtype=np.int32)
+
+    def step_varlen():
+        for d in layers:
+            ne.ne_attn_fwd_varlen(d["q"], d["k"], d["v"], d["o"], d["lse"], sl, d["ws"], w.theta)
+            ne.ne_attn_bwd_varlen(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"],
+                                  d["dk"], d["dv"], sl, d["ws"], w.theta)
+
+    def step_padded():
+        for d in layers:
+            ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], w.theta)
+            ne.ne_attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"],
+                           d["dv"], d["ws"], w.theta)
+
+    def timed(step, sampler=None):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        st = ne.ne_attn_get_error()
+        if st != 0:
+            raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)}")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if sampler:
+            sampler.mark(True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark(False)
+        return e0.elapsed_time(e1) / args.steps
+
+    ms_pad = timed(step_padded)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ms = timed(step_varlen, sampler)
+    sampler.stop()
+    pairs = w.valid_pairs()
+    flops = 14.0 * w.d * pairs * w.Hq * w.layers
+    peaks = load_peaks()
+    value = flops / (ms * 1e-3) / 1e12
+    counts, _ = ne.ne_attn_varlen_plan(lens, w.T, w.Hq, w.Hkv, w.d, with_tables=False)
+    return {
+        "metric": "padded variable-length GQA attn fwd+bwd TFLOP/s (valid causal pairs) at "
+                  "T=512 12/4 heads",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) and lengths, see ne_inputs.py)",
+        "config": {"workload": w.name, "valid_tokens": int(sum(lens)),
+                   "padded_tokens": w.B * w.T, "valid_pair_fraction": pairs / (w.B * w.pairs),
+                   "live_units": counts,
+                   "path": "ne_attn_fwd_varlen + ne_attn_bwd_varlen, eager"},
+        "valid_tokens_per_s": sum(lens) * w.layers / (ms * 1e-3),
+        "padded_causal_ms_per_step": ms_pad,
+        "speedup_vs_padded": ms_pad / ms,
+        "pct_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
+        "gpu_launches": 6 * w.layers * args.steps,
+        "clocks": sampler.summary(),
+    }
+
+
 def run_one_layer_for_profiler():
     """One layer (B64 T512 12/4 d64, 270 MB of buffers), fwd then bwd, twice.
     The first pass warms up; a profiler captures the second (-s 4 -c 4)."""
@@ -642,7 +731,13 @@ def main():
     ap.add_argument("--window", type=int, default=0,
                     help="time the training step with a sliding window of this many keys "
                          "(the window entry points) instead; prints its own JSON line")
+    ap.add_argument("--varlen", action="store_true",
+                    help="time the padded variable-length SFT step (16 layers of B64 padded "
+                         "to 512, seeded lengths) instead; prints its own JSON line")
     args = ap.parse_args()
+    if args.varlen:
+        print(json.dumps(run_varlen(args)), flush=True)
+        return
     if args.window > 0:
         print(json.dumps(run_window(args)), flush=True)
         return

@@ -10,6 +10,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 from . import _build
@@ -25,7 +26,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn
             "ne_attn_set_wait_limit_ns", "ne_attn_selftest_timeout", "ne_attn_bwd_noalloc",
             "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save", "ne_attn_bwd_saved",
             "ne_attn_bwd_preprocess_d", "ne_attn_decode", "ne_attn_decode_workspace_size",
-            "ne_attn_fwd_window", "ne_attn_bwd_window")
+            "ne_attn_fwd_window", "ne_attn_bwd_window", "ne_attn_varlen_workspace_size",
+            "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan")
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +95,14 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_decode.restype = i
         lib.ne_attn_decode_workspace_size.argtypes = [i] * 5
         lib.ne_attn_decode_workspace_size.restype = sz
+        lib.ne_attn_varlen_workspace_size.argtypes = [i] * 5
+        lib.ne_attn_varlen_workspace_size.restype = sz
+        lib.ne_attn_fwd_varlen.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd_varlen.restype = i
+        lib.ne_attn_bwd_varlen.argtypes = [vp] * 11 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_varlen.restype = i
+        lib.ne_attn_varlen_plan.argtypes = [vp] + [i] * 5 + [vp] * 3 + [sz, vp]
+        lib.ne_attn_varlen_plan.restype = i
         _lib = lib
         return lib
 
@@ -398,6 +408,82 @@ def attention_decode(q, k_cache, v_cache, rope_theta: float = 10000.0, stream=No
                                 dtype=torch.uint8, device=q.device)
     ne_attn_decode(q, k_cache, v_cache, o, lse, workspace, rope_theta, stream)
     return o, lse
+
+
+def _host_seqlens(seqlens, B: int):
+    """seqlens as a contiguous host int32 array of B lengths (the library reads it
+    on the host during the call)."""
+    if isinstance(seqlens, torch.Tensor):
+        if seqlens.device.type != "cpu":
+            raise ValueError("seqlens must be in host memory (a list, array or CPU tensor)")
+        seqlens = seqlens.numpy()
+    sl = np.ascontiguousarray(np.asarray(seqlens).reshape(-1), dtype=np.int32)
+    if sl.shape != (B,):
+        raise ValueError(f"seqlens must hold {B} lengths, got {sl.shape[0]}")
+    return sl
+
+
+def ne_attn_varlen_workspace_size(B: int, T: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(load_library().ne_attn_varlen_workspace_size(B, T, Hq, Hkv, d))
+
+
+def ne_attn_varlen_plan(seqlens, T: int, Hq: int, Hkv: int, d: int, with_tables: bool = True):
+    """Host-only: the live work units of a padded variable-length batch.  Returns
+    (counts [fwd, dq, dkdv], [fwd table, dq table, dkdv table] or None)."""
+    sl = np.ascontiguousarray(np.asarray(seqlens).reshape(-1), dtype=np.int32)
+    B = int(sl.shape[0])
+    cap = ((T + 127) // 128) * B * Hq if with_tables else 0
+    tabs = [np.zeros(max(cap, 1), dtype=np.int32) for _ in range(3)]
+    counts = np.zeros(3, dtype=np.int32)
+    ptr = (lambda a: a.ctypes.data) if with_tables else (lambda a: None)
+    rc = load_library().ne_attn_varlen_plan(sl.ctypes.data, B, T, Hq, Hkv, d, ptr(tabs[0]),
+                                            ptr(tabs[1]), ptr(tabs[2]), cap, counts.ctypes.data)
+    if rc:
+        raise NeAttnError(rc, "ne_attn_varlen_plan")
+    if not with_tables:
+        return counts.tolist(), None
+    return counts.tolist(), [t[:c].copy() for t, c in zip(tabs, counts.tolist())]
+
+
+def ne_attn_fwd_varlen(q, k, v, o, lse, seqlens, workspace, rope_theta: float = 10000.0,
+                       stream=None) -> None:
+    """Padded variable-length forward: sequence b is its first seqlens[b] rows (host
+    lengths); padding rows get o = 0 and lse = -inf."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (B, T, Hq, d), bf)
+    _check(k, "k", (B, T, Hkv, d), bf)
+    _check(v, "v", (B, T, Hkv, d), bf)
+    _check(o, "o", (B, T, Hq, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    sl = _host_seqlens(seqlens, B)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           lse.data_ptr(), sl.ctypes.data, wp, wbytes, B, T, Hq,
+                                           Hkv, d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd_varlen")
+
+
+def ne_attn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, seqlens, workspace,
+                       rope_theta: float = 10000.0, stream=None) -> None:
+    """Padded variable-length backward (o, lse from ne_attn_fwd_varlen); padding
+    positions of dq, dk, dv get 0."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    sl = _host_seqlens(seqlens, B)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                           o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                           sl.ctypes.data, wp, wbytes, B, T, Hq, Hkv, d,
+                                           float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_varlen")
 
 
 def attention_forward(q, k, v, rope_theta: float = 10000.0, stream=None):

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libne_attn.so")
-SOURCES = ["ne_api.cu", "ne_fwd.cu", "ne_bwd.cu", "ne_decode.cu"]
+SOURCES = ["ne_api.cu", "ne_fwd.cu", "ne_bwd.cu", "ne_decode.cu", "ne_varlen.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", CSRC, "-I", INCLUDE] + ARCH

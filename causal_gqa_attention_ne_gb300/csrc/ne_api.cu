@@ -1,10 +1,12 @@
 // ne_api.cu -- the C ABI of include/ne_attn.h: argument validation, TMA
 // descriptor construction, launch sequencing and the device status word.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -624,6 +626,233 @@ int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream)
     cudaError_t e = ne::launch_timeout_selftest(status, limit_ns ? limit_ns : 1,
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // extern "C"
+
+// ------------------------------------------------------------------------
+// Padded variable-length batches.  Workspace: the unit tables [seqlen: int32
+// B][forward units][dq units][dk/dv units], each region 256-byte aligned and
+// sized for every unit of the padded shape, then (backward) the backward
+// workspace of ne_attn_bwd.
+namespace {
+
+struct VarlenLayout {
+    size_t off_fwd, off_dq, off_dkv, tables, total;
+};
+
+VarlenLayout varlen_layout(int B, int T, int Hq, int Hkv, int d)
+{
+    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const int G = Hq / Hkv;
+    const size_t tiles = static_cast<size_t>((T + 127) / 128) * B * Hkv;
+    const size_t nf = tiles * static_cast<size_t>(G / ne::fwd_heads_per_cta(d, G));
+    const size_t nq = tiles * static_cast<size_t>(G / ne::dq_heads_per_cta(d, G));
+    VarlenLayout L;
+    L.off_fwd = al(sizeof(int32_t) * static_cast<size_t>(B));
+    L.off_dq = L.off_fwd + al(sizeof(int32_t) * nf);
+    L.off_dkv = L.off_dq + al(sizeof(int32_t) * nq);
+    L.tables = L.off_dkv + al(sizeof(int32_t) * tiles);
+    L.total = L.tables + ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d);
+    return L;
+}
+
+int check_seqlens(const int32_t *seqlens, int B, int T)
+{
+    if (!seqlens)
+        return NE_ERR_NULL;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] < 0 || seqlens[b] > T)
+            return NE_ERR_ARG;
+    return NE_OK;
+}
+
+// The workspace's table region as the host builds it: the lengths, then each
+// table at its offset, filled up to its own region's capacity.
+int build_table_image(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
+                      const VarlenLayout &L, std::vector<int32_t> &img, int counts[3])
+{
+    const size_t w = sizeof(int32_t);
+    img.assign(L.tables / w, 0);
+    std::memcpy(img.data(), seqlens, w * static_cast<size_t>(B));
+    const size_t caps[3] = {(L.off_dq - L.off_fwd) / w, (L.off_dkv - L.off_dq) / w,
+                            (L.tables - L.off_dkv) / w};
+    ne::varlen_plan(seqlens, B, T, Hq, Hkv, d, img.data() + L.off_fwd / w,
+                    img.data() + L.off_dq / w, img.data() + L.off_dkv / w, caps, counts);
+    for (int i = 0; i < 3; ++i)
+        if (static_cast<size_t>(counts[i]) > caps[i])
+            return NE_ERR_ARG;   // cannot happen: every region holds all units of its kernel
+    return NE_OK;
+}
+
+// Builds the table image and copies it into the workspace on `st`.  The copy
+// is from pageable memory: it is staged before cudaMemcpyAsync returns, so
+// the host buffer may go away afterwards.
+int upload_tables(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
+                  const VarlenLayout &L, void *workspace, cudaStream_t st, int counts[3])
+{
+    std::vector<int32_t> img;
+    const int rc = build_table_image(seqlens, B, T, Hq, Hkv, d, L, img, counts);
+    if (rc != NE_OK)
+        return rc;
+    return cudaMemcpyAsync(workspace, img.data(), L.tables, cudaMemcpyHostToDevice, st) ==
+                   cudaSuccess
+               ? NE_OK
+               : NE_ERR_CUDA;
+}
+
+const int *ws_int(void *workspace, size_t off)
+{
+    return reinterpret_cast<const int *>(static_cast<uint8_t *>(workspace) + off);
+}
+
+} // namespace
+
+extern "C" {
+
+size_t ne_attn_varlen_workspace_size(int B, int T, int Hq, int Hkv, int d)
+{
+    if (check_shape(B, T, Hq, Hkv, d, 1.0f) != NE_OK)
+        return 0;
+    return varlen_layout(B, T, Hq, Hkv, d).total;
+}
+
+int ne_attn_varlen_plan(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
+                        int32_t *fwd_units, int32_t *dq_units, int32_t *dkv_units, size_t cap,
+                        int32_t *counts)
+{
+    if (!counts)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, 1.0f);
+    if (rc != NE_OK)
+        return rc;
+    if ((rc = check_seqlens(seqlens, B, T)) != NE_OK)
+        return rc;
+    // the very image the varlen entry points copy into the workspace
+    const VarlenLayout L = varlen_layout(B, T, Hq, Hkv, d);
+    std::vector<int32_t> img;
+    int c[3];
+    if ((rc = build_table_image(seqlens, B, T, Hq, Hkv, d, L, img, c)) != NE_OK)
+        return rc;
+    int32_t *out[3] = {fwd_units, dq_units, dkv_units};
+    const size_t off[3] = {L.off_fwd, L.off_dq, L.off_dkv};
+    for (int i = 0; i < 3; ++i) {
+        counts[i] = c[i];
+        if (out[i])
+            std::memcpy(out[i], img.data() + off[i] / sizeof(int32_t),
+                        sizeof(int32_t) * std::min(cap, static_cast<size_t>(c[i])));
+    }
+    return NE_OK;
+}
+
+int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    if (!q || !k || !v || !o || !lse || !workspace)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
+    if (rc != NE_OK)
+        return rc;
+    if ((rc = check_seqlens(seqlens, B, T)) != NE_OK)
+        return rc;
+    const VarlenLayout L = varlen_layout(B, T, Hq, Hkv, d);
+    if (workspace_bytes < L.tables)
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+        !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ne::AttnParams p = base_params(B, T, Hq, Hkv, d, rope_theta, status);
+    p.GC = ne::fwd_heads_per_cta(d, p.G);
+    p.nchunks = p.G / p.GC;
+    p.out0 = o;
+    p.lse = lse;
+    CUtensorMap mq, mk, mv, mo;
+    if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
+        make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
+        return NE_ERR_CUDA;
+    int counts[3];
+    if ((rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts)) != NE_OK)
+        return rc;
+    p.seqlen = ws_int(workspace, 0);
+    p.units = ws_int(workspace, L.off_fwd);
+    p.num_units = counts[0];
+    if (counts[0] > 0 && ne::launch_fwd(d, mq, mk, mv, mo, mq, mk, p, st) != cudaSuccess)
+        return NE_ERR_CUDA;
+    ne::PadFillParams f;
+    std::memset(&f, 0, sizeof(f));
+    f.x[0] = o;
+    f.row_bytes[0] = Hq * d * 2;
+    f.ntensors = 1;
+    f.lse = lse;
+    f.B = B;
+    f.T = T;
+    f.Hq = Hq;
+    f.seqlen = p.seqlen;
+    return ne::launch_pad_fill(f, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    if (!o || !dq || !dk || !dv || !workspace)
+        return NE_ERR_NULL;
+    int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
+    if (rc != NE_OK)
+        return rc;
+    if ((rc = check_seqlens(seqlens, B, T)) != NE_OK)
+        return rc;
+    const VarlenLayout L = varlen_layout(B, T, Hq, Hkv, d);
+    if (workspace_bytes < L.total)
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    void *bws = static_cast<uint8_t *>(workspace) + L.tables;
+    ne::AttnParams p;
+    CUtensorMap mq, mk, mv, mdo, mqr, mkr;
+    rc = bwd_setup(q, k, v, lse, dO, bws, workspace_bytes - L.tables, B, T, Hq, Hkv, d,
+                   rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
+    if (rc != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int counts[3];
+    if ((rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts)) != NE_OK)
+        return rc;
+    p.o_in = o;
+    void *qrot = static_cast<uint8_t *>(bws) + ws_d_bytes(B, T, Hq);
+    void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
+    if (ne::launch_bwd_pre(d, p, q, qrot, k, krot, st) != cudaSuccess)
+        return NE_ERR_CUDA;
+    p.seqlen = ws_int(workspace, 0);
+    p.units = ws_int(workspace, L.off_dq);
+    p.num_units = counts[1];
+    if (counts[1] > 0 && (rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
+        return rc;
+    p.units = ws_int(workspace, L.off_dkv);
+    p.num_units = counts[2];
+    if (counts[2] > 0 && (rc = run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st)) != NE_OK)
+        return rc;
+    ne::PadFillParams f;
+    std::memset(&f, 0, sizeof(f));
+    f.x[0] = dq;
+    f.x[1] = dk;
+    f.x[2] = dv;
+    f.row_bytes[0] = Hq * d * 2;
+    f.row_bytes[1] = Hkv * d * 2;
+    f.row_bytes[2] = Hkv * d * 2;
+    f.ntensors = 3;
+    f.B = B;
+    f.T = T;
+    f.Hq = Hq;
+    f.seqlen = p.seqlen;
+    return ne::launch_pad_fill(f, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
 } // extern "C"

@@ -351,10 +351,16 @@ struct DqCfg {
 
 struct DqUnit {
     int m, b, j, h0, lo;   // lo: first key tile (sliding window; 0 otherwise)
+    int tl;                // valid rows of sequence b (varlen; T otherwise)
 };
 
+// VAR: u indexes the launch's table of live units (padded variable-length
+// batches), which holds indices into the full enumeration below.
+template <bool VAR>
 __device__ __forceinline__ DqUnit dq_unit(int u, int GC, const AttnParams &p)
 {
+    if constexpr (VAR)
+        u = __ldg(p.units + u);
     DqUnit w;
     const int per_m = p.B * p.Hkv * p.nchunks;
     w.m = p.M - 1 - u / per_m;
@@ -365,11 +371,14 @@ __device__ __forceinline__ DqUnit dq_unit(int u, int GC, const AttnParams &p)
     w.b = rem / p.Hkv;
     w.h0 = w.j * p.G + chunk * GC;
     w.lo = key_tile_lo(w.m, p.window);
+    w.tl = VAR ? __ldg(p.seqlen + w.b) : p.T;
     return w;
 }
 
-// WIN: a sliding window may mask keys off the diagonal tile.
-template <int D, int GC, int ST, bool WIN>
+// WIN: a sliding window may mask keys off the diagonal tile.  VAR: padded
+// variable-length batch; rows past their sequence's length get lse = +inf
+// (P = 0, dS = 0), and their dq is overwritten afterwards by the padding fill.
+template <int D, int GC, int ST, bool WIN, bool VAR>
 __global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
                     break;
-                const DqUnit w = dq_unit(u, GC, p);
+                const DqUnit w = dq_unit<VAR>(u, GC, p);
                 for (int g = 0; g < GC && ok; ++g) {
                     if (k >= 1 && !mbar_wait(smem_u32(&bar_q_empty[g]), (k - 1) & 1, wc)) {
                         ok = false;
@@ -509,7 +518,7 @@ __global__ void __launch_bounds__(384, 1)
                     const int u = snake_unit(k, cta, P);
                     if (u >= p.num_units)
                         break;
-                    const DqUnit w = dq_unit(u, GC, p);
+                    const DqUnit w = dq_unit<VAR>(u, GC, p);
                     const int nitems = (w.m - w.lo + 1) * GC;
                     for (int it = 0; it < nitems; ++it, ++gi) {
                         const int jk = w.lo + it / GC, g = it % GC;
@@ -547,7 +556,7 @@ __global__ void __launch_bounds__(384, 1)
                     const int u = snake_unit(k, cta, P);
                     if (u >= p.num_units)
                         break;
-                    const DqUnit w = dq_unit(u, GC, p);
+                    const DqUnit w = dq_unit<VAR>(u, GC, p);
                     const int nitems = (w.m - w.lo + 1) * GC;
                     for (int it = 0; it < nitems; ++it, ++gi) {
                         const int jk = w.lo + it / GC, g = it % GC;
@@ -608,15 +617,19 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (u >= p.num_units)
             return;
-        const DqUnit un = dq_unit(u, GC, p);
+        const DqUnit un = dq_unit<VAR>(u, GC, p);
         const int t = un.m * kRows + r;
-        if (t < p.T) {
+        if (t < (VAR ? un.tl : p.T)) {
 #pragma unroll
             for (int g = 0; g < GC; ++g) {
                 const size_t idx = (static_cast<size_t>(un.b) * p.Hq + un.h0 + g) * p.T + t;
                 l2[g] = p.lse[idx] * kLog2e;
                 dd[g] = p.Dws[idx];
             }
+        } else if constexpr (VAR) {
+#pragma unroll
+            for (int g = 0; g < GC; ++g)
+                l2[g] = INFINITY;
         }
     };
     // A unit's epilogue (dq out of TMEM) runs after the next unit's first
@@ -690,7 +703,7 @@ __global__ void __launch_bounds__(384, 1)
         const int u = snake_unit(k, cta, P);
         if (u >= p.num_units)
             break;
-        const DqUnit un = dq_unit(u, GC, p);
+        const DqUnit un = dq_unit<VAR>(u, GC, p);
         float l2[GC], dd[GC];
 #pragma unroll
         for (int g = 0; g < GC; ++g) {
@@ -849,22 +862,33 @@ struct DkvCfg {
 
 struct DkvUnit {
     int n, b, j, nitems;
+    int tl;                // valid rows of sequence b (varlen; T otherwise)
 };
 
+// VAR: u indexes the launch's table of live units (padded variable-length
+// batches); a unit's query tiles then end at its sequence's last tile.
+template <bool VAR>
 __device__ __forceinline__ DkvUnit dkv_unit(int u, const AttnParams &p)
 {
+    if constexpr (VAR)
+        u = __ldg(p.units + u);
     DkvUnit w;
     const int per_n = p.B * p.Hkv;
     w.n = u / per_n;
     const int rem = u % per_n;
     w.j = rem % p.Hkv;
     w.b = rem / p.Hkv;
-    w.nitems = (query_tile_hi(w.n, p.window, p.M) - w.n + 1) * p.G;
+    w.tl = VAR ? __ldg(p.seqlen + w.b) : p.T;
+    const int mtiles = VAR ? (w.tl + kRows - 1) / kRows : p.M;
+    w.nitems = (query_tile_hi(w.n, p.window, mtiles) - w.n + 1) * p.G;
     return w;
 }
 
-// WIN: a sliding window may mask queries off the diagonal tile.
-template <int D, int ST, bool WIN>
+// WIN: a sliding window may mask queries off the diagonal tile.  VAR: padded
+// variable-length batch; query rows past their sequence's length get
+// lse = +inf and D = 0 (P = 0, dS = 0), like rows past T, and the dk/dv rows
+// of padding keys are overwritten afterwards by the padding fill.
+template <int D, int ST, bool WIN, bool VAR>
 __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -957,7 +981,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
                     break;
-                const DkvUnit w = dkv_unit(u, p);
+                const DkvUnit w = dkv_unit<VAR>(u, p);
                 const int kb = k % KB, ku = k / KB;
                 if (ku >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[kb]), (ku - 1) & 1, wc)) {
                     ok = false;
@@ -1034,7 +1058,7 @@ __global__ void __launch_bounds__(512, 1)
                     const int u = snake_unit(k, cta, P);
                     if (u >= p.num_units)
                         break;
-                    const DkvUnit w = dkv_unit(u, p);
+                    const DkvUnit w = dkv_unit<VAR>(u, p);
                     const int kb = k % KB, ku = k / KB;
                     if (!(mbar_wait_warp(smem_u32(&bar_k_full[kb]), ku & 1, wc) &&
                           mbar_wait_warp(smem_u32(&bar_v_full[kb]), ku & 1, wc))) {
@@ -1085,7 +1109,7 @@ __global__ void __launch_bounds__(512, 1)
                     const int u = snake_unit(k, cta, P);
                     if (u >= p.num_units)
                         break;
-                    const DkvUnit w = dkv_unit(u, p);
+                    const DkvUnit w = dkv_unit<VAR>(u, p);
                     const int kb = k % KB;
                     for (int it = 0; it < w.nitems; ++it, ++gi) {
                         const int st = gi % ST;
@@ -1145,7 +1169,7 @@ __global__ void __launch_bounds__(512, 1)
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
                 break;
-            const DkvUnit w = dkv_unit(u, p);
+            const DkvUnit w = dkv_unit<VAR>(u, p);
             // lse and D of the item's queries are fetched one item ahead so the
             // global-load latency overlaps the wait for the previous item.
             auto fetch = [&](int it, float &l, float &dd) {
@@ -1153,7 +1177,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int t = mt * kRows + r;
                 l = INFINITY;
                 dd = 0.f;
-                if (t < p.T) {
+                if (t < (VAR ? w.tl : p.T)) {
                     const size_t idx = (static_cast<size_t>(w.b) * p.Hq + h) * p.T + t;
                     l = p.lse[idx];
                     dd = p.Dws[idx];
@@ -1236,7 +1260,7 @@ __global__ void __launch_bounds__(512, 1)
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
                 break;
-            const DkvUnit un = dkv_unit(u, p);
+            const DkvUnit un = dkv_unit<VAR>(u, p);
             for (int it = 0; it < un.nitems; ++it, ++gi) {
                 const int st = gi % ST, su = gi / ST;
                 const int mt = un.n + it / p.G;
@@ -1334,13 +1358,13 @@ __global__ void __launch_bounds__(512, 1)
 
 // ------------------------------------------------------------- launch ---
 
-template <int D, int GC, int ST, bool WIN>
+template <int D, int GC, int ST, bool WIN, bool VAR>
 static cudaError_t launch_dq_w(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                const CUtensorMap &dO, const CUtensorMap &dq,
                                const AttnParams &p0, cudaStream_t stream)
 {
     using C = DqCfg<D, GC, ST>;
-    auto kern = dq_kernel<D, GC, ST, WIN>;
+    auto kern = dq_kernel<D, GC, ST, WIN, VAR>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
@@ -1350,7 +1374,8 @@ static cudaError_t launch_dq_w(const CUtensorMap &q, const CUtensorMap &k, const
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
     AttnParams p = p0;
-    p.num_units = p.M * p.B * p.Hkv * p.nchunks;
+    if (!VAR)
+        p.num_units = p.M * p.B * p.Hkv * p.nchunks;   // varlen: the table's length
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
     return launch_pdl(kern, grid, 384, C::SMEM_BYTES, stream, q, k, v, dO, dq, p);
 }
@@ -1361,8 +1386,10 @@ static cudaError_t launch_dq_t(const CUtensorMap &q, const CUtensorMap &k, const
                                cudaStream_t stream)
 {
     if (p.window > 0)
-        return launch_dq_w<D, GC, ST, true>(q, k, v, dO, dq, p, stream);
-    return launch_dq_w<D, GC, ST, false>(q, k, v, dO, dq, p, stream);
+        return launch_dq_w<D, GC, ST, true, false>(q, k, v, dO, dq, p, stream);
+    if (p.units)
+        return launch_dq_w<D, GC, ST, false, true>(q, k, v, dO, dq, p, stream);
+    return launch_dq_w<D, GC, ST, false, false>(q, k, v, dO, dq, p, stream);
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
@@ -1396,12 +1423,12 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, con
     return cudaErrorInvalidValue;
 }
 
-template <int D, int ST, bool WIN>
+template <int D, int ST, bool WIN, bool VAR>
 static cudaError_t launch_dkdv_w(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                  const CUtensorMap &dO, const AttnParams &p0, cudaStream_t stream)
 {
     using C = DkvCfg<D, ST>;
-    auto kern = dkdv_kernel<D, ST, WIN>;
+    auto kern = dkdv_kernel<D, ST, WIN, VAR>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
@@ -1411,7 +1438,8 @@ static cudaError_t launch_dkdv_w(const CUtensorMap &q, const CUtensorMap &k, con
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
     AttnParams p = p0;
-    p.num_units = p.M * p.B * p.Hkv;
+    if (!VAR)
+        p.num_units = p.M * p.B * p.Hkv;   // varlen: the table's length
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
     return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, dO, p);
 }
@@ -1421,8 +1449,10 @@ static cudaError_t launch_dkdv_t(const CUtensorMap &q, const CUtensorMap &k, con
                                  const CUtensorMap &dO, const AttnParams &p, cudaStream_t stream)
 {
     if (p.window > 0)
-        return launch_dkdv_w<D, ST, true>(q, k, v, dO, p, stream);
-    return launch_dkdv_w<D, ST, false>(q, k, v, dO, p, stream);
+        return launch_dkdv_w<D, ST, true, false>(q, k, v, dO, p, stream);
+    if (p.units)
+        return launch_dkdv_w<D, ST, false, true>(q, k, v, dO, p, stream);
+    return launch_dkdv_w<D, ST, false, false>(q, k, v, dO, p, stream);
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap &q, const CUtensorMap &k,

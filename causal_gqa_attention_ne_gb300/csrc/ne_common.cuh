@@ -378,6 +378,11 @@ struct AttnParams {
     uint64_t wait_limit_ns;
     int save_rot;                // forward: also store Q' and K' (fp16) for the backward
     int window;                  // 0: causal; W > 0: query t sees keys t-W+1 .. t
+    // padded variable-length batches (varlen instantiations only): the live
+    // work units of the launch (indices into the full enumeration, num_units
+    // of them) and the valid length of every sequence, both in device memory
+    const int *units;
+    const int *seqlen;
     RopeFreqs rope;
 };
 

@@ -95,8 +95,13 @@ struct FwdUnit {
     int m, b, j, h0, lo;   // lo: first key tile (sliding window; 0 otherwise)
 };
 
+// VAR: u indexes the launch's table of live units (padded variable-length
+// batches), which holds indices into the full enumeration below.
+template <bool VAR>
 __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
 {
+    if constexpr (VAR)
+        u = __ldg(p.units + u);
     FwdUnit w;
     const int per_m = p.B * p.Hkv * p.nchunks;
     w.m = p.M - 1 - u / per_m;
@@ -111,8 +116,11 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
 }
 
 // WIN: a sliding window may mask keys off the diagonal tile (compiled out of
-// the causal instantiations).
-template <int D, int GC, int ST, bool WIN>
+// the causal instantiations).  VAR: padded variable-length batch, the units
+// come from a table that leaves out every query tile past its sequence's
+// length; rows of a live tile past that length are computed like any other
+// (over the padding keys) and overwritten afterwards by the padding fill.
+template <int D, int GC, int ST, bool WIN, bool VAR>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -223,7 +231,7 @@ __global__ void __launch_bounds__(512, 1)
             // Q' tiles of unit kk into set kk % QB, once the set's previous
             // unit has issued its last S
             auto load_q = [&](int kk) {
-                const FwdUnit w = fwd_unit(snake_unit(kk, cta, P), GC, p);
+                const FwdUnit w = fwd_unit<VAR>(snake_unit(kk, cta, P), GC, p);
                 const int qb = kk % QB, use = kk / QB;
                 for (int g = 0; g < GC; ++g) {
                     if (use >= 1 && !mbar_wait_warp(smem_u32(&bar_q_empty[qb][g]), (use - 1) & 1, wc))
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
                     break;
-                const FwdUnit w = fwd_unit(u, GC, p);
+                const FwdUnit w = fwd_unit<VAR>(u, GC, p);
                 // order: [Q of this unit if not prefetched], K/V lo, [Q of the
                 // next unit], K/V lo+1..m
                 if (QB == 1 || k == 0)
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
                     break;
-                const FwdUnit w = fwd_unit(u, GC, p);
+                const FwdUnit w = fwd_unit<VAR>(u, GC, p);
                 const int nq0 = (QB == 1 || k == 0) ? GC : 0;
                 const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
                 const int nq1 = has_next ? GC : 0;
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(512, 1)
                                                       : C::OFF_K + st * TL::BYTES);
                     if (lane == 0) {
                         const FwdUnit wq =
-                            isq && qunit != k ? fwd_unit(snake_unit(qunit, cta, P), GC, p) : w;
+                            isq && qunit != k ? fwd_unit<VAR>(snake_unit(qunit, cta, P), GC, p) : w;
                         for (int cb = 0; cb < TL::NB; ++cb) {
                             const uint32_t src = smem_u32(tile + cb * TL::BLOCK);
                             if (isq)
@@ -416,7 +424,7 @@ __global__ void __launch_bounds__(512, 1)
                 const int u = snake_unit(k, cta, P);
                 if (u >= p.num_units)
                     break;
-                const FwdUnit w = fwd_unit(u, GC, p);
+                const FwdUnit w = fwd_unit<VAR>(u, GC, p);
                 const int qb = k % QB;
                 for (int jk = w.lo; jk <= w.m && ok; ++jk, ++kt) {
                     const int st = kt % ST;
@@ -486,14 +494,14 @@ __global__ void __launch_bounds__(512, 1)
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
                 break;
-            const FwdUnit w = fwd_unit(u, GC, p);
+            const FwdUnit w = fwd_unit<VAR>(u, GC, p);
             // Tiles in the order the producer loads them: [Q of this unit
             // unless prefetched], K 0, [Q of the next unit], K 1..m.  One call
             // site keeps the unrolled rotation in the instruction cache once.
             const int nq0 = (QB == 1 || k == 0) ? GC : 0;
             const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
             const int nq1 = has_next ? GC : 0;
-            const int mnext = has_next ? fwd_unit(snake_unit(k + 1, cta, P), GC, p).m : 0;
+            const int mnext = has_next ? fwd_unit<VAR>(snake_unit(k + 1, cta, P), GC, p).m : 0;
             for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
                 const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
                 const int qunit = t < nq0 ? k : k + 1;
@@ -638,7 +646,7 @@ __global__ void __launch_bounds__(512, 1)
         const int u = snake_unit(k, cta, P);
         if (u >= p.num_units)
             break;
-        const FwdUnit un = fwd_unit(u, GC, p);
+        const FwdUnit un = fwd_unit<VAR>(u, GC, p);
         for (int jk = un.lo; jk <= un.m && ok; ++jk) {
             for (int pi = 0; pi < GC; ++pi, ++n) {
                 const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
@@ -858,13 +866,13 @@ __global__ void __launch_bounds__(512, 1)
 }
 // ------------------------------------------------------------- launch ---
 
-template <int D, int GC, int ST, bool WIN>
+template <int D, int GC, int ST, bool WIN, bool VAR>
 static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                 const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
                                 const AttnParams &p0, cudaStream_t stream)
 {
     using C = FwdCfg<D, GC, ST>;
-    auto kern = fwd_kernel<D, GC, ST, WIN>;
+    auto kern = fwd_kernel<D, GC, ST, WIN, VAR>;
     static bool attr_done[64] = {};   // one flag set per template instantiation
     cudaError_t e = ensure_smem_attr(kern, C::SMEM_BYTES, attr_done);
     if (e != cudaSuccess)
@@ -874,7 +882,8 @@ static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, cons
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
     AttnParams p = p0;
-    p.num_units = p.M * p.B * p.Hkv * p.nchunks;
+    if (!VAR)
+        p.num_units = p.M * p.B * p.Hkv * p.nchunks;   // varlen: the table's length
     const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
     return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, o, qs, ks, p);
 }
@@ -885,8 +894,10 @@ static cudaError_t launch_fwd_p(const CUtensorMap &q, const CUtensorMap &k, cons
                                 const AttnParams &p, cudaStream_t stream)
 {
     if (p.window > 0)
-        return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, true>(q, k, v, o, qs, ks, p, stream);
-    return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, false>(q, k, v, o, qs, ks, p, stream);
+        return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, true, false>(q, k, v, o, qs, ks, p, stream);
+    if (p.units)
+        return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, false, true>(q, k, v, o, qs, ks, p, stream);
+    return launch_fwd_t<D, GC, FwdPlan<D, GC>::ST, false, false>(q, k, v, o, qs, ks, p, stream);
 }
 
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

@@ -54,6 +54,27 @@ struct DecodeParams {
 cudaError_t launch_decode(int d, const DecodeParams &p, cudaStream_t stream);
 int decode_chunk_keys();
 
+// Padded variable-length batches.  varlen_plan lists the live work units of
+// the forward, dq and dk/dv kernels for per-sequence lengths seqlen[B] (host
+// array, 0 <= seqlen[b] <= T) as indices into each kernel's full unit
+// enumeration, writing at most caps[i] entries into table i (a null table is
+// only counted) and the three counts; the kernels take a table through
+// AttnParams::units with num_units = its count.  launch_pad_fill writes the
+// padding rows t >= seqlen[b]: zero in up to three [B][T][row_bytes] tensors
+// (row_bytes a multiple of 16, 16-byte aligned bases) and -inf in lse
+// [B][Hq][T] when lse is not null.  seqlen is a device array there.
+struct PadFillParams {
+    void *x[3];
+    int row_bytes[3];
+    int ntensors;
+    float *lse;
+    int B, T, Hq;
+    const int *seqlen;
+};
+int varlen_plan(const int *seqlen, int B, int T, int Hq, int Hkv, int d, int *fwd_units,
+                int *dq_units, int *dkv_units, const size_t caps[3], int counts[3]);
+cudaError_t launch_pad_fill(const PadFillParams &p, cudaStream_t stream);
+
 // One-block kernel whose wait can never complete (checks the timeout path).
 cudaError_t launch_timeout_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream);
 

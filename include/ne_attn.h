@@ -206,6 +206,56 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
                    float rope_theta, void *stream);
 
 /*
+ * Padded variable-length batches (the NanoEuler SFT stage pads each
+ * instruction/response pair to the context and masks the loss on prompt and
+ * padding: walkthrough section 3.2).  Sequence b holds its first
+ * seqlens[b] tokens, 0 <= seqlens[b] <= T, at positions 0 .. seqlens[b]-1;
+ * the rows after them are padding.  Each sequence is its own causal problem,
+ * so its valid rows equal the same rows of ne_attn_fwd on the padded batch;
+ * a padding row attends to nothing.
+ *   seqlens    int32 [B], HOST memory, read during the call only
+ *   workspace  caller-owned device memory (16-byte aligned, no initial
+ *              contents) of at least ne_attn_varlen_workspace_size() bytes;
+ *              the forward uses only its first part (the work-unit tables)
+ * ne_attn_fwd_varlen writes o and lse like ne_attn_fwd on valid rows, and
+ * o = 0, lse = -inf on padding rows.  ne_attn_bwd_varlen takes o and lse
+ * from ne_attn_fwd_varlen and writes the gradients of the sum of O * dO over
+ * the valid rows: dq, dk, dv like ne_attn_bwd on valid positions (dO of
+ * padding rows is never used) and 0 on padding positions.
+ * Padding rows of q, k, v and dO must hold finite values (zeros, or a pad
+ * token's embedding): tiles that straddle a sequence's end compute over them
+ * before the padding is overwritten.  Work is proportional to the valid
+ * rows: query tiles (and, in the backward, key tiles) wholly past a
+ * sequence's end are skipped.  The library builds the tables of live work
+ * units on the host and copies them into the workspace with an asynchronous
+ * copy from pageable memory, so these calls cannot be captured into a CUDA
+ * graph; calls that share a workspace must not overlap on the GPU.
+ * Errors as for ne_attn_fwd / ne_attn_bwd; seqlens NULL gives NE_ERR_NULL, a
+ * length outside [0, T] NE_ERR_ARG.  ne_attn_varlen_workspace_size returns 0
+ * for an invalid shape.
+ */
+size_t ne_attn_varlen_workspace_size(int B, int T, int Hq, int Hkv, int d);
+int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+
+/*
+ * The work units a padded variable-length batch launches (host only; no GPU
+ * needed): per-sequence lengths seqlens[B] (host) give counts[0..2], the
+ * live units of the forward, dq and dk/dv kernels, and each non-NULL table
+ * receives up to `cap` of them as indices into that kernel's full unit
+ * enumeration, in launch order.  Returns NE_OK, or the error
+ * ne_attn_fwd_varlen would return for these arguments.
+ */
+int ne_attn_varlen_plan(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
+                        int32_t *fwd_units, int32_t *dq_units, int32_t *dkv_units, size_t cap,
+                        int32_t *counts);
+
+/*
  * Synchronises `stream`, then returns and clears the device-side status of
  * the current device: NE_ERR_TIMEOUT or NE_ERR_RANGE if a kernel recorded
  * one since the last call, NE_ERR_CUDA if the stream reports a CUDA error,

@@ -17,6 +17,12 @@ stress shape, ``torch.randint`` on the same generator then draws one position
 per (tensor, batch, head) for q, k and v, and that row is multiplied by 8.
 Finally every tensor is rounded to bfloat16.  Multi-layer workloads use seed
 ``seed + layer`` for layer ``layer``.
+
+Padded variable-length (SFT) workloads also draw one length per sequence
+from a second CPU generator seeded with ``seed``: integers uniform on
+[16, T], the same for every layer of the step.  The pages give no length
+mix for their instruction data (pairs padded to the context); a uniform mix
+keeps about half of the padded work and spans every tile count.
 """
 from __future__ import annotations
 
@@ -40,6 +46,7 @@ class Workload:
     outlier_rows: bool = False
     layers: int = 1
     theta: float = ROPE_THETA
+    varlen: bool = False
 
     @property
     def G(self) -> int:
@@ -61,6 +68,17 @@ class Workload:
     def tokens(self) -> int:
         return self.B * self.T
 
+    def seqlens(self) -> list[int]:
+        """Per-sequence valid lengths of a padded variable-length workload."""
+        if not self.varlen:
+            return [self.T] * self.B
+        g = torch.Generator(device="cpu").manual_seed(self.seed)
+        return torch.randint(16, self.T + 1, (self.B,), generator=g).tolist()
+
+    def valid_pairs(self) -> int:
+        """Causal (t, s) pairs summed over the sequences' valid rows."""
+        return sum(L * (L + 1) // 2 for L in self.seqlens())
+
 
 WORKLOADS = {
     w.name: w
@@ -80,6 +98,10 @@ WORKLOADS = {
         # with their own caches.
         Workload("gpt116m_decode_16x_b64_tk512_h12x4_d64", B=64, T=512, Hq=12, Hkv=4, d=64,
                  seed=1006, layers=16),
+        # NanoEuler 116M SFT step: 16 layers of B=64 sequences padded to 512,
+        # each with its own valid length.
+        Workload("gpt116m_sft_16x_b64_t512_h12x4_d64", B=64, T=512, Hq=12, Hkv=4, d=64,
+                 seed=1007, layers=16, varlen=True),
         # Long-context stress shape with one 8x row per (tensor, batch, head).
         Workload("stress_b4_t4096_h16x4_d128", B=4, T=4096, Hq=16, Hkv=4, d=128, seed=1005,
                  outlier_rows=True),
@@ -92,6 +114,7 @@ LAYER_116M = WORKLOADS["gpt116m_b16_t512_h12x4_d64"]
 STEP_116M = WORKLOADS["gpt116m_step_16x_b64_t512_h12x4_d64"]
 STRESS = WORKLOADS["stress_b4_t4096_h16x4_d128"]
 DECODE_116M = WORKLOADS["gpt116m_decode_16x_b64_tk512_h12x4_d64"]
+SFT_116M = WORKLOADS["gpt116m_sft_16x_b64_t512_h12x4_d64"]
 
 
 def make_inputs(w: Workload, layer: int = 0) -> dict[str, torch.Tensor]:
