@@ -222,9 +222,10 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
  * from ne_attn_fwd_varlen and writes the gradients of the sum of O * dO over
  * the valid rows: dq, dk, dv like ne_attn_bwd on valid positions (dO of
  * padding rows is never used) and 0 on padding positions.
- * Padding rows of q, k, v and dO must hold finite values (zeros, or a pad
- * token's embedding): tiles that straddle a sequence's end compute over them
- * before the padding is overwritten.  Work is proportional to the valid
+ * Padding rows of q, k, v and dO must hold values the other entry points
+ * accept (finite, within the fp16 range after rotation; zeros or a pad
+ * token's activations do): tiles that straddle a sequence's end compute over
+ * them, with zero weight, before the padding is overwritten.  Work is proportional to the valid
  * rows: query tiles (and, in the backward, key tiles) wholly past a
  * sequence's end are skipped.  The library builds the tables of live work
  * units on the host and copies them into the workspace with an asynchronous
