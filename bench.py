@@ -196,6 +196,23 @@ def make_event(torch, external):
     return torch.cuda.Event(enable_timing=True)
 
 
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The slowest rank's time: every rank passes its own, every rank gets the max
+    (one all-reduce; a no-op for a single process)."""
+    if world <= 1:
+        return ms
+    import torch
+    tt = torch.tensor([ms], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(world: int, units_per_step: float, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: the units all ranks processed
+    over the slowest rank's time."""
+    return world * units_per_step * steps / (elapsed_ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -310,14 +327,10 @@ def run_ours(args, rank, world, local_rank):
                 per[n].append(le[i].elapsed_time(le[i + 1]))
     avg_ms = {n: statistics.mean(v) for n, v in per.items()}
 
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-
+    elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     ms_per_step = elapsed_ms / K
-    value = world * FLOP_PER_STEP * K / (elapsed_ms * 1e-3) / 1e12
-    tokens_per_s = world * TOKENS_PER_STEP * K / (elapsed_ms * 1e-3)
+    value = job_rate(world, FLOP_PER_STEP, K, elapsed_ms) / 1e12
+    tokens_per_s = job_rate(world, TOKENS_PER_STEP, K, elapsed_ms)
 
     # end to end: host buffers in, host buffers out, through the eager C-ABI calls
     e2e_steps = max(1, min(args.e2e_steps, K))
@@ -345,11 +358,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     host_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps
-    e2e_ms = max(e2e_ms, host_ms)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(max(e2e_ms, host_ms), dev, world)
     st = ne.ne_attn_get_error()
     if st != 0:
         raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)} after e2e")
@@ -388,7 +397,7 @@ def run_ours(args, rank, world, local_rank):
         "config": CONFIG,
         "tokens_per_s": tokens_per_s,
         "pct_bf16_peak": value / (peaks["bf16_tflops"] * world) * 100.0,
-        "e2e": {"value": world * FLOP_PER_STEP / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_rate(world, FLOP_PER_STEP, 1, e2e_ms) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
         "gpu_launches": 4 * W.layers * K,
