@@ -4,6 +4,7 @@ so the only cross-rank steps are the barriers around the timed region and
 the max over ranks of the elapsed time.  Two gloo ranks check that every
 rank gets the slowest rank's time and that the whole-job rate counts the
 units of all ranks over that time.  CPU only."""
+import json
 import os
 import socket
 
@@ -21,7 +22,7 @@ def _free_port() -> int:
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, out):
+def _rank_main(rank, world, port, outdir):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -29,19 +30,17 @@ def _rank_main(rank, world, port, out):
         dist.barrier()
         slowest = bench.max_over_ranks(mine, torch.device("cpu"), world)
         rate = bench.job_rate(world, 1000.0, 4, slowest)
-        out[rank] = (mine, slowest, rate)
+        with open(os.path.join(outdir, f"rank{rank}.json"), "w") as f:
+            json.dump([mine, slowest, rate], f)
         dist.barrier()
     finally:
         dist.destroy_process_group()
 
 
-def test_two_replicas_report_the_slowest_rank():
+def test_two_replicas_report_the_slowest_rank(tmp_path):
     world = 2
-    with mp.Manager() as m:
-        out = m.dict()
-        mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
-        res = dict(out)
-    assert sorted(res) == [0, 1]
+    mp.spawn(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    res = {r: json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)}
     for rank, (mine, slowest, rate) in res.items():
         assert mine == 10.0 * (rank + 1) + 0.25
         assert slowest == 20.25                    # every rank sees the max
