@@ -249,8 +249,10 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
  * needed): per-sequence lengths seqlens[B] (host) give counts[0..2], the
  * live units of the forward, dq and dk/dv kernels, and each non-NULL table
  * receives up to `cap` of them as indices into that kernel's full unit
- * enumeration, in launch order.  Returns NE_OK, or the error
- * ne_attn_fwd_varlen would return for these arguments.
+ * enumeration, in launch order (each table is the one the varlen entry
+ * points copy into the workspace).  Returns NE_OK; NE_ERR_NULL if seqlens or
+ * counts is NULL; NE_ERR_SHAPE / NE_ERR_UNSUPPORTED for a shape
+ * ne_attn_fwd_varlen rejects; NE_ERR_ARG for a length outside [0, T].
  */
 int ne_attn_varlen_plan(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
                         int32_t *fwd_units, int32_t *dq_units, int32_t *dkv_units, size_t cap,

@@ -122,5 +122,7 @@ def test_argument_errors():
     assert lib.ne_attn_varlen_plan(bad, 2, 8, 2, 2, 64, None, None, None, 0, counts) == 9
     assert lib.ne_attn_varlen_plan(ok, 2, 8, 3, 2, 64, None, None, None, 0, counts) == 2
     assert lib.ne_attn_varlen_plan(ok, 2, 8, 2, 2, 64, None, None, None, 0, None) == 1
+    assert lib.ne_attn_varlen_plan(None, 2, 8, 2, 2, 64, None, None, None, 0, counts) == 1
+    assert lib.ne_attn_varlen_plan(ok, 2, 8, 2, 2, 48, None, None, None, 0, counts) == 3
     assert lib.ne_attn_varlen_plan(ok, 2, 8, 2, 2, 64, None, None, None, 0, counts) == 0
     assert list(counts) == [4, 4, 4]      # 2 sequences x 1 tile x 2 kv heads (G = 1)
