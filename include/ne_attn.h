@@ -42,6 +42,11 @@
  * backward's dS) go through the tensor cores as fp16, so elements of q and k,
  * and of dS = P (dP - D), must stay below 65504 in magnitude; a kernel that
  * sees a larger value records NE_ERR_RANGE in the status word.
+ * RoPE angles are evaluated from each frequency rounded to a 32-bit
+ * fixed-point fraction of a turn, times the position (exact modulo one
+ * turn).  The angle error is at most 2 pi * pos * 2^-33 radians:
+ * 3e-6 at position 4096, 8e-4 at 2^20 and 1.2e-2 at 2^24.  The tolerances
+ * above are verified up to T = 4096.
  *
  * Errors.  Argument errors are returned synchronously and launch nothing.
  * Launch failures return NE_ERR_CUDA.  Device-side errors (a bounded wait
