@@ -67,6 +67,12 @@ def _bind(path: str):
     lib.ne_oracle_bwd_varlen.restype = ctypes.c_int
     lib.ne_oracle_bwd_varlen.argtypes = [_DP] * 7 + [_IP] + [ctypes.c_int] * 5 + [
         ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_fwd_packed.restype = ctypes.c_int
+    lib.ne_oracle_fwd_packed.argtypes = [_DP] * 5 + [_IP] + [ctypes.c_int] * 4 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
+    lib.ne_oracle_bwd_packed.restype = ctypes.c_int
+    lib.ne_oracle_bwd_packed.argtypes = [_DP] * 7 + [_IP] + [ctypes.c_int] * 4 + [
+        ctypes.c_double, ctypes.c_long, ctypes.c_int]
     lib.ne_oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -204,6 +210,51 @@ class Oracle:
         return {"dq": dq, "dk": dk, "dv": dv}
 
 
+    def _cu(self, cu_seqlens, total: int):
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens).reshape(-1), dtype=np.intc)
+        if cu.shape[0] < 2 or cu[0] != 0 or cu[-1] != total or (np.diff(cu) < 0).any():
+            raise ValueError("cu_seqlens must start at 0, not decrease and end at the pack length")
+        return cu
+
+    def attn_fwd_packed(self, q, k, v, cu_seqlens, theta: float, pos_offset: int = 0,
+                        threads: int = 0):
+        """Packed variable-length batch: q [total, Hq, d], k and v [total, Hkv, d];
+        sequence b is tokens cu_seqlens[b] .. cu_seqlens[b+1]-1, a causal problem
+        of its own (positions restart at 0).  Returns (o [total,Hq,d], lse [Hq,total])."""
+        q, k, v = _c(q), _c(k), _c(v)
+        total, Hq, d = q.shape
+        Hkv = k.shape[1]
+        if k.shape != (total, Hkv, d) or v.shape != k.shape:
+            raise ValueError("k and v must be [total, Hkv, d] matching q")
+        cu = self._cu(cu_seqlens, total)
+        o = np.zeros_like(q)
+        lse = np.full((Hq, total), -np.inf)
+        rc = self._lib.ne_oracle_fwd_packed(
+            _p(q), _p(k), _p(v), _p(o), _p(lse), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+            cu.shape[0] - 1, Hq, Hkv, d, float(theta), int(pos_offset), int(threads))
+        if rc:
+            raise ValueError(f"ne_oracle_fwd_packed failed with code {rc}")
+        return o, lse
+
+    def attn_bwd_packed(self, q, k, v, do, cu_seqlens, theta: float, pos_offset: int = 0,
+                        threads: int = 0):
+        """Gradients of sum(O * dO) for a packed batch.  Dict with dq, dk, dv."""
+        q, k, v, do = _c(q), _c(k), _c(v), _c(do)
+        total, Hq, d = q.shape
+        Hkv = k.shape[1]
+        if do.shape != q.shape or k.shape != (total, Hkv, d) or v.shape != k.shape:
+            raise ValueError("shape mismatch")
+        cu = self._cu(cu_seqlens, total)
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        rc = self._lib.ne_oracle_bwd_packed(
+            _p(q), _p(k), _p(v), _p(do), _p(dq), _p(dk), _p(dv),
+            cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), cu.shape[0] - 1, Hq, Hkv, d,
+            float(theta), int(pos_offset), int(threads))
+        if rc:
+            raise ValueError(f"ne_oracle_bwd_packed failed with code {rc}")
+        return {"dq": dq, "dk": dk, "dv": dv}
+
+
 def compile_source(src_path: str, lib_path: str) -> str:
     """Compile one copy of the oracle's C source into a shared library."""
     tmp = lib_path + f".tmp{os.getpid()}"
@@ -253,6 +304,15 @@ def attn_fwd_varlen(q, k, v, seqlens, theta: float, pos_offset: int = 0, threads
 
 def attn_bwd_varlen(q, k, v, do, seqlens, theta: float, pos_offset: int = 0, threads: int = 0):
     return default().attn_bwd_varlen(q, k, v, do, seqlens, theta, pos_offset, threads)
+
+
+def attn_fwd_packed(q, k, v, cu_seqlens, theta: float, pos_offset: int = 0, threads: int = 0):
+    return default().attn_fwd_packed(q, k, v, cu_seqlens, theta, pos_offset, threads)
+
+
+def attn_bwd_packed(q, k, v, do, cu_seqlens, theta: float, pos_offset: int = 0,
+                    threads: int = 0):
+    return default().attn_bwd_packed(q, k, v, do, cu_seqlens, theta, pos_offset, threads)
 
 
 def group_slice(x: np.ndarray, b: int, j: int, heads_per_group: int):

@@ -355,6 +355,71 @@ int ne_oracle_bwd_varlen(const double *q, const double *k, const double *v, cons
 }
 
 /*
+ * Packed variable-length batches: the B sequences are concatenated along the
+ * token axis, sequence b holding tokens cu[b] .. cu[b+1]-1 of the pack
+ * (cu[0] = 0, non-decreasing, cu[B] = total), with no padding between them.
+ * Same definition as the padded form above: each sequence is a causal
+ * problem of its own over positions 0 .. len-1.  q, o, dO, dq are
+ * [total][Hq][d]; k, v, dk, dv are [total][Hkv][d]; lse is [Hq][total].
+ * Every sequence's rows are contiguous, so each call is the B = 1, T = len
+ * problem on a pointer into the pack.
+ */
+static int check_cu(const int *cu, int B)
+{
+    if (!cu || B < 1 || cu[0] != 0)
+        return 1;
+    for (int b = 0; b < B; ++b)
+        if (cu[b + 1] < cu[b])
+            return 1;
+    return 0;
+}
+
+int ne_oracle_fwd_packed(const double *q, const double *k, const double *v, double *o,
+                         double *lse, const int *cu, int B, int Hq, int Hkv, int d,
+                         double theta, long pos_offset, int nthreads)
+{
+    if (check_cu(cu, B) || check_shape(1, 1, Hq, Hkv, d))
+        return 1;
+    const int total = cu[B];
+    double *lse1 = malloc(sizeof(double) * (size_t)Hq * (total > 0 ? total : 1));
+    if (!lse1)
+        return 2;
+    int err = 0;
+    for (int b = 0; b < B && !err; ++b) {
+        int L = cu[b + 1] - cu[b];
+        if (L == 0)
+            continue;
+        err = ne_oracle_fwd(q + (size_t)cu[b] * Hq * d, k + (size_t)cu[b] * Hkv * d,
+                            v + (size_t)cu[b] * Hkv * d, o + (size_t)cu[b] * Hq * d, lse1, 1, L,
+                            Hq, Hkv, d, theta, pos_offset, nthreads, 0);
+        for (int h = 0; h < Hq; ++h)
+            memcpy(lse + (size_t)h * total + cu[b], lse1 + (size_t)h * L, sizeof(double) * L);
+    }
+    free(lse1);
+    return err;
+}
+
+int ne_oracle_bwd_packed(const double *q, const double *k, const double *v, const double *dO,
+                         double *dq, double *dk, double *dv, const int *cu, int B, int Hq,
+                         int Hkv, int d, double theta, long pos_offset, int nthreads)
+{
+    if (check_cu(cu, B) || check_shape(1, 1, Hq, Hkv, d))
+        return 1;
+    int err = 0;
+    for (int b = 0; b < B && !err; ++b) {
+        int L = cu[b + 1] - cu[b];
+        if (L == 0)
+            continue;
+        err = ne_oracle_bwd(q + (size_t)cu[b] * Hq * d, k + (size_t)cu[b] * Hkv * d,
+                            v + (size_t)cu[b] * Hkv * d, dO + (size_t)cu[b] * Hq * d,
+                            dq + (size_t)cu[b] * Hq * d, dk + (size_t)cu[b] * Hkv * d,
+                            dv + (size_t)cu[b] * Hkv * d, NULL, NULL, NULL, 1, L, Hq, Hkv, d,
+                            theta, pos_offset, nthreads, 0);
+    }
+    return err;
+}
+
+/*
  * Decode against a key/value cache (one new token per sequence).  The new
  * token is the last of Tk positions: its own key and value are the cache's
  * last rows, so every cached key is visible to it.  By definition this is the

@@ -458,6 +458,64 @@ def pin_varlen_prefix_and_closed_forms(orc):
     assert _rel(r["dv"][2, 0], do[2, 0].reshape(Hkv, G, d).sum(axis=1)) < 1e-14
 
 
+def _packed_case(lens, Hq, Hkv, d, seed):
+    total = sum(lens)
+    q = _rand((total, Hq, d), seed)
+    k = _rand((total, Hkv, d), seed + 1)
+    v = _rand((total, Hkv, d), seed + 2)
+    do = _rand((total, Hq, d), seed + 3)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(int)
+    return q, k, v, do, cu
+
+
+def pin_packed_torch_sdpa(orc):
+    """Packed batches against torch in float64: each sequence rotated at its
+    own positions 0 .. len-1 (complex-rotation RoPE per segment), then one
+    scaled_dot_product_attention over the whole pack with a block-diagonal
+    causal mask, and autograd of sum(O * dO); to 1e-10."""
+    for (lens, Hq, Hkv, d, seed) in (((5, 17, 1, 9), 6, 2, 16, 131), ((30,), 4, 4, 8, 135),
+                                     ((12, 0, 21), 4, 1, 8, 139)):
+        q, k, v, do, cu = _packed_case(lens, Hq, Hkv, d, seed)
+        total = int(cu[-1])
+        tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+        seg = torch.repeat_interleave(torch.arange(len(lens)), torch.tensor(lens))
+        t = torch.arange(total)
+        allowed = (seg[:, None] == seg[None, :]) & (t[None, :] <= t[:, None])
+        qr = torch.cat([_torch_rope(tq[None, a:b], THETA) for a, b in zip(cu[:-1], cu[1:])
+                        if b > a], dim=1).transpose(1, 2)
+        kr = torch.cat([_torch_rope(tk[None, a:b], THETA) for a, b in zip(cu[:-1], cu[1:])
+                        if b > a], dim=1).transpose(1, 2)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qr, kr, tv[None].transpose(1, 2), attn_mask=allowed, scale=1.0 / math.sqrt(d),
+            enable_gqa=True)
+        (o * torch.tensor(do)[None].transpose(1, 2)).sum().backward()
+        with torch.no_grad():
+            sc = qr @ kr.repeat_interleave(Hq // Hkv, dim=1).transpose(-1, -2) / math.sqrt(d)
+            lse = torch.logsumexp(sc.masked_fill(~allowed, float("-inf")), dim=-1)[0]
+        o1, lse1 = orc.attn_fwd_packed(q, k, v, cu, THETA)
+        r = orc.attn_bwd_packed(q, k, v, do, cu, THETA)
+        assert _rel(o1, o.detach()[0].transpose(0, 1).numpy()) < 1e-10, "o"
+        assert np.abs(lse1 - lse.numpy()).max() < 1e-10, "lse"
+        for n, g in (("dq", tq.grad), ("dk", tk.grad), ("dv", tv.grad)):
+            assert _rel(r[n], g.numpy()) < 1e-10, (n, _rel(r[n], g.numpy()))
+
+
+def pin_packed_single_tokens(orc):
+    """A pack of one-token sequences: each token sees only itself, so
+    O = v of its own token, lse = <q, k> / sqrt(d) (position 0 rotates
+    nothing), dq = dk = 0 and dv = the sum of dO over the group's heads."""
+    n, Hq, Hkv, d = 7, 6, 3, 8
+    q, k, v, do, cu = _packed_case([1] * n, Hq, Hkv, d, 141)
+    G = Hq // Hkv
+    o, lse = orc.attn_fwd_packed(q, k, v, cu, THETA)
+    assert _rel(o, np.repeat(v, G, axis=1)) < 1e-14
+    want = (q * np.repeat(k, G, axis=1)).sum(-1).T / math.sqrt(d)
+    assert np.abs(lse - want).max() < 1e-13
+    r = orc.attn_bwd_packed(q, k, v, do, cu, THETA)
+    assert np.abs(r["dq"]).max() < 1e-14 and np.abs(r["dk"]).max() < 1e-14
+    assert _rel(r["dv"], do.reshape(n, Hkv, G, d).sum(axis=2)) < 1e-14
+
+
 ALL_PINS = [
     pin_rope_closed_form,
     pin_rope_identity_and_orthogonal,
@@ -478,4 +536,6 @@ ALL_PINS = [
     pin_decode_closed_forms,
     pin_varlen_torch_sdpa,
     pin_varlen_prefix_and_closed_forms,
+    pin_packed_torch_sdpa,
+    pin_packed_single_tokens,
 ]

@@ -47,12 +47,17 @@ MUTATIONS = [
      "lse[((size_t)b * Hq + h) * T + t] = 0.0;"),
     ("varlen_fwd_full_length", "1, L, Hq, Hkv, d, theta, pos_offset, nthreads, 0);",
      "1, T, Hq, Hkv, d, theta, pos_offset, nthreads, 0);"),
-    ("varlen_bwd_reads_padding_dO", "NULL, NULL, NULL, 1, L, Hq, Hkv, d,",
-     "NULL, NULL, NULL, 1, T, Hq, Hkv, d,"),
+    ("varlen_bwd_reads_padding_dO", "dv + IDX(b, 0, 0, 0, T, Hkv, d), NULL, NULL, NULL, 1, L,",
+     "dv + IDX(b, 0, 0, 0, T, Hkv, d), NULL, NULL, NULL, 1, T,"),
     ("varlen_batch_stride", "err = ne_oracle_fwd(q + IDX(b, 0, 0, 0, T, Hq, d),",
      "err = ne_oracle_fwd(q + IDX(b, 0, 0, 0, L, Hq, d),"),
-    ("varlen_lse_row_stride", "lse1 + (size_t)h * L, sizeof(double) * L);",
-     "lse1 + (size_t)h * T, sizeof(double) * L);"),
+    ("varlen_lse_row_stride", "* T, lse1 + (size_t)h * L, sizeof(double) * L);",
+     "* T, lse1 + (size_t)h * T, sizeof(double) * L);"),
+    ("packed_output_stride", "o + (size_t)cu[b] * Hq * d, lse1",
+     "o + (size_t)cu[b] * Hkv * d, lse1"),
+    ("packed_lse_drops_offset", "memcpy(lse + (size_t)h * total + cu[b],",
+     "memcpy(lse + (size_t)h * total,"),
+    ("packed_bwd_dO_stride", "dO + (size_t)cu[b] * Hq * d,", "dO + (size_t)cu[b] * Hkv * d,"),
 ]
 
 
