@@ -230,9 +230,10 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
  * Padding rows of q, k, v and dO must hold values the other entry points
  * accept (finite, within the fp16 range after rotation; zeros or a pad
  * token's activations do): tiles that straddle a sequence's end compute over
- * them, with zero weight, before the padding is overwritten.  Work is proportional to the valid
- * rows: query tiles (and, in the backward, key tiles) wholly past a
- * sequence's end are skipped.  The library builds the tables of live work
+ * them, with zero weight, before the padding is overwritten.  Query tiles
+ * (and, in the backward, key tiles) wholly past a sequence's end are
+ * skipped; the backward's preprocess still covers every row.  The library
+ * builds the tables of live work
  * units on the host and copies them into the workspace with an asynchronous
  * copy from pageable memory, so these calls cannot be captured into a CUDA
  * graph; calls that share a workspace must not overlap on the GPU.
