@@ -38,8 +38,9 @@
  *
  * Preconditions: B, T >= 1 (T <= 2^24); Hq, Hkv >= 1 and Hq % Hkv == 0; d in
  * {32, 64, 128}; rope_theta > 0 and finite; tensor and workspace pointers
- * 16-byte aligned, lse 4-byte aligned; the current device is an sm_103 GPU.  Score-side operands (the rotated q and k, and the
- * backward's dS) go through the tensor cores as fp16, so elements of q and k,
+ * 16-byte aligned, lse 4-byte aligned; the current device is an sm_103 GPU.
+ * Score-side operands (the rotated q and k, and the backward's dS) go
+ * through the tensor cores as fp16, so elements of q and k,
  * and of dS = P (dP - D), must stay below 65504 in magnitude; a kernel that
  * sees a larger value records NE_ERR_RANGE in the status word.
  * RoPE angles are evaluated from each frequency rounded to a 32-bit
