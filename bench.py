@@ -61,7 +61,14 @@ def _mb(n_elem, bytes_per):
 
 def kernel_work(w=W):
     """Algorithmic flops and compulsory HBM bytes of ONE launch of each kernel
-    for one layer (per-unit figures x the units one launch processes)."""
+    for one layer (per-unit figures x the units one launch processes).
+
+    "bytes" follows the compulsory-traffic convention: the forward reads Q, K,
+    V and writes O and lse.  Traffic a kernel makes by choice goes to
+    "extra_bytes" and is not counted in the roofline: the training-path
+    forward also stores the fp16 rotated Q' and K' for the backward.  The dq
+    and dk/dv kernels read those fp16 Q', K' in place of the bf16 q, k (the
+    same number of bytes)."""
     B, T, Hq, Hkv, d = w.B, w.T, w.Hq, w.Hkv, w.d
     pairs = w.pairs * B * Hq                       # causal (t, s) pairs x heads
     q = B * T * Hq * d * 2
@@ -69,14 +76,16 @@ def kernel_work(w=W):
     row = B * Hq * T * 4                           # lse or D
     return {
         # QK^T and PV: 2 GEMMs of 2d flops per pair; reads Q K V, writes O lse
-        # and the fp16 Q', K' it rotated (for the backward)
-        "fwd": {"flops": 4.0 * d * pairs, "bytes": q + 2 * kv + q + row + q + kv},
+        "fwd": {"flops": 4.0 * d * pairs, "bytes": q + 2 * kv + q + row, "extra_bytes": q + kv},
         # D = rowsum(dO * O): reads O, dO; writes D
-        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 2 * q + row},
-        # dQ = dS K' (one GEMM; the S and dP recompute is not algorithmic work)
-        "bwd_dq": {"flops": 2.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + q},
-        # S, dP, dV, dK (four GEMMs); reads Q' K' (fp16) V dO lse D, writes dK dV
-        "bwd_dkdv": {"flops": 8.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + 2 * kv},
+        "bwd_pre": {"flops": 2.0 * B * T * Hq * d, "bytes": 2 * q + row, "extra_bytes": 0},
+        # dQ = dS K' (one GEMM; the S and dP recompute is not algorithmic work);
+        # reads Q' K' V dO lse D, writes dQ
+        "bwd_dq": {"flops": 2.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + q,
+                   "extra_bytes": 0},
+        # S, dP, dV, dK (four GEMMs); reads Q' K' V dO lse D, writes dK dV
+        "bwd_dkdv": {"flops": 8.0 * d * pairs, "bytes": q + 2 * kv + q + 2 * row + 2 * kv,
+                     "extra_bytes": 0},
     }
 
 
@@ -381,7 +390,8 @@ def run_ours(args, rank, world, local_rank):
     roof["traffic"] = measured_traffic(dom)
     roof["kernel"] = dom
     roof["peak_source"] = f"{peaks['source']} (burst: kernels timed inside a short step)"
-    roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
+    roof["algorithmic"] = {"flops": wk["flops"], "bytes": wk["bytes"],
+                           "extra_bytes": wk["extra_bytes"]}
 
     kernels = {n: {"avg_us": avg_ms[n] * 1e3, "launches": len(per[n]),
                    "share": avg_ms[n] / sum(avg_ms.values()),

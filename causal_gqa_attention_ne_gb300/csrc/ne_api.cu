@@ -1,7 +1,6 @@
 // ne_api.cu -- the C ABI of include/ne_attn.h: argument validation, TMA
 // descriptor construction, launch sequencing and the device status word.
 #include <algorithm>
-#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -21,7 +20,10 @@ namespace {
 // that run out and fp16 range overflows are OR-ed into it by the kernels.
 __device__ uint32_t g_status_word;
 
-std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+// Bound on device-side waits for launches made by this host thread (each
+// thread has its own value, so a thread changing it never affects another
+// thread's launches).
+thread_local uint64_t g_wait_limit_ns = 2000000000ull;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -124,7 +126,11 @@ int make_map(CUtensorMap *m, const void *ptr, int B, int T, int H, int d, bool f
     return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
-// Fixed-point RoPE frequencies: round(2^32 * theta^(-2i/d) / (2 pi)) mod 2^32.
+// Fixed-point RoPE frequencies: F_i = round(2^64 * theta^(-2i/d) / (2 pi))
+// mod 2^64 as two 32-bit words.  The fraction f (in [0, 1)) is a double, so
+// F_i carries its 53 significant bits: an error below 2^-54 turn per
+// position, 2^-30 turn at position 2^24.  Scaling by 2^32 and taking the
+// integer part are exact in double arithmetic.
 void fill_rope(ne::RopeFreqs &fr, int d, float theta)
 {
     std::memset(&fr, 0, sizeof(fr));
@@ -132,9 +138,16 @@ void fill_rope(ne::RopeFreqs &fr, int d, float theta)
     for (int i = 0; i < d / 2; ++i) {
         double f = std::pow(static_cast<double>(theta), -2.0 * i / d) / two_pi;
         f -= std::floor(f);
-        const unsigned long long v =
-            static_cast<unsigned long long>(std::llround(f * 4294967296.0));
-        fr.turn[i] = static_cast<uint32_t>(v & 0xffffffffull);
+        const double top = std::floor(f * 4294967296.0);          // high word
+        const double rest = f * 4294967296.0 - top;               // in [0, 1)
+        unsigned long long hi = static_cast<unsigned long long>(top);
+        unsigned long long lo = static_cast<unsigned long long>(std::llround(rest * 4294967296.0));
+        if (lo > 0xffffffffull) {   // rounded up to the next high word
+            lo = 0;
+            ++hi;
+        }
+        fr.hi[i] = static_cast<uint32_t>(hi & 0xffffffffull);
+        fr.lo[i] = static_cast<uint32_t>(lo);
     }
 }
 
@@ -162,7 +175,7 @@ ne::AttnParams base_params(int B, int T, int Hq, int Hkv, int d, float theta, ui
     p.scale = 1.0f / std::sqrt(static_cast<float>(d));
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.status = status;
-    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.wait_limit_ns = g_wait_limit_ns;
     fill_rope(p.rope, d, theta);
     return p;
 }
@@ -614,7 +627,7 @@ const char *ne_attn_status_string(int status)
 
 void ne_attn_set_wait_limit_ns(uint64_t limit_ns)
 {
-    g_wait_limit_ns.store(limit_ns ? limit_ns : 1);
+    g_wait_limit_ns = limit_ns ? limit_ns : 1;
 }
 
 int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream)
@@ -900,11 +913,22 @@ int ne_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void 
                         const float *lse, const void *dO, void *dq, void *dk, void *dv, int B,
                         int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
 {
+    // The checks run in ne_attn_bwd's order, with the scratch limit where
+    // ne_attn_bwd checks the workspace, so the same arguments give the same
+    // status.
+    if (!o || !dq || !dk || !dv)
+        return NE_ERR_NULL;
+    if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return NE_ERR_ALIGN;
+    if (!q || !k || !v || !lse || !dO)
+        return NE_ERR_NULL;
     int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
     if (ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d) > kNoAllocScratchBytes)
         return NE_ERR_TOO_LARGE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse))
+        return NE_ERR_ALIGN;
     uint32_t *status = nullptr;
     if ((rc = device_state(&status)) != NE_OK)
         return rc;

@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float sn, cs;
-                    rope_sincos(t, p.rope.turn[8 * c + 2 * e + hh], sn, cs);
+                    rope_sincos(t, p.rope, 8 * c + 2 * e + hh, sn, cs);
                     const float x = hh ? bf16_hi(qav[e]) : bf16_lo(qav[e]);
                     const float y = hh ? bf16_hi(qbv[e]) : bf16_lo(qbv[e]);
                     u[hh] = x * cs - y * sn;
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float sn, cs;
-                rope_sincos(pos, p.rope.turn[8 * c + 2 * e + hh], sn, cs);
+                rope_sincos(pos, p.rope, 8 * c + 2 * e + hh, sn, cs);
                 const float x = hh ? bf16_hi(kav[e]) : bf16_lo(kav[e]);
                 const float y = hh ? bf16_hi(kbv[e]) : bf16_lo(kbv[e]);
                 u[hh] = x * cs - y * sn;
@@ -290,7 +290,7 @@ __device__ __forceinline__ void epilogue_inverse_rope(uint32_t taddr, float scal
             for (int e = 0; e < 32; ++e) {
                 x[e] = __uint_as_float(a[e]) * scale;
                 y[e] = __uint_as_float(b[e]) * scale;
-                rope_inverse_pair(x[e], y[e], pos, fr.turn[c0 + e]);
+                rope_inverse_pair(x[e], y[e], pos, fr, c0 + e);
             }
             if (store) {
                 store_row32_bf16(dst + c0, x);
@@ -307,7 +307,7 @@ __device__ __forceinline__ void epilogue_inverse_rope(uint32_t taddr, float scal
             x[e] = __uint_as_float(a[e]) * scale;
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-            rope_inverse_pair(x[e], x[e + 16], pos, fr.turn[e]);
+            rope_inverse_pair(x[e], x[e + 16], pos, fr, e);
         if (store)
             store_row32_bf16(dst, x);
     }
@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(384, 1)
         if constexpr (C::STAGE) {
 #pragma unroll
             for (int e = 0; e < D / 2; ++e)
-                rope_sincos(static_cast<uint32_t>(t), p.rope.turn[e], sn[e], cs[e]);
+                rope_sincos(static_cast<uint32_t>(t), p.rope, e, sn[e], cs[e]);
         }
 #pragma unroll
         for (int g = 0; g < GC; ++g)

@@ -93,134 +93,40 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_addr, int nc, int
                      TL::LAYOUT);
 }
 
-// RoPE angles.  Frequency i is passed as a 32-bit fixed-point number of turns
-// per position, F_i = round(2^32 * theta^(-2i/d) / (2 pi)).  The angle of
-// position p is then p * F_i modulo 2^32 turns (exact integer wrap-around),
-// mapped to [-pi, pi) before the hardware sine/cosine.
+// RoPE angles.  Frequency i is passed as a 64-bit fixed-point number of
+// turns per position, F_i = round(2^64 * theta^(-2i/d) / (2 pi)) mod 2^64,
+// split into its high and low 32-bit words.  The angle of position p, in
+// turns modulo 1, is p * F_i mod 2^64; its top 32 bits are
+// p * hi + floor(p * lo / 2^32) (mod 2^32): integer arithmetic, exact but for
+// the dropped low word (under 2^-32 turn).  That top word, read as a signed
+// fraction of a turn, is the angle in [-pi, pi) before the hardware
+// sine/cosine, so the error of the angle does not grow with the position.
 struct RopeFreqs {
-    uint32_t turn[64];
+    uint32_t hi[64];
+    uint32_t lo[64];
 };
 
-__device__ __forceinline__ void rope_sincos(uint32_t pos, uint32_t f, float &s, float &c)
+__device__ __forceinline__ void rope_sincos(uint32_t pos, const RopeFreqs &fr, int i, float &s,
+                                            float &c)
 {
-    const int32_t t = static_cast<int32_t>(pos * f);
+    const int32_t t = static_cast<int32_t>(pos * fr.hi[i] + __umulhi(pos, fr.lo[i]));
     const float ang = static_cast<float>(t) * 1.4629180792671596e-09f;   // 2 pi / 2^32
     __sincosf(ang, &s, &c);
 }
 
-// Rotate row r of a bf16 tile in place, writing fp16 (the score-side operand
-// type).  x'_i = x_i cos - x_{i+D/2} sin, x'_{i+D/2} = x_{i+D/2} cos + x_i sin.
-// Returns the largest |x'| seen (for the fp16 range check).
-template <int D>
-__device__ __forceinline__ float rope_row_to_f16(uint8_t *tile, int r, uint32_t pos,
-                                                 const RopeFreqs &fr)
-{
-    constexpr int HC = D / 16;   // chunks in the first half of the row
-    float mx = 0.f;
-#pragma unroll
-    for (int c = 0; c < HC; ++c) {
-        uint4 *pa = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c));
-        uint4 *pb = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c + HC));
-        const uint4 a = *pa, b = *pb;
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-        const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
-        uint32_t ao[4], bo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float s0, c0, s1, c1;
-            rope_sincos(pos, fr.turn[8 * c + 2 * e], s0, c0);
-            rope_sincos(pos, fr.turn[8 * c + 2 * e + 1], s1, c1);
-            const float x0 = bf16_lo(av[e]), x1 = bf16_hi(av[e]);
-            const float y0 = bf16_lo(bv[e]), y1 = bf16_hi(bv[e]);
-            const float u0 = x0 * c0 - y0 * s0, w0 = y0 * c0 + x0 * s0;
-            const float u1 = x1 * c1 - y1 * s1, w1 = y1 * c1 + x1 * s1;
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(u0), fabsf(w0)), fmaxf(fabsf(u1), fabsf(w1))));
-            ao[e] = pack_f16x2(u0, u1);
-            bo[e] = pack_f16x2(w0, w1);
-        }
-        *pa = make_uint4(ao[0], ao[1], ao[2], ao[3]);
-        *pb = make_uint4(bo[0], bo[1], bo[2], bo[3]);
-    }
-    return mx;
-}
-
-// ---- table-driven RoPE (no special-function unit work per element) ----
-//
-// A CTA keeps float2 tab[j][r] = (cos, sin)(r * theta_j) for the 128 rows r
-// of a tile and the D/2 frequencies j, and per rotated tile the 64 values
-// base[j] = (cos, sin)(p0 * theta_j) of the tile's first position p0.  The
-// angle of row r is p0*theta_j + r*theta_j; its cosine and sine come from the
-// angle-addition formulas (four multiply-adds).  Both tables come from the
-// hardware sine/cosine on the exactly reduced angle in [-pi, pi), where its
-// absolute error is below 4e-7 (far below the fp16 rounding of the result).
-
-__device__ __forceinline__ float2 rope_cs(uint32_t pos, uint32_t f)
-{
-    float s, c;
-    rope_sincos(pos, f, s, c);
-    return make_float2(c, s);
-}
-
-// Thread r (0..127) fills row r of the table.
-template <int D>
-__device__ __forceinline__ void rope_table_fill(float2 *tab, int r, const RopeFreqs &fr)
-{
-#pragma unroll 4
-    for (int j = 0; j < D / 2; ++j)
-        tab[j * kRows + r] = rope_cs(static_cast<uint32_t>(r), fr.turn[j]);
-}
-
-// Rotate row r of a bf16 tile in place to fp16 using the table and the
-// tile's base; returns the largest |x'| (fp16 range check).
-template <int D>
-__device__ __forceinline__ float rope_row_table(uint8_t *tile, int r, const float2 *tab,
-                                                const float2 *base)
-{
-    constexpr int HC = D / 16;
-    float mx = 0.f;
-#pragma unroll
-    for (int c = 0; c < HC; ++c) {
-        uint4 *pa = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c));
-        uint4 *pb = reinterpret_cast<uint4 *>(tile + tile_chunk<D>(r, c + HC));
-        const uint4 a = *pa, b = *pb;
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-        const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
-        uint32_t ao[4], bo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float u[2], w[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j = 8 * c + 2 * e + h;
-                const float2 t = tab[j * kRows + r];
-                const float2 bs = base[j];
-                const float cs = bs.x * t.x - bs.y * t.y;
-                const float sn = bs.y * t.x + bs.x * t.y;
-                const float x = h ? bf16_hi(av[e]) : bf16_lo(av[e]);
-                const float y = h ? bf16_hi(bv[e]) : bf16_lo(bv[e]);
-                u[h] = x * cs - y * sn;
-                w[h] = y * cs + x * sn;
-                mx = fmaxf(mx, fmaxf(fabsf(u[h]), fabsf(w[h])));
-            }
-            ao[e] = pack_f16x2(u[0], u[1]);
-            bo[e] = pack_f16x2(w[0], w[1]);
-        }
-        *pa = make_uint4(ao[0], ao[1], ao[2], ao[3]);
-        *pb = make_uint4(bo[0], bo[1], bo[2], bo[3]);
-    }
-    return mx;
-}
-
 // Rotate row r of a bf16 tile in place to fp16 with the hardware sine/cosine
 // per pair, loading a batch of up to four chunk pairs before computing so the
-// shared-memory and special-function latencies overlap.  Returns max |x'|.
+// shared-memory and special-function latencies overlap.  Returns max |x'|
+// (the fp16 range check) and sets ss to the sum of x'^2 over the row (fp32,
+// before rounding).
 template <int D>
 __device__ __forceinline__ float rope_row_ilp(uint8_t *tile, int r, uint32_t pos,
-                                              const RopeFreqs &fr)
+                                              const RopeFreqs &fr, float &ss)
 {
     constexpr int HC = D / 16;
     constexpr int BATCH = HC < 2 ? HC : 2;
     float mx = 0.f;
+    ss = 0.f;
 #pragma unroll
     for (int c0 = 0; c0 < HC; c0 += BATCH) {
         uint4 a[BATCH], b[BATCH];
@@ -239,12 +145,13 @@ __device__ __forceinline__ float rope_row_ilp(uint8_t *tile, int r, uint32_t pos
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float sn, cs;
-                    rope_sincos(pos, fr.turn[8 * (c0 + i) + 2 * e + h], sn, cs);
+                    rope_sincos(pos, fr, 8 * (c0 + i) + 2 * e + h, sn, cs);
                     const float x = h ? bf16_hi(av[e]) : bf16_lo(av[e]);
                     const float y = h ? bf16_hi(bv[e]) : bf16_lo(bv[e]);
                     u[h] = x * cs - y * sn;
                     w[h] = y * cs + x * sn;
                     mx = fmaxf(mx, fmaxf(fabsf(u[h]), fabsf(w[h])));
+                    ss = fmaf(u[h], u[h], fmaf(w[h], w[h], ss));
                 }
                 av[e] = pack_f16x2(u[0], u[1]);
                 bv[e] = pack_f16x2(w[0], w[1]);
@@ -274,10 +181,11 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16 *dst, const float
 }
 
 // Inverse rotation (by -angle) of a pair of fp32 values held in registers.
-__device__ __forceinline__ void rope_inverse_pair(float &x, float &y, uint32_t pos, uint32_t f)
+__device__ __forceinline__ void rope_inverse_pair(float &x, float &y, uint32_t pos,
+                                                  const RopeFreqs &fr, int i)
 {
     float s, c;
-    rope_sincos(pos, f, s, c);
+    rope_sincos(pos, fr, i, s, c);
     const float u = x * c + y * s;
     const float w = y * c - x * s;
     x = u;
@@ -367,6 +275,7 @@ struct AttnParams {
     int GC, nchunks;             // query heads per CTA, CTAs per KV group (Q-major kernels)
     float scale_log2;            // log2(e) / sqrt(d)
     float scale;                 // 1 / sqrt(d)
+    const void *q_in, *k_in;     // forward: bf16 q, k (re-read for exact scores of large rows)
     const void *o_in;            // backward: forward output O (preprocess)
     const void *do_in;           // backward: dO (preprocess)
     void *out0;                  // forward: O; backward: dq / dk

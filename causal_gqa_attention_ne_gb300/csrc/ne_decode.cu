@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kDecThreads, 8)
         const int g = idx / (D / 2), i = idx % (D / 2);
         const __nv_bfloat16 *qrow = qg + (static_cast<size_t>(b) * p.Hq + j * G + g) * D;
         float sn, cs;
-        rope_sincos(qpos, p.rope.turn[i], sn, cs);
+        rope_sincos(qpos, p.rope, i, sn, cs);
         const float x = __bfloat162float(qrow[i]), y = __bfloat162float(qrow[i + D / 2]);
         qs[g * D + i] = x * cs - y * sn;
         qs[g * D + i + D / 2] = y * cs + x * sn;
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kDecThreads, 8)
                 for (int e = 0; e < 8; ++e) {
                     const int i = 8 * cc + e;
                     float sn, cs;
-                    rope_sincos(static_cast<uint32_t>(s), p.rope.turn[i], sn, cs);
+                    rope_sincos(static_cast<uint32_t>(s), p.rope, i, sn, cs);
                     const float x = (e & 1) ? bf16_hi(av[e >> 1]) : bf16_lo(av[e >> 1]);
                     const float y = (e & 1) ? bf16_hi(bv[e >> 1]) : bf16_lo(bv[e >> 1]);
                     const float xr = x * cs - y * sn, yr = y * cs + x * sn;

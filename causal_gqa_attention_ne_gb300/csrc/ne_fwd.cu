@@ -47,20 +47,32 @@ namespace ne {
 // Shared-memory plan: QB Q-tile sets of GC heads (two for D <= 64, so the
 // next unit's Q' is loaded and rotated while the current unit runs), ST K/V
 // stages (as many as fit, at most four), two O staging blocks (D <= 64), the
-// running max / sum.
+// running max / sum of a split head, and the exact-score bookkeeping of
+// large-norm rows: per Q slot the ballot of its large rows and their exact
+// rotated vectors, the exact vectors of one K tile's large rows, and per K
+// stage a patch record (see below).
 template <int D, int GC>
 struct FwdPlan {
     using TL = Tile<D>;
     static constexpr bool STAGE = (D <= 64);
     static constexpr int QB = (D <= 64) ? 2 : 1;
+    // large-norm rows scored exactly per Q tile and per K tile
+    static constexpr int NOUT = (D == 64) ? 2 : 4;
+    static constexpr int BALLOT_BYTES = 256;                    // [QB][GC][4] + [4] words
+    static constexpr int QOV_BYTES = QB * GC * NOUT * D * 4;    // exact q' of large rows
+    static constexpr int KOV_BYTES = NOUT * D * 4;              // exact k' of large rows
+    static constexpr int PHDR_BYTES = 256;                      // counts and row indices
+    // per stage: header, then dS_k [NOUT][GC][128] and dS_q [GC][NOUT][128] (fp16)
+    static constexpr int PREC_BYTES = PHDR_BYTES + 2 * NOUT * GC * kRows * 2;
     static constexpr int fixed_bytes()
     {
-        return QB * GC * TL::BYTES + (STAGE ? 2 * TL::BLOCK : 0) + 2 * kRows * 4 + 1024;
+        return QB * GC * TL::BYTES + (STAGE ? 2 * TL::BLOCK : 0) + 2 * kRows * 4 + BALLOT_BYTES +
+               QOV_BYTES + KOV_BYTES + 1024;
     }
     static constexpr int stages()
     {
         int st = 4;
-        while (st > 1 && fixed_bytes() + st * 2 * TL::BYTES > 232448 - 1024)
+        while (st > 1 && fixed_bytes() + st * (2 * TL::BYTES + PREC_BYTES) > 232448 - 1024)
             --st;
         return st;
     }
@@ -70,15 +82,23 @@ struct FwdPlan {
 template <int D, int GC, int ST>
 struct FwdCfg {
     using TL = Tile<D>;
-    static constexpr bool STAGE = FwdPlan<D, GC>::STAGE;     // O leaves by TMA store
-    static constexpr int QB = FwdPlan<D, GC>::QB;
+    using PL = FwdPlan<D, GC>;
+    static constexpr bool STAGE = PL::STAGE;                 // O leaves by TMA store
+    static constexpr int QB = PL::QB;
+    static constexpr int NOUT = PL::NOUT;
     static constexpr int OFF_Q = 0;                          // [QB][GC] tiles
     static constexpr int OFF_K = OFF_Q + QB * GC * TL::BYTES;
     static constexpr int OFF_V = OFF_K + ST * TL::BYTES;
     static constexpr int OFF_O = OFF_V + ST * TL::BYTES;      // [2] staging blocks
     // group 1's running max and sum of the split head: float [2][128]
     static constexpr int OFF_SPL = OFF_O + (STAGE ? 2 * TL::BLOCK : 0);
-    static constexpr int SMEM_BYTES = smem_one_cta(OFF_SPL + 2 * kRows * 4 + 1024);
+    // uint32 ballots of large rows: Q slots [QB][GC][4 warps], then the
+    // current K tile [4 warps]
+    static constexpr int OFF_BAL = OFF_SPL + 2 * kRows * 4;
+    static constexpr int OFF_QOV = OFF_BAL + PL::BALLOT_BYTES;   // float [QB][GC][NOUT][D]
+    static constexpr int OFF_KOV = OFF_QOV + PL::QOV_BYTES;      // float [NOUT][D]
+    static constexpr int OFF_PREC = OFF_KOV + PL::KOV_BYTES;     // [ST] patch records
+    static constexpr int SMEM_BYTES = smem_one_cta(OFF_PREC + ST * PL::PREC_BYTES + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NSL = (GC + 1) / 2;          // O accumulators per softmax group
     static constexpr bool SPLIT = (GC & 1) != 0;      // one head's key halves in both groups
@@ -89,6 +109,25 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448 - 1024, "shared memory budget");
     static_assert(ST >= 2, "K/V double buffering");
     static_assert(!STAGE || TL::NB == 1, "staged epilogue stores one column block per head");
+    static_assert(QB * GC * 4 * 4 + 16 <= PL::BALLOT_BYTES, "ballot words");
+    static_assert(4 * (1 + NOUT + GC + GC * NOUT) <= PL::PHDR_BYTES, "patch record header");
+};
+
+// Patch record of one K stage, written by the RoPE warpgroup once it has
+// rotated the stage's K tile, read by the softmax groups for every item of
+// that tile.  A row whose rotated vector has mean square above 2 (sum of
+// squares > 2 D) is "large": its scores' fp16 rounding error, proportional to
+// |q'||k'|, would exceed what the 1e-3 lse tolerance allows.  For the pairs
+// with a large key row (column kcol[i] of the tile) or a large query row
+// (row qrow[g][i] of head g's Q tile) the record holds
+//   delta = <q', k'> exact (fp32 from the bf16 inputs) - <fp16 q', fp16 k'>
+// which the softmax thread adds to the score the tensor cores computed from
+// the fp16 operands.
+struct PatchHdr {
+    int kcnt;        // large key rows in the tile (<= NOUT)
+    int qcnt[4];     // per head of the unit: large query rows (<= NOUT)
+    int kcol[4];     // their key indices in the tile
+    int qrow[4][4];  // [head][i]: their row indices in the Q tile
 };
 
 struct FwdUnit {

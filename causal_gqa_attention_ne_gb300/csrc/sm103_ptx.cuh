@@ -14,6 +14,7 @@ namespace ne {
 // Device status bits (the word is OR-ed; the host maps them to ne_status).
 constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevRange = 2u;
+constexpr uint32_t kDevPrecision = 4u;   // more large-norm rows in a tile than are scored exactly
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

@@ -43,11 +43,12 @@
  * through the tensor cores as fp16, so elements of q and k,
  * and of dS = P (dP - D), must stay below 65504 in magnitude; a kernel that
  * sees a larger value records NE_ERR_RANGE in the status word.
- * RoPE angles are evaluated from each frequency rounded to a 32-bit
- * fixed-point fraction of a turn, times the position (exact modulo one
- * turn).  The angle error is at most 2 pi * pos * 2^-33 radians:
- * 3e-6 at position 4096, 8e-4 at 2^20 and 1.2e-2 at 2^24.  The tolerances
- * above are verified up to T = 4096.
+ * RoPE angles are evaluated from each frequency rounded to a 64-bit
+ * fixed-point fraction of a turn, times the position (exact modulo one turn
+ * but for the dropped low word, under 2^-32 turn), so the angle is reduced
+ * exactly into [-pi, pi) at every position and its error does not grow with
+ * T: about 2e-7 radians from the float conversion, plus the hardware
+ * sine/cosine error.
  *
  * Errors.  Argument errors are returned synchronously and launch nothing.
  * Launch failures return NE_ERR_CUDA.  Device-side errors (a bounded wait
@@ -277,10 +278,11 @@ int ne_attn_get_error(void *stream);
 const char *ne_attn_status_string(int status);
 
 /*
- * Upper bound, in nanoseconds, on every device-side wait of later launches
- * (default 2e9).  A wait that runs out makes its kernel record NE_ERR_TIMEOUT,
- * drain its own in-flight work and return.  Not thread-safe against
- * concurrent launches from other host threads.
+ * Upper bound, in nanoseconds, on every device-side wait of the launches the
+ * calling host thread makes afterwards (default 2e9).  Each host thread has
+ * its own value, so setting it never changes another thread's launches.  A
+ * wait that runs out makes its kernel record NE_ERR_TIMEOUT, drain its own
+ * in-flight work and return.
  */
 void ne_attn_set_wait_limit_ns(uint64_t limit_ns);
 
@@ -302,7 +304,9 @@ int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream);
  * fail or fragment, and callers whose own interface gives them no place to
  * pass a workspace pointer through.
  *
- * Same arguments, results and errors as ne_attn_bwd, minus the workspace.
+ * Same arguments, results and errors as ne_attn_bwd, minus the workspace
+ * (argument checks run in ne_attn_bwd's order; NE_ERR_TOO_LARGE takes the
+ * place of NE_ERR_WORKSPACE).
  * The scratch ne_attn_bwd keeps in the workspace (D, Q', K') lives instead in
  * one fixed device array of ne_attn_bwd_noalloc_max_scratch() bytes (32 MiB)
  * compiled into the library: every GPU that loads the library holds it until
@@ -311,7 +315,10 @@ int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream);
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array: calls that can overlap on the GPU
+ * capture.  The address is kept for the rest of the process, like the status
+ * word's: after cudaDeviceReset the library's device variables live at new
+ * addresses, so do not call the library again in that process after a
+ * reset.  All calls share the one array: calls that can overlap on the GPU
  * (different streams, or different host threads, on the same device) race on
  * it and must be serialised by the caller.  The array keeps the last call's
  * contents; every byte a call reads is written earlier in that same call, so

@@ -90,6 +90,17 @@ def test_backward_argument_errors(lib):
     # no-allocation variant: shape whose scratch exceeds its fixed buffer
     assert lib.ne_attn_bwd_noalloc(*args, 8, 4096, 8, 8, 128, 10000.0, None) == 10
     assert lib.ne_attn_bwd_noalloc(*args, 1, 8, 3, 2, 64, 10000.0, None) == 2
+    # pointer checks come first, as in ne_attn_bwd: an oversized shape with a
+    # NULL or misaligned pointer reports the pointer
+    for i in range(9):
+        bad = list(args)
+        bad[i] = None
+        assert lib.ne_attn_bwd_noalloc(*bad, 8, 4096, 8, 8, 128, 10000.0, None) == 1
+    for i in (0, 1, 2, 3, 5, 6, 7, 8):          # 16-byte tensors (lse at 4 needs 4 bytes)
+        bad = list(args)
+        bad[i] = a + 2
+        assert lib.ne_attn_bwd_noalloc(*bad, 1, 8, 2, 2, 64, 10000.0, None) == 4
+        assert lib.ne_attn_bwd(*bad, a, 1 << 20, 1, 8, 2, 2, 64, 10000.0, None) == 4
 
 
 def test_decode_workspace_size_and_argument_errors(lib):
