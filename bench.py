@@ -654,6 +654,102 @@ def run_varlen(args):
     }
 
 
+def run_config(args):
+    """One workload of the parity set timed on its own (SURVEY measurement
+    plan): c3 = gpt116m_b16_t512_h12x4_d64 (one 116M layer, B16), c5 =
+    stress_b4_t4096_h16x4_d128.  Per call, CUDA events on the stream, 10
+    warm-up calls then the median of `--reps`: the forward (ne_attn_fwd), the
+    backward (ne_attn_bwd, preprocess included), the two back to back, and
+    the training pair (ne_attn_fwd_save + ne_attn_bwd_saved).  Inputs of c3
+    fit in L2, so c3 is timed warm (back to back) and with L2 flushed (a
+    write of a buffer twice the L2 size before every timed call)."""
+    import torch
+
+    import causal_gqa_attention_ne_gb300 as ne
+    w = {"c3": ne_inputs.LAYER_116M, "c5": ne_inputs.STRESS}[args.config]
+    ne.load_library()
+    dev = torch.device("cuda", 0)
+    x = {n: t.to(dev) for n, t in ne_inputs.make_inputs(w, 0).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(w.B, w.Hq, w.T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    ws = torch.empty(ne.ne_attn_bwd_workspace_size(w.B, w.T, w.Hq, w.Hkv, w.d),
+                     dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def fwd():
+        ne.ne_attn_fwd(x["q"], x["k"], x["v"], o, lse, w.theta)
+
+    def bwd():
+        ne.ne_attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, ws, w.theta)
+
+    def both():
+        fwd()
+        bwd()
+
+    def pair():
+        ne.ne_attn_fwd_save(x["q"], x["k"], x["v"], o, lse, ws, w.theta)
+        ne.ne_attn_bwd_saved(x["q"], x["k"], x["v"], o, lse, x["do"], dq, dk, dv, ws, w.theta)
+
+    def median_ms(fn, flush_l2):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.reps):
+            if flush_l2:
+                flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        st = ne.ne_attn_get_error()
+        if st != 0:
+            raise RuntimeError(f"device status {ne.NE_STATUS.get(st, st)}")
+        return statistics.median(times)
+
+    peaks = load_peaks()
+    flops = {"fwd": w.flops_fwd(), "bwd": w.flops_bwd()}
+    flops["fwd_bwd"] = flops["fwd"] + flops["bwd"]
+    flops["train_pair"] = flops["fwd_bwd"]
+    modes = [False, True] if args.config == "c3" else [False]
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    sampler.mark(True)
+    out = {}
+    for fl in modes:
+        key = "l2_flushed" if fl else "warm"
+        res = {}
+        for name, fn in (("fwd", fwd), ("bwd", bwd), ("fwd_bwd", both), ("train_pair", pair)):
+            ms = median_ms(fn, fl)
+            tf = flops[name] / (ms * 1e-3) / 1e12
+            res[name] = {"median_ms": ms, "tflops": tf,
+                         "pct_bf16_peak": tf / peaks["bf16_tflops"] * 100.0}
+        out[key] = res
+    sampler.mark(False)
+    sampler.stop()
+    head = out["warm"]["fwd_bwd"]
+    return {
+        "metric": f"causal GQA attn fwd+bwd TFLOP/s, {w.name}",
+        "value": head["tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.reps,
+        "warmup": 10, "ms_per_step": head["median_ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, see ne_inputs.py)",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "timing": "median of per-call CUDA events",
+                   "l2": "warm and L2-flushed (c3 fits in L2)" if args.config == "c3"
+                   else "inputs larger than L2"},
+        "tokens_per_s": w.tokens() / (head["median_ms"] * 1e-3),
+        "results": out,
+        "gpu_launches": None,
+        "clocks": sampler.summary(),
+    }
+
+
 def run_one_layer_for_profiler():
     """One layer (B64 T512 12/4 d64, 270 MB of buffers), fwd then bwd, twice.
     The first pass warms up; a profiler captures the second (-s 4 -c 4)."""
@@ -690,16 +786,22 @@ def oracle_sample(batch_rows: int, threads: int = 0, layer: int = 0):
     return flops / dt / 1e12, dt, used
 
 
-def cpu_baseline(n_layers: int):
-    """The oracle on the first `n_layers` full layers of the workload (fwd + bwd)."""
+def cpu_baseline(n_layers: int, single_rows: int = 2):
+    """The oracle on the first `n_layers` full layers of the workload (fwd + bwd)
+    on all host cores, and on the first `single_rows` batch rows of layer 0
+    with one thread."""
     total, used = 0.0, 1
     for layer in range(n_layers):
         _, dt, used = oracle_sample(W.B, layer=layer)
         total += dt
     val = FLOP_PER_LAYER * n_layers / total / 1e12
+    v1, dt1, _ = oracle_sample(single_rows, threads=1)
     return {"value": val, "unit": UNIT, "cores": used, "kind": "oracle", "seconds": total,
             "sample": f"layers 0-{n_layers - 1} of the {W.layers} of {W.name} (all {W.B} batch "
-                      f"rows), fwd + bwd in float64 (OpenMP over heads / kv groups)"}
+                      f"rows), fwd + bwd in float64 (OpenMP over heads / kv groups)",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1, "seconds": dt1,
+                              "sample": f"layer 0, first {single_rows} of {W.B} batch rows, "
+                                        f"fwd + bwd in float64, one thread"}}
 
 
 def run_reference(args):
@@ -750,10 +852,17 @@ def main():
     ap.add_argument("--window", type=int, default=0,
                     help="time the training step with a sliding window of this many keys "
                          "(the window entry points) instead; prints its own JSON line")
+    ap.add_argument("--config", choices=("c3", "c5"), default=None,
+                    help="time one parity workload on its own (fwd, bwd, fwd+bwd and the "
+                         "training pair; medians of per-call events); own JSON line")
+    ap.add_argument("--reps", type=int, default=50)
     ap.add_argument("--varlen", action="store_true",
                     help="time the padded variable-length SFT step (16 layers of B64 padded "
                          "to 512, seeded lengths) instead; prints its own JSON line")
     args = ap.parse_args()
+    if args.config:
+        print(json.dumps(run_config(args)), flush=True)
+        return
     if args.varlen:
         print(json.dumps(run_varlen(args)), flush=True)
         return

@@ -33,6 +33,9 @@ from ._binding import (  # noqa: F401
     ne_attn_bwd_varlen,
     ne_attn_varlen_plan,
     ne_attn_varlen_workspace_size,
+    ne_attn_packed_workspace_size,
+    ne_attn_fwd_packed,
+    ne_attn_bwd_packed,
     ne_attn_get_error,
     ne_attn_selftest_timeout,
     ne_attn_set_wait_limit_ns,
@@ -43,7 +46,8 @@ __all__ = [
     "NE_STATUS", "NeAttnError", "attention_backward", "attention_decode", "attention_forward",
     "lib_path", "ne_attn_decode", "ne_attn_decode_workspace_size", "ne_attn_fwd_window",
     "ne_attn_bwd_window", "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan",
-    "ne_attn_varlen_workspace_size",
+    "ne_attn_varlen_workspace_size", "ne_attn_packed_workspace_size", "ne_attn_fwd_packed",
+    "ne_attn_bwd_packed",
     "load_library", "ne_attn_bwd", "ne_attn_bwd_dkdv", "ne_attn_bwd_dq",
     "ne_attn_bwd_noalloc", "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save",
     "ne_attn_bwd_saved", "ne_attn_bwd_preprocess_d",

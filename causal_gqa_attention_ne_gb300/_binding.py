@@ -18,7 +18,7 @@ from . import _build
 NE_STATUS = {
     0: "NE_OK", 1: "NE_ERR_NULL", 2: "NE_ERR_SHAPE", 3: "NE_ERR_UNSUPPORTED", 4: "NE_ERR_ALIGN",
     5: "NE_ERR_WORKSPACE", 6: "NE_ERR_CUDA", 7: "NE_ERR_TIMEOUT", 8: "NE_ERR_RANGE",
-    9: "NE_ERR_ARG", 10: "NE_ERR_TOO_LARGE",
+    9: "NE_ERR_ARG", 10: "NE_ERR_TOO_LARGE", 11: "NE_WARN_PRECISION",
 }
 
 EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn_bwd_preprocess",
@@ -27,7 +27,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn
             "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save", "ne_attn_bwd_saved",
             "ne_attn_bwd_preprocess_d", "ne_attn_decode", "ne_attn_decode_workspace_size",
             "ne_attn_fwd_window", "ne_attn_bwd_window", "ne_attn_varlen_workspace_size",
-            "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan")
+            "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan",
+            "ne_attn_packed_workspace_size", "ne_attn_fwd_packed", "ne_attn_bwd_packed")
 
 _lock = threading.Lock()
 _lib = None
@@ -103,6 +104,12 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_bwd_varlen.restype = i
         lib.ne_attn_varlen_plan.argtypes = [vp] + [i] * 5 + [vp] * 3 + [sz, vp]
         lib.ne_attn_varlen_plan.restype = i
+        lib.ne_attn_packed_workspace_size.argtypes = [i] * 5
+        lib.ne_attn_packed_workspace_size.restype = sz
+        lib.ne_attn_fwd_packed.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd_packed.restype = i
+        lib.ne_attn_bwd_packed.argtypes = [vp] * 11 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_packed.restype = i
         _lib = lib
         return lib
 
@@ -484,6 +491,66 @@ def ne_attn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, seqlens, workspace,
                                            float(rope_theta), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd_varlen")
+
+
+def _host_cu(cu_seqlens, total: int):
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32).reshape(-1))
+    if cu.shape[0] < 2:
+        raise ValueError("cu_seqlens needs at least two entries")
+    return cu
+
+
+def _packed_dims(q, k):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("packed q and k are [total, H, d]")
+    total, Hq, d = q.shape
+    return total, Hq, k.shape[1], d
+
+
+def ne_attn_packed_workspace_size(nseq: int, total: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(load_library().ne_attn_packed_workspace_size(nseq, total, Hq, Hkv, d))
+
+
+def ne_attn_fwd_packed(q, k, v, o, lse, cu_seqlens, workspace, rope_theta: float = 10000.0,
+                       stream=None) -> None:
+    """Packed variable-length forward: q [total, Hq, d], k and v [total, Hkv, d],
+    sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (host offsets); lse
+    is [Hq, total]."""
+    total, Hq, Hkv, d = _packed_dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (total, Hq, d), bf)
+    _check(k, "k", (total, Hkv, d), bf)
+    _check(v, "v", (total, Hkv, d), bf)
+    _check(o, "o", (total, Hq, d), bf)
+    _check(lse, "lse", (Hq, total), torch.float32)
+    cu = _host_cu(cu_seqlens, total)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_fwd_packed(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           lse.data_ptr(), cu.ctypes.data, wp, wbytes,
+                                           cu.shape[0] - 1, total, Hq, Hkv, d, float(rope_theta),
+                                           _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd_packed")
+
+
+def ne_attn_bwd_packed(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, workspace,
+                       rope_theta: float = 10000.0, stream=None) -> None:
+    """Packed variable-length backward (o, lse from ne_attn_fwd_packed)."""
+    total, Hq, Hkv, d = _packed_dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (total, h, d), bf)
+    _check(lse, "lse", (Hq, total), torch.float32)
+    cu = _host_cu(cu_seqlens, total)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_packed(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                           o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                           cu.ctypes.data, wp, wbytes, cu.shape[0] - 1, total,
+                                           Hq, Hkv, d, float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_packed")
 
 
 def attention_forward(q, k, v, rope_theta: float = 10000.0, stream=None):

@@ -251,6 +251,8 @@ int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, v
     p.nchunks = p.G / p.GC;
     p.out0 = o;
     p.lse = lse;
+    p.q_in = q;
+    p.k_in = k;
     p.save_rot = save ? 1 : 0;
     p.window = window;
     CUtensorMap mq, mk, mv, mo, mqs, mks;
@@ -347,7 +349,8 @@ int run_dq(int d, const ne::AttnParams &base, void *dq, const CUtensorMap &mq,
     p.nchunks = p.G / p.GC;
     p.out0 = dq;
     CUtensorMap mdq;
-    if (make_map(&mdq, dq, p.B, p.T, p.Hq, d))
+    // packed batches: one batch entry in memory (p.B counts the sequences)
+    if (make_map(&mdq, dq, p.cu != nullptr ? 1 : p.B, p.T, p.Hq, d))
         return NE_ERR_CUDA;
     return ne::launch_bwd_dq(d, mq, mk, mv, mdo, mdq, p, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
@@ -603,6 +606,8 @@ int ne_attn_get_error(void *stream)
         return NE_ERR_TIMEOUT;
     if (word & ne::kDevRange)
         return NE_ERR_RANGE;
+    if (word & ne::kDevPrecision)
+        return NE_WARN_PRECISION;
     return NE_OK;
 }
 
@@ -621,6 +626,8 @@ const char *ne_attn_status_string(int status)
     case NE_ERR_ARG: return "invalid argument (rope_theta must be finite and > 0)";
     case NE_ERR_TOO_LARGE:
         return "shape needs more scratch than ne_attn_bwd_noalloc's fixed buffer holds";
+    case NE_WARN_PRECISION:
+        return "a forward tile held more large-norm rows than are scored exactly";
     default: return "unknown status";
     }
 }
@@ -784,6 +791,8 @@ int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, flo
     p.nchunks = p.G / p.GC;
     p.out0 = o;
     p.lse = lse;
+    p.q_in = q;
+    p.k_in = k;
     CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
         make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
@@ -839,11 +848,12 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
     if ((rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts)) != NE_OK)
         return rc;
     p.o_in = o;
+    // the lengths let the preprocess skip padding rows
+    p.seqlen = ws_int(workspace, 0);
     void *qrot = static_cast<uint8_t *>(bws) + ws_d_bytes(B, T, Hq);
     void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(B, T, Hq, d);
     if (ne::launch_bwd_pre(d, p, q, qrot, k, krot, st) != cudaSuccess)
         return NE_ERR_CUDA;
-    p.seqlen = ws_int(workspace, 0);
     p.units = ws_int(workspace, L.off_dq);
     p.num_units = counts[1];
     if (counts[1] > 0 && (rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
@@ -866,6 +876,210 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
     f.Hq = Hq;
     f.seqlen = p.seqlen;
     return ne::launch_pad_fill(f, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // extern "C"
+
+// ------------------------------------------------------------------------
+// Packed variable-length batches: the sequences concatenated along the rows
+// of one batch entry (q [total][Hq][d], lse [Hq][total]), sequence b at rows
+// cu[b] .. cu[b+1]-1 with positions restarting at 0.  The kernels are the
+// padded variable-length instantiations with the sequences' first rows
+// (cu) added: a unit's TMA coordinates start at its sequence's first row,
+// rows past the sequence inside its last tile are masked like padding and
+// stored row by row, so a tile never writes the next sequence's rows.
+// Workspace: [lengths int32 nseq][cu int32 nseq+1][forward units][dq
+// units][dk/dv units], each region 256-byte aligned, then (backward) the
+// backward workspace of a [1][total] batch.
+namespace {
+
+struct PackedLayout {
+    size_t off_cu, off_fwd, off_dq, off_dkv, tables, total;
+};
+
+PackedLayout packed_layout(int nseq, int total, int Hq, int Hkv, int d)
+{
+    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const int G = Hq / Hkv;
+    // live tiles per KV head: sum over sequences of ceil(L_b / 128) is at
+    // most floor(total / 128) + nseq
+    const size_t tiles = (static_cast<size_t>(total) / 128 + nseq) * Hkv;
+    const size_t nf = tiles * static_cast<size_t>(G / ne::fwd_heads_per_cta(d, G));
+    const size_t nq = tiles * static_cast<size_t>(G / ne::dq_heads_per_cta(d, G));
+    PackedLayout L;
+    L.off_cu = al(sizeof(int32_t) * static_cast<size_t>(nseq));
+    L.off_fwd = L.off_cu + al(sizeof(int32_t) * (static_cast<size_t>(nseq) + 1));
+    L.off_dq = L.off_fwd + al(sizeof(int32_t) * nf);
+    L.off_dkv = L.off_dq + al(sizeof(int32_t) * nq);
+    L.tables = L.off_dkv + al(sizeof(int32_t) * tiles);
+    L.total = L.tables + ne_attn_bwd_workspace_size(1, total, Hq, Hkv, d);
+    return L;
+}
+
+// Shape and cu_seqlens checks; on success *maxlen is the longest sequence.
+int check_packed(const int32_t *cu, int nseq, int total, int Hq, int Hkv, int d, float theta,
+                 int *maxlen)
+{
+    if (!cu)
+        return NE_ERR_NULL;
+    if (nseq < 1)
+        return NE_ERR_SHAPE;
+    int rc = check_shape(1, total, Hq, Hkv, d, theta);
+    if (rc != NE_OK)
+        return rc;
+    if (cu[0] != 0 || cu[nseq] != total)
+        return NE_ERR_ARG;
+    int mx = 0;
+    for (int b = 0; b < nseq; ++b) {
+        if (cu[b + 1] < cu[b])
+            return NE_ERR_ARG;
+        mx = std::max(mx, cu[b + 1] - cu[b]);
+    }
+    if ((rc = check_shape(nseq, mx > 0 ? mx : 1, Hq, Hkv, d, theta)) != NE_OK)
+        return rc;
+    *maxlen = mx;
+    return NE_OK;
+}
+
+// Builds [lengths][cu][tables] and copies it into the workspace on `st` (a
+// copy from pageable memory, staged before cudaMemcpyAsync returns).
+int upload_packed_tables(const int32_t *cu, int nseq, int maxlen, int Hq, int Hkv, int d,
+                         const PackedLayout &L, void *workspace, cudaStream_t st, int counts[3])
+{
+    const size_t w = sizeof(int32_t);
+    std::vector<int32_t> img(L.tables / w, 0);
+    for (int b = 0; b < nseq; ++b)
+        img[static_cast<size_t>(b)] = cu[b + 1] - cu[b];
+    std::memcpy(img.data() + L.off_cu / w, cu, w * (static_cast<size_t>(nseq) + 1));
+    const size_t caps[3] = {(L.off_dq - L.off_fwd) / w, (L.off_dkv - L.off_dq) / w,
+                            (L.tables - L.off_dkv) / w};
+    ne::varlen_plan(img.data(), nseq, maxlen > 0 ? maxlen : 1, Hq, Hkv, d, img.data() + L.off_fwd / w,
+                    img.data() + L.off_dq / w, img.data() + L.off_dkv / w, caps, counts);
+    for (int i = 0; i < 3; ++i)
+        if (static_cast<size_t>(counts[i]) > caps[i])
+            return NE_ERR_ARG;   // cannot happen: the regions bound every live unit
+    return cudaMemcpyAsync(workspace, img.data(), L.tables, cudaMemcpyHostToDevice, st) ==
+                   cudaSuccess
+               ? NE_OK
+               : NE_ERR_CUDA;
+}
+
+// The launch parameters of a packed batch's kernels: the sequence count as
+// the batch of the unit enumeration, the longest sequence's tiles as M, the
+// pack's rows as T.
+void set_packed(ne::AttnParams &p, void *workspace, const PackedLayout &L, int nseq, int maxlen)
+{
+    p.B = nseq;
+    p.M = (maxlen + 127) / 128;
+    p.seqlen = ws_int(workspace, 0);
+    p.cu = ws_int(workspace, L.off_cu);
+    p.nseq = nseq;
+}
+
+} // namespace
+
+extern "C" {
+
+size_t ne_attn_packed_workspace_size(int nseq, int total, int Hq, int Hkv, int d)
+{
+    if (nseq < 1 || check_shape(1, total, Hq, Hkv, d, 1.0f) != NE_OK)
+        return 0;
+    return packed_layout(nseq, total, Hq, Hkv, d).total;
+}
+
+int ne_attn_fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
+                       void *stream)
+{
+    if (!q || !k || !v || !o || !lse || !workspace)
+        return NE_ERR_NULL;
+    int maxlen = 0;
+    int rc = check_packed(cu_seqlens, nseq, total, Hq, Hkv, d, rope_theta, &maxlen);
+    if (rc != NE_OK)
+        return rc;
+    const PackedLayout L = packed_layout(nseq, total, Hq, Hkv, d);
+    if (workspace_bytes < L.tables)
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+        !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    if ((rc = device_state(&status)) != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ne::AttnParams p = base_params(1, total, Hq, Hkv, d, rope_theta, status);
+    p.GC = ne::fwd_heads_per_cta(d, p.G);
+    p.nchunks = p.G / p.GC;
+    p.out0 = o;
+    p.lse = lse;
+    p.q_in = q;
+    p.k_in = k;
+    CUtensorMap mq, mk, mv, mo;
+    if (make_map(&mq, q, 1, total, Hq, d) || make_map(&mk, k, 1, total, Hkv, d) ||
+        make_map(&mv, v, 1, total, Hkv, d) || make_map(&mo, o, 1, total, Hq, d))
+        return NE_ERR_CUDA;
+    int counts[3];
+    if ((rc = upload_packed_tables(cu_seqlens, nseq, maxlen, Hq, Hkv, d, L, workspace, st,
+                                   counts)) != NE_OK)
+        return rc;
+    set_packed(p, workspace, L, nseq, maxlen);
+    p.units = ws_int(workspace, L.off_fwd);
+    p.num_units = counts[0];
+    if (counts[0] > 0 && ne::launch_fwd(d, mq, mk, mv, mo, mq, mk, p, st) != cudaSuccess)
+        return NE_ERR_CUDA;
+    return NE_OK;
+}
+
+int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
+                       void *stream)
+{
+    if (!o || !dq || !dk || !dv || !workspace)
+        return NE_ERR_NULL;
+    int maxlen = 0;
+    int rc = check_packed(cu_seqlens, nseq, total, Hq, Hkv, d, rope_theta, &maxlen);
+    if (rc != NE_OK)
+        return rc;
+    const PackedLayout L = packed_layout(nseq, total, Hq, Hkv, d);
+    if (workspace_bytes < L.total)
+        return NE_ERR_WORKSPACE;
+    if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(workspace))
+        return NE_ERR_ALIGN;
+    void *bws = static_cast<uint8_t *>(workspace) + L.tables;
+    ne::AttnParams p;
+    CUtensorMap mq, mk, mv, mdo, mqr, mkr;
+    rc = bwd_setup(q, k, v, lse, dO, bws, workspace_bytes - L.tables, 1, total, Hq, Hkv, d,
+                   rope_theta, &p, &mq, &mk, &mv, &mdo, &mqr, &mkr);
+    if (rc != NE_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int counts[3];
+    if ((rc = upload_packed_tables(cu_seqlens, nseq, maxlen, Hq, Hkv, d, L, workspace, st,
+                                   counts)) != NE_OK)
+        return rc;
+    // the preprocess streams over the pack's rows (B = 1 in memory) and
+    // finds each row's position in its sequence through cu
+    p.o_in = o;
+    p.cu = ws_int(workspace, L.off_cu);
+    p.nseq = nseq;
+    void *qrot = static_cast<uint8_t *>(bws) + ws_d_bytes(1, total, Hq);
+    void *krot = static_cast<uint8_t *>(qrot) + ws_q_bytes(1, total, Hq, d);
+    if (ne::launch_bwd_pre(d, p, q, qrot, k, krot, st) != cudaSuccess)
+        return NE_ERR_CUDA;
+    set_packed(p, workspace, L, nseq, maxlen);
+    p.units = ws_int(workspace, L.off_dq);
+    p.num_units = counts[1];
+    if (counts[1] > 0 && (rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
+        return rc;
+    p.units = ws_int(workspace, L.off_dkv);
+    p.num_units = counts[2];
+    if (counts[2] > 0 && (rc = run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st)) != NE_OK)
+        return rc;
+    return NE_OK;
 }
 
 } // extern "C"

@@ -20,6 +20,51 @@ namespace ne {
 
 // ---------------------------------------------------------- preprocess ---
 
+// Partial sum of dO * O over one 16-byte chunk (8 elements) in a fixed
+// order.  D of a row is then the chunks' partials added pairwise by a
+// butterfly: chunk c with chunk c + D/16 first (one thread of bwd_pre_kernel,
+// or two lanes of bwd_d_kernel), then the shuffle levels; both kernels use
+// this order, so the standalone backward and the training pair get the same
+// D bit for bit.
+__device__ __forceinline__ float d_chunk(const uint4 &o4, const uint4 &g4)
+{
+    const uint32_t oa[4] = {o4.x, o4.y, o4.z, o4.w};
+    const uint32_t ga[4] = {g4.x, g4.y, g4.z, g4.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        acc = __fmaf_rn(bf16_hi(oa[e]), bf16_hi(ga[e]), __fmaf_rn(bf16_lo(oa[e]), bf16_lo(ga[e]), acc));
+    return acc;
+}
+
+// Position of row bt = b*T + t of the [B][T] row space, and whether it is a
+// valid row: plain batches, t; padded variable-length batches, t, valid if
+// t < seqlen[b]; packed batches (B = 1, cu set), the row's offset in its
+// sequence (cu[i] <= bt < cu[i+1], found by binary search; every row is in
+// one).
+struct RowPos {
+    uint32_t pos;
+    bool valid;
+};
+__device__ __forceinline__ RowPos row_pos(const AttnParams &p, size_t bt)
+{
+    if (p.cu != nullptr) {
+        int lo = 0, hi = p.nseq;   // cu[lo] <= bt < cu[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<size_t>(__ldg(p.cu + mid)) <= bt)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        return RowPos{static_cast<uint32_t>(bt - static_cast<size_t>(__ldg(p.cu + lo))), true};
+    }
+    const int t = static_cast<int>(bt % p.T);
+    if (p.seqlen != nullptr)
+        return RowPos{static_cast<uint32_t>(t), t < __ldg(p.seqlen + bt / p.T)};
+    return RowPos{static_cast<uint32_t>(t), true};
+}
+
 // One pass over the query-side rows (b, t, h), one thread per pair of
 // 16-byte chunks (c, c + D/16) of a row, so the thread holds rotate-half
 // partners:
@@ -30,6 +75,9 @@ namespace ne {
 //                once here instead of once per tile inside the loops)
 // Pure streaming over O, dO, q and k.  With qrot == nullptr (Q' and K' already
 // in the workspace, stored by the forward's training path) only D is computed.
+// Rows past a padded sequence's length are not read: their D is never used
+// (the kernels give such rows lse = +inf and D = 0) and their Q', K' rows are
+// written as zeros, so the tiles that straddle a sequence's end stay finite.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const uint4 *q,
                                                       uint4 *qrot, const uint4 *k, uint4 *krot)
@@ -49,22 +97,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
         float acc = 0.f;
         const size_t row = idx / TPR;                // ((b*T + t)*Hq + h)
         const int c = static_cast<int>(idx % TPR);
-        if (idx < nthreads) {
+        const RowPos rp = idx < nthreads ? row_pos(p, row / p.Hq) : RowPos{0u, false};
+        if (rp.valid) {
             const size_t c0 = row * CPR + c, c1 = c0 + TPR;
-            const uint4 oa = o[c0], ob = o[c1], ga = g[c0], gb = g[c1];
-            const uint32_t oav[4] = {oa.x, oa.y, oa.z, oa.w}, obv[4] = {ob.x, ob.y, ob.z, ob.w};
-            const uint32_t gav[4] = {ga.x, ga.y, ga.z, ga.w}, gbv[4] = {gb.x, gb.y, gb.z, gb.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc += bf16_lo(oav[e]) * bf16_lo(gav[e]) + bf16_hi(oav[e]) * bf16_hi(gav[e]);
-                acc += bf16_lo(obv[e]) * bf16_lo(gbv[e]) + bf16_hi(obv[e]) * bf16_hi(gbv[e]);
-            }
+            // chunks c and c + D/16: each chunk's partial sum, then the pair
+            // (the same order as bwd_d_kernel, so both give the same bits)
+            acc = d_chunk(o[c0], g[c0]) + d_chunk(o[c1], g[c1]);
         }
         if (idx < nthreads && qrot != nullptr) {
             const size_t c0 = row * CPR + c, c1 = c0 + TPR;
-            const uint4 qa = q[c0], qb = q[c1];
+            const uint4 qa = rp.valid ? q[c0] : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 qb = rp.valid ? q[c1] : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t qav[4] = {qa.x, qa.y, qa.z, qa.w}, qbv[4] = {qb.x, qb.y, qb.z, qb.w};
-            const uint32_t t = static_cast<uint32_t>((row / p.Hq) % p.T);
+            const uint32_t t = rp.pos;
             uint32_t ra[4], rb[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -75,8 +120,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
                     rope_sincos(t, p.rope, 8 * c + 2 * e + hh, sn, cs);
                     const float x = hh ? bf16_hi(qav[e]) : bf16_lo(qav[e]);
                     const float y = hh ? bf16_hi(qbv[e]) : bf16_lo(qbv[e]);
-                    u[hh] = x * cs - y * sn;
-                    w[hh] = y * cs + x * sn;
+                    rope_rotate(x, y, cs, sn, u[hh], w[hh]);
                     mx = fmaxf(mx, fmaxf(fabsf(u[hh]), fabsf(w[hh])));
                 }
                 ra[e] = pack_f16x2(u[0], u[1]);
@@ -88,7 +132,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
 #pragma unroll
         for (int off = TPR / 2; off >= 1; off /= 2)
             acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (idx < nthreads && c == 0) {
+        if (rp.valid && c == 0) {
             const int h = static_cast<int>(row % p.Hq);
             const size_t bt = row / p.Hq;
             const int t = static_cast<int>(bt % p.T);
@@ -103,9 +147,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
         const size_t row = idx / TPR;                // ((b*T + s)*Hkv + j)
         const int c = static_cast<int>(idx % TPR);
         const size_t c0 = row * CPR + c, c1 = c0 + TPR;
-        const uint4 ka = k[c0], kb = k[c1];
+        const RowPos rp = row_pos(p, row / p.Hkv);
+        const uint4 ka = rp.valid ? k[c0] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 kb = rp.valid ? k[c1] : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t kav[4] = {ka.x, ka.y, ka.z, ka.w}, kbv[4] = {kb.x, kb.y, kb.z, kb.w};
-        const uint32_t pos = static_cast<uint32_t>((row / p.Hkv) % p.T);
+        const uint32_t pos = rp.pos;
         uint32_t ra[4], rb[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -116,8 +162,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
                 rope_sincos(pos, p.rope, 8 * c + 2 * e + hh, sn, cs);
                 const float x = hh ? bf16_hi(kav[e]) : bf16_lo(kav[e]);
                 const float y = hh ? bf16_hi(kbv[e]) : bf16_lo(kbv[e]);
-                u[hh] = x * cs - y * sn;
-                w[hh] = y * cs + x * sn;
+                rope_rotate(x, y, cs, sn, u[hh], w[hh]);
                 mx = fmaxf(mx, fmaxf(fabsf(u[hh]), fabsf(w[hh])));
             }
             ra[e] = pack_f16x2(u[0], u[1]);
@@ -167,12 +212,7 @@ __global__ void __launch_bounds__(256, kDCtasPerSm) bwd_d_kernel(const AttnParam
         }
 #pragma unroll
         for (int i = 0; i < RU; ++i) {
-            const uint32_t oa[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
-            const uint32_t ga[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-            float acc = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc = fmaf(bf16_hi(oa[e]), bf16_hi(ga[e]), fmaf(bf16_lo(oa[e]), bf16_lo(ga[e]), acc));
+            float acc = d_chunk(ov[i], gv[i]);
 #pragma unroll
             for (int off = LPR / 2; off >= 1; off /= 2)
                 acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -352,6 +392,7 @@ struct DqCfg {
 struct DqUnit {
     int m, b, j, h0, lo;   // lo: first key tile (sliding window; 0 otherwise)
     int tl;                // valid rows of sequence b (varlen; T otherwise)
+    SeqLoc sq;             // where sequence b's rows live
 };
 
 // VAR: u indexes the launch's table of live units (padded variable-length
@@ -371,7 +412,8 @@ __device__ __forceinline__ DqUnit dq_unit(int u, int GC, const AttnParams &p)
     w.b = rem / p.Hkv;
     w.h0 = w.j * p.G + chunk * GC;
     w.lo = key_tile_lo(w.m, p.window);
-    w.tl = VAR ? __ldg(p.seqlen + w.b) : p.T;
+    w.sq = seq_loc<VAR>(p, w.b);
+    w.tl = w.sq.len;
     return w;
 }
 
@@ -472,9 +514,11 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive_expect_tx(qb, 2 * TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb) {
                         tma_load_4d(smem_u32(smem + C::OFF_Q + g * TL::BYTES + cb * TL::BLOCK),
-                                    &tmQ, qb, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                                    &tmQ, qb, cb * TL::BOX_COLS, w.h0 + g,
+                                    w.sq.base + w.m * kRows, w.sq.bc);
                         tma_load_4d(smem_u32(smem + C::OFF_DO + g * TL::BYTES + cb * TL::BLOCK),
-                                    &tmDO, qb, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                                    &tmDO, qb, cb * TL::BOX_COLS, w.h0 + g,
+                                    w.sq.base + w.m * kRows, w.sq.bc);
                     }
                 }
                 for (int jk = w.lo; jk <= w.m && ok; ++jk, ++kt) {
@@ -487,9 +531,11 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive_expect_tx(kb, 2 * TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb) {
                         tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmK, kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                                    &tmK, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
+                                    w.sq.bc);
                         tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmV, kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                                    &tmV, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
+                                    w.sq.bc);
                     }
                 }
             }
@@ -619,10 +665,11 @@ __global__ void __launch_bounds__(384, 1)
             return;
         const DqUnit un = dq_unit<VAR>(u, GC, p);
         const int t = un.m * kRows + r;
-        if (t < (VAR ? un.tl : p.T)) {
+        if (t < un.tl) {
 #pragma unroll
             for (int g = 0; g < GC; ++g) {
-                const size_t idx = (static_cast<size_t>(un.b) * p.Hq + un.h0 + g) * p.T + t;
+                const size_t idx =
+                    (static_cast<size_t>(un.sq.bc) * p.Hq + un.h0 + g) * p.T + un.sq.base + t;
                 l2[g] = p.lse[idx] * kLog2e;
                 dd[g] = p.Dws[idx];
             }
@@ -653,10 +700,22 @@ __global__ void __launch_bounds__(384, 1)
             for (int e = 0; e < D / 2; ++e)
                 rope_sincos(static_cast<uint32_t>(t), p.rope, e, sn[e], cs[e]);
         }
+        // the last tile of a packed sequence goes out row by row: a tile
+        // store would overwrite the next sequence's first rows
+        const bool direct = VAR && p.cu != nullptr && (pend.m + 1) * kRows > pend.tl;
+        auto store_direct = [&](int g) {
+            __nv_bfloat16 *row = dq + (seq_row(p, pend.sq, t) * p.Hq + pend.h0 + g) * D;
+            epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
+                                     static_cast<uint32_t>(t), p.rope, row, t < pend.tl);
+        };
 #pragma unroll
         for (int g = 0; g < GC; ++g)
             if ((g & 1) == w) {
                 if constexpr (C::STAGE) {
+                    if (direct) {
+                        store_direct(g);
+                        continue;
+                    }
                     // the staging block is free once this group's previous
                     // store has read it
                     if (nepi >= 1) {
@@ -677,18 +736,15 @@ __global__ void __launch_bounds__(384, 1)
                         if (!mbar_wait_warp(smem_u32(&bar_stg_full[w]), nepi & 1, wc))
                             return false;
                         if (lane == 0) {
-                            tma_store_4d(&tmDQ, smem_u32(stage), 0, pend.h0 + g, pend.m * kRows,
-                                         pend.b);
+                            tma_store_4d(&tmDQ, smem_u32(stage), 0, pend.h0 + g,
+                                         pend.sq.base + pend.m * kRows, pend.sq.bc);
                             bulk_commit();
                         }
                         __syncwarp();
                     }
                     ++nepi;
                 } else {
-                    __nv_bfloat16 *row =
-                        dq + ((static_cast<size_t>(pend.b) * p.T + t) * p.Hq + pend.h0 + g) * D;
-                    epilogue_inverse_rope<D>(lane_base + C::COL_DQ + g * D, p.scale,
-                                             static_cast<uint32_t>(t), p.rope, row, t < p.T);
+                    store_direct(g);
                 }
             }
         tc_fence_before();
@@ -863,6 +919,7 @@ struct DkvCfg {
 struct DkvUnit {
     int n, b, j, nitems;
     int tl;                // valid rows of sequence b (varlen; T otherwise)
+    SeqLoc sq;             // where sequence b's rows live
 };
 
 // VAR: u indexes the launch's table of live units (padded variable-length
@@ -878,7 +935,8 @@ __device__ __forceinline__ DkvUnit dkv_unit(int u, const AttnParams &p)
     const int rem = u % per_n;
     w.j = rem % p.Hkv;
     w.b = rem / p.Hkv;
-    w.tl = VAR ? __ldg(p.seqlen + w.b) : p.T;
+    w.sq = seq_loc<VAR>(p, w.b);
+    w.tl = w.sq.len;
     const int mtiles = VAR ? (w.tl + kRows - 1) / kRows : p.M;
     w.nitems = (query_tile_hi(w.n, p.window, mtiles) - w.n + 1) * p.G;
     return w;
@@ -991,11 +1049,11 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive_expect_tx(kbar, TL::BYTES);
                 for (int cb = 0; cb < TL::NB; ++cb)
                     tma_load_4d(smem_u32(smem + C::OFF_K + kb * TL::BYTES + cb * TL::BLOCK), &tmK,
-                                kbar, cb * TL::BOX_COLS, w.j, w.n * kRows, w.b);
+                                kbar, cb * TL::BOX_COLS, w.j, w.sq.base + w.n * kRows, w.sq.bc);
                 mbar_arrive_expect_tx(vbar, TL::BYTES);
                 for (int cb = 0; cb < TL::NB; ++cb)
                     tma_load_4d(smem_u32(smem + C::OFF_V + kb * TL::BYTES + cb * TL::BLOCK), &tmV,
-                                vbar, cb * TL::BOX_COLS, w.j, w.n * kRows, w.b);
+                                vbar, cb * TL::BOX_COLS, w.j, w.sq.base + w.n * kRows, w.sq.bc);
                 for (int it = 0; it < w.nitems; ++it, ++gi) {
                     const int st = gi % ST, su = gi / ST;
                     if (su >= 1 && !mbar_wait(smem_u32(&bar_st_empty[st]), (su - 1) & 1, wc)) {
@@ -1007,11 +1065,13 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_arrive_expect_tx(qb, TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb)
                         tma_load_4d(smem_u32(smem + C::OFF_Q + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmQ, qb, cb * TL::BOX_COLS, h, mt * kRows, w.b);
+                                    &tmQ, qb, cb * TL::BOX_COLS, h, w.sq.base + mt * kRows,
+                                    w.sq.bc);
                     mbar_arrive_expect_tx(db, TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb)
                         tma_load_4d(smem_u32(smem + C::OFF_DO + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmDO, db, cb * TL::BOX_COLS, h, mt * kRows, w.b);
+                                    &tmDO, db, cb * TL::BOX_COLS, h, w.sq.base + mt * kRows,
+                                    w.sq.bc);
                 }
             }
             if (*wc.abort) {
@@ -1177,8 +1237,9 @@ __global__ void __launch_bounds__(512, 1)
                 const int t = mt * kRows + r;
                 l = INFINITY;
                 dd = 0.f;
-                if (t < (VAR ? w.tl : p.T)) {
-                    const size_t idx = (static_cast<size_t>(w.b) * p.Hq + h) * p.T + t;
+                if (t < w.tl) {
+                    const size_t idx =
+                        (static_cast<size_t>(w.sq.bc) * p.Hq + h) * p.T + w.sq.base + t;
                     l = p.lse[idx];
                     dd = p.Dws[idx];
                 }
@@ -1229,7 +1290,7 @@ __global__ void __launch_bounds__(512, 1)
                 return false;
             tc_fence_after();
             const int s = pend.n * kRows + r;
-            const size_t rowoff = ((static_cast<size_t>(pend.b) * p.T + s) * p.Hkv + pend.j) * D;
+            const size_t rowoff = (seq_row(p, pend.sq, s) * p.Hkv + pend.j) * D;
             if (w == 0) {
                 __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(p.out1) + rowoff;
 #pragma unroll
@@ -1241,13 +1302,13 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         x[e] = __uint_as_float(a[e]);
-                    if (s < p.T)
+                    if (s < pend.tl)
                         store_row32_bf16(dv + cc * 32, x);
                 }
             } else {
                 __nv_bfloat16 *dkp = static_cast<__nv_bfloat16 *>(p.out0) + rowoff;
                 epilogue_inverse_rope<D>(lane_base + C::COL_DK, p.scale, static_cast<uint32_t>(s),
-                                         p.rope, dkp, s < p.T);
+                                         p.rope, dkp, s < pend.tl);
             }
             tc_fence_before();
             __syncwarp();

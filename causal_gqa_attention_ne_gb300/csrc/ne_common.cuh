@@ -114,6 +114,18 @@ __device__ __forceinline__ void rope_sincos(uint32_t pos, const RopeFreqs &fr, i
     __sincosf(ang, &s, &c);
 }
 
+// One rotate-half pair (x, y) rotated by the angle with cosine c and sine s:
+// (x c - y s, y c + x s).  The operations are rounded explicitly (one
+// product, then a fused multiply-add), so the forward, the backward's
+// preprocess and the exact-score path produce the same bits for the same
+// input, whatever contractions the compiler would choose in each kernel.
+__device__ __forceinline__ void rope_rotate(float x, float y, float c, float s, float &u,
+                                            float &w)
+{
+    u = __fmaf_rn(x, c, -__fmul_rn(y, s));
+    w = __fmaf_rn(y, c, __fmul_rn(x, s));
+}
+
 // Rotate row r of a bf16 tile in place to fp16 with the hardware sine/cosine
 // per pair, loading a batch of up to four chunk pairs before computing so the
 // shared-memory and special-function latencies overlap.  Returns max |x'|
@@ -148,8 +160,7 @@ __device__ __forceinline__ float rope_row_ilp(uint8_t *tile, int r, uint32_t pos
                     rope_sincos(pos, fr, 8 * (c0 + i) + 2 * e + h, sn, cs);
                     const float x = h ? bf16_hi(av[e]) : bf16_lo(av[e]);
                     const float y = h ? bf16_hi(bv[e]) : bf16_lo(bv[e]);
-                    u[h] = x * cs - y * sn;
-                    w[h] = y * cs + x * sn;
+                    rope_rotate(x, y, cs, sn, u[h], w[h]);
                     mx = fmaxf(mx, fmaxf(fabsf(u[h]), fabsf(w[h])));
                     ss = fmaf(u[h], u[h], fmaf(w[h], w[h], ss));
                 }
@@ -292,8 +303,39 @@ struct AttnParams {
     // of them) and the valid length of every sequence, both in device memory
     const int *units;
     const int *seqlen;
+    // packed variable-length batches (varlen instantiations with cu set):
+    // the sequences are concatenated along the rows of one batch entry
+    // (B = 1 in memory, T = the total row count), sequence b starting at row
+    // cu[b]; the launch's B is the sequence count
+    const int *cu;
+    int nseq;                    // packed: the number of sequences (cu has nseq + 1 entries)
     RopeFreqs rope;
 };
+
+// Where sequence b of a launch lives: the TMA batch coordinate bc and first
+// row base of its rows, and its valid rows len.  Plain and padded batches:
+// bc = b, base = 0 (len = T, or the sequence's length); packed batches:
+// bc = 0, base = cu[b].
+struct SeqLoc {
+    int bc, base, len;
+};
+template <bool VAR>
+__device__ __forceinline__ SeqLoc seq_loc(const AttnParams &p, int b)
+{
+    if constexpr (VAR) {
+        const int len = __ldg(p.seqlen + b);
+        if (p.cu != nullptr)
+            return SeqLoc{0, __ldg(p.cu + b), len};
+        return SeqLoc{b, 0, len};
+    }
+    return SeqLoc{b, 0, p.T};
+}
+
+// Row t of a sequence in the [B][T] row space of a tensor (T = p.T).
+__device__ __forceinline__ size_t seq_row(const AttnParams &p, const SeqLoc &s, int t)
+{
+    return static_cast<size_t>(s.bc) * p.T + s.base + t;
+}
 
 // Sliding window: the first key tile any row of query tile m sees (0 without
 // a window: its first row t = 128 m sees keys >= t - W + 1), and the last

@@ -38,6 +38,7 @@
 // buffers per group (bf16 pairs, columns 128-255), then the groups' O
 // accumulators (COL_O + (w*NSL + slot)*D).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ne_common.cuh"
 #include "ne_kernels.h"
@@ -58,8 +59,8 @@ struct FwdPlan {
     static constexpr int QB = (D <= 64) ? 2 : 1;
     // large-norm rows scored exactly per Q tile and per K tile
     static constexpr int NOUT = (D == 64) ? 2 : 4;
-    static constexpr int BALLOT_BYTES = 256;                    // [QB][GC][4] + [4] words
-    static constexpr int QOV_BYTES = QB * GC * NOUT * D * 4;    // exact q' of large rows
+    static constexpr int BALLOT_BYTES = 256;                    // [2][GC][4] + [ST][4] words
+    static constexpr int QOV_BYTES = 2 * GC * NOUT * D * 4;     // exact q' of large rows
     static constexpr int KOV_BYTES = NOUT * D * 4;              // exact k' of large rows
     static constexpr int PHDR_BYTES = 256;                      // counts and row indices
     // per stage: header, then dS_k [NOUT][GC][128] and dS_q [GC][NOUT][128] (fp16)
@@ -92,10 +93,10 @@ struct FwdCfg {
     static constexpr int OFF_O = OFF_V + ST * TL::BYTES;      // [2] staging blocks
     // group 1's running max and sum of the split head: float [2][128]
     static constexpr int OFF_SPL = OFF_O + (STAGE ? 2 * TL::BLOCK : 0);
-    // uint32 ballots of large rows: Q slots [QB][GC][4 warps], then the
-    // current K tile [4 warps]
+    // uint32 ballots of large rows (one word per RoPE warp): the Q tiles of
+    // units of each parity [2][GC][4], then the K stages [ST][4]
     static constexpr int OFF_BAL = OFF_SPL + 2 * kRows * 4;
-    static constexpr int OFF_QOV = OFF_BAL + PL::BALLOT_BYTES;   // float [QB][GC][NOUT][D]
+    static constexpr int OFF_QOV = OFF_BAL + PL::BALLOT_BYTES;   // float [2][GC][NOUT][D]
     static constexpr int OFF_KOV = OFF_QOV + PL::QOV_BYTES;      // float [NOUT][D]
     static constexpr int OFF_PREC = OFF_KOV + PL::KOV_BYTES;     // [ST] patch records
     static constexpr int SMEM_BYTES = smem_one_cta(OFF_PREC + ST * PL::PREC_BYTES + 1024);
@@ -109,7 +110,7 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448 - 1024, "shared memory budget");
     static_assert(ST >= 2, "K/V double buffering");
     static_assert(!STAGE || TL::NB == 1, "staged epilogue stores one column block per head");
-    static_assert(QB * GC * 4 * 4 + 16 <= PL::BALLOT_BYTES, "ballot words");
+    static_assert(2 * GC * 4 * 4 + ST * 4 * 4 <= PL::BALLOT_BYTES, "ballot words");
     static_assert(4 * (1 + NOUT + GC + GC * NOUT) <= PL::PHDR_BYTES, "patch record header");
 };
 
@@ -132,6 +133,7 @@ struct PatchHdr {
 
 struct FwdUnit {
     int m, b, j, h0, lo;   // lo: first key tile (sliding window; 0 otherwise)
+    SeqLoc sq;             // where sequence b's rows live
 };
 
 // VAR: u indexes the launch's table of live units (padded variable-length
@@ -151,7 +153,242 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
     w.b = rem / p.Hkv;
     w.h0 = w.j * p.G + chunk * GC;
     w.lo = key_tile_lo(w.m, p.window);
+    w.sq = seq_loc<VAR>(p, w.b);
     return w;
+}
+
+
+// ---------------------------------------------- exact scores of large rows ---
+
+// The rotated row of the bf16 vector at `row` (global memory) in fp32:
+// f(i, x'_i, x'_{i + D/2}) for every rotate-half pair i, position pos.  One
+// pair per iteration, so the few registers of the RoPE warps suffice (this
+// runs only for tiles with large rows).
+template <int D, typename F>
+__device__ __forceinline__ void exact_pairs(const __nv_bfloat16 *row, uint32_t pos,
+                                            const RopeFreqs &fr, F &&f)
+{
+#pragma unroll 1
+    for (int i = 0; i < D / 2; ++i) {
+        float sn, cs;
+        rope_sincos(pos, fr, i, sn, cs);
+        const float x = __bfloat162float(row[i]);
+        const float y = __bfloat162float(row[i + D / 2]);
+        float u, w;
+        rope_rotate(x, y, cs, sn, u, w);
+        f(i, u, w);
+    }
+}
+
+// Element (r, col) of a rotated fp16 tile in shared memory.
+template <int D>
+__device__ __forceinline__ float tile_f16(const uint8_t *tile, int r, int col)
+{
+    return __half2float(
+        *reinterpret_cast<const __half *>(tile + tile_chunk<D>(r, col >> 3) + (col & 7) * 2));
+}
+
+// Row index (32 w + lane) of the o-th set bit of four ballot words, in
+// increasing row order; -1 if there are not that many.
+__device__ __forceinline__ int nth_row(const uint32_t *bal, int o)
+{
+    for (int w = 0; w < 4; ++w) {
+        uint32_t m = bal[w];
+        const int c = __popc(m);
+        if (o < c) {
+            for (int i = 0; i < o; ++i)
+                m &= m - 1u;
+            return 32 * w + __ffs(m) - 1;
+        }
+        o -= c;
+    }
+    return -1;
+}
+
+// Rank of row r among the set bits of four ballot words (rows below it), or
+// -1 if its bit is clear.
+__device__ __forceinline__ int row_rank(const uint32_t *bal, int r)
+{
+    const int wr = r >> 5;
+    if (!((bal[wr] >> (r & 31)) & 1u))
+        return -1;
+    int rank = __popc(bal[wr] & ((1u << (r & 31)) - 1u));
+    for (int i = 0; i < wr; ++i)
+        rank += __popc(bal[i]);
+    return rank;
+}
+
+// Builds the patch record of K stage st (key tile jk of unit w, whose Q
+// tiles sit in slot qslot and whose ballots are those of unit parity up).
+// Runs in all 128 threads of the RoPE warpgroup after the ballots of the K
+// tile are visible; thread r stands for query row r of the Q tiles and key
+// row r of the K tile.  Without large rows it only clears the counts.
+template <int D, int GC, int ST, bool VAR, typename Sync>
+__device__ __forceinline__ bool patch_tile(uint8_t *smem, int r, int st, int jk, const FwdUnit &w,
+                                        int qslot, int up, const uint32_t *qbal,
+                                        const uint32_t *kbal, const AttnParams &p, Sync &rsync)
+{
+    using C = FwdCfg<D, GC, ST>;
+    using TL = Tile<D>;
+    constexpr int NOUT = C::NOUT;
+    uint8_t *rec = smem + C::OFF_PREC + st * C::PL::PREC_BYTES;
+    PatchHdr *hdr = reinterpret_cast<PatchHdr *>(rec);
+    __half *dk = reinterpret_cast<__half *>(rec + C::PL::PHDR_BYTES);   // [NOUT][GC][128]
+    __half *dq = dk + NOUT * GC * kRows;                               // [GC][NOUT][128]
+    const uint32_t *kb = kbal + st * 4;
+    const uint32_t *qb0 = qbal + up * GC * 4;
+    const int nk = __popc(kb[0]) + __popc(kb[1]) + __popc(kb[2]) + __popc(kb[3]);
+    int anyq = 0, overq = 0;
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        const uint32_t *qg = qb0 + g * 4;
+        const int n = __popc(qg[0]) + __popc(qg[1]) + __popc(qg[2]) + __popc(qg[3]);
+        anyq |= n;
+        overq |= n > NOUT ? 1 : 0;
+    }
+    if (nk == 0 && anyq == 0) {
+        if (r == 0) {
+            hdr->kcnt = 0;
+#pragma unroll
+            for (int g = 0; g < GC; ++g)
+                hdr->qcnt[g] = 0;
+        }
+        return true;
+    }
+    // ---- a tile with large rows: exact scores for their pairs ----
+    const int kc = nk < NOUT ? nk : NOUT;
+    if (r == 0 && (nk > NOUT || overq))
+        atomicOr(p.status, kDevPrecision);
+    const uint8_t *ktile = smem + C::OFF_K + st * TL::BYTES;
+    float *kov = reinterpret_cast<float *>(smem + C::OFF_KOV);                        // [NOUT][D]
+    float *qov = reinterpret_cast<float *>(smem + C::OFF_QOV) + up * GC * NOUT * D;   // [GC][NOUT][D]
+    const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(p.q_in);
+    const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(p.k_in);
+    const int t = w.m * kRows + r;   // this thread's query row
+    const int s = jk * kRows + r;    // this thread's key row
+    const __nv_bfloat16 *krow = kin + (seq_row(p, w.sq, s) * p.Hkv + w.j) * D;
+    auto qrow_ptr = [&](int g) { return qin + (seq_row(p, w.sq, t) * p.Hq + w.h0 + g) * D; };
+    // 1. the owners of large rows write their exact rotated vectors
+    const int krank = row_rank(kb, r);
+    if (krank >= 0 && krank < NOUT)
+        exact_pairs<D>(krow, static_cast<uint32_t>(s), p.rope, [&](int i, float x, float y) {
+            kov[krank * D + i] = x;
+            kov[krank * D + i + D / 2] = y;
+        });
+#pragma unroll 1
+    for (int g = 0; g < GC; ++g) {
+        const int qrank = row_rank(qb0 + g * 4, r);
+        if (qrank >= 0 && qrank < NOUT) {
+            float *dst = qov + (g * NOUT + qrank) * D;
+            exact_pairs<D>(qrow_ptr(g), static_cast<uint32_t>(t), p.rope,
+                           [&](int i, float x, float y) {
+                               dst[i] = x;
+                               dst[i + D / 2] = y;
+                           });
+        }
+    }
+    if (!rsync())
+        return false;
+    if (r == 0) {
+        hdr->kcnt = kc;
+        for (int o = 0; o < kc; ++o)
+            hdr->kcol[o] = nth_row(kb, o);
+        for (int g = 0; g < GC; ++g) {
+            const uint32_t *qg = qb0 + g * 4;
+            const int n = __popc(qg[0]) + __popc(qg[1]) + __popc(qg[2]) + __popc(qg[3]);
+            hdr->qcnt[g] = n < NOUT ? n : NOUT;
+            for (int o = 0; o < NOUT && o < n; ++o)
+                hdr->qrow[g][o] = nth_row(qg, o);
+        }
+    }
+    float dmax = 0.f;
+    // 2. pairs (query row r, large key o), every head: the exact score minus
+    //    the product of the fp16 operands the tensor cores see.  One pair
+    //    list entry at a time, so few registers stay live.
+#pragma unroll 1
+    for (int g = 0; g < GC; ++g) {
+        const uint8_t *qtile = smem + C::OFF_Q + (qslot * GC + g) * TL::BYTES;
+#pragma unroll 1
+        for (int o = 0; o < kc; ++o) {
+            const int kr = nth_row(kb, o);
+            const float *kv = kov + o * D;
+            float ae = 0.f, ah = 0.f;
+            if (t < w.sq.len)
+                exact_pairs<D>(qrow_ptr(g), static_cast<uint32_t>(t), p.rope,
+                               [&](int i, float x, float y) {
+                                   ae = fmaf(x, kv[i], fmaf(y, kv[i + D / 2], ae));
+                                   ah = fmaf(tile_f16<D>(qtile, r, i), tile_f16<D>(ktile, kr, i),
+                                             fmaf(tile_f16<D>(qtile, r, i + D / 2),
+                                                  tile_f16<D>(ktile, kr, i + D / 2), ah));
+                               });
+            dmax = fmaxf(dmax, fabsf(ae - ah));
+            dk[(o * GC + g) * kRows + r] = __float2half_rn(ae - ah);
+        }
+    }
+    // 3. pairs (large query row o of head g, key row r); a key that is itself
+    //    corrected in step 2 gets 0 here, so no pair is corrected twice
+    const bool key_patched = krank >= 0 && krank < NOUT;
+#pragma unroll 1
+    for (int g = 0; g < GC; ++g) {
+        const uint32_t *qg = qb0 + g * 4;
+        const int n = __popc(qg[0]) + __popc(qg[1]) + __popc(qg[2]) + __popc(qg[3]);
+        const int qc = n < NOUT ? n : NOUT;
+        const uint8_t *qtile = smem + C::OFF_Q + (qslot * GC + g) * TL::BYTES;
+#pragma unroll 1
+        for (int o = 0; o < qc; ++o) {
+            const int qr = nth_row(qg, o);
+            const float *qv = qov + (g * NOUT + o) * D;
+            float ae = 0.f, ah = 0.f;
+            if (s < w.sq.len && !key_patched)
+                exact_pairs<D>(krow, static_cast<uint32_t>(s), p.rope,
+                               [&](int i, float x, float y) {
+                                   ae = fmaf(x, qv[i], fmaf(y, qv[i + D / 2], ae));
+                                   ah = fmaf(tile_f16<D>(ktile, r, i), tile_f16<D>(qtile, qr, i),
+                                             fmaf(tile_f16<D>(ktile, r, i + D / 2),
+                                                  tile_f16<D>(qtile, qr, i + D / 2), ah));
+                               });
+            dmax = fmaxf(dmax, fabsf(ae - ah));
+            dq[(g * NOUT + o) * kRows + r] = __float2half_rn(ae - ah);
+        }
+    }
+    if (dmax > kFp16Max)
+        atomicOr(p.status, kDevRange);
+    return true;
+}
+
+// Adds a K stage's exact-score corrections to the 64 raw scores a softmax
+// thread holds for query row r and key half `half` of head hrel: the column
+// of every large key row in this half, and every column if r is a large
+// query row of that head.
+template <int NOUT, int GC>
+__device__ __forceinline__ void apply_patches(uint32_t (&s)[2][32], const uint8_t *deltas,
+                                              const PatchHdr *hdr, int kc, int qc, int hrel,
+                                              int half, int r)
+{
+    const __half *dk = reinterpret_cast<const __half *>(deltas);   // [NOUT][GC][128]
+    const __half *dq = dk + NOUT * GC * kRows;                     // [GC][NOUT][128]
+    for (int o = 0; o < kc; ++o) {
+        const int col = hdr->kcol[o] - 64 * half;
+        if (col < 0 || col >= 64)
+            continue;
+        const float d = __half2float(dk[(o * GC + hrel) * kRows + r]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (32 * c + e == col)
+                    s[c][e] = __float_as_uint(__uint_as_float(s[c][e]) + d);
+    }
+    for (int o = 0; o < qc; ++o) {
+        if (hdr->qrow[hrel][o] != r)
+            continue;
+        const __half *row = dq + (hrel * NOUT + o) * kRows + 64 * half;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                s[c][e] = __float_as_uint(__uint_as_float(s[c][e]) + __half2float(row[32 * c + e]));
+    }
 }
 
 // WIN: a sliding window may mask keys off the diagonal tile (compiled out of
@@ -185,6 +422,9 @@ __global__ void __launch_bounds__(512, 1)
     // release a Q slot or a stored K stage before it is reloaded), and warp
     // 15's store has read a Q slot / K stage
     __shared__ uint64_t bar_sv[16], bar_q_rd[QB][GC], bar_k_rd[ST];
+    // patch record of stage st written (four RoPE warps); barrier of the RoPE
+    // warpgroup for the exact-score path
+    __shared__ uint64_t bar_patch[ST], bar_rsync;
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
 
@@ -207,7 +447,9 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(smem_u32(&bar_v_full[s]), 1);
             mbar_init(smem_u32(&bar_kv_empty[s]), 2);
             mbar_init(smem_u32(&bar_k_rd[s]), 1);
+            mbar_init(smem_u32(&bar_patch[s]), 4);
         }
+        mbar_init(smem_u32(&bar_rsync), 4);
         for (int w = 0; w < 2; ++w) {
             mbar_init(smem_u32(&bar_s_full[w]), 1);
             mbar_init(smem_u32(&bar_s_empty[w]), 4);
@@ -285,7 +527,8 @@ __global__ void __launch_bounds__(512, 1)
                         for (int cb = 0; cb < TL::NB; ++cb)
                             tma_load_4d(smem_u32(smem + C::OFF_Q + (qb * GC + g) * TL::BYTES +
                                                  cb * TL::BLOCK),
-                                        &tmQ, bar, cb * TL::BOX_COLS, w.h0 + g, w.m * kRows, w.b);
+                                        &tmQ, bar, cb * TL::BOX_COLS, w.h0 + g,
+                                        w.sq.base + w.m * kRows, w.sq.bc);
                     }
                     __syncwarp();
                     ++qloads[qb][g];
@@ -311,11 +554,13 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_arrive_expect_tx(kb, TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb)
                         tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmK, kb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                                    &tmK, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
+                                    w.sq.bc);
                     mbar_arrive_expect_tx(vb, TL::BYTES);
                     for (int cb = 0; cb < TL::NB; ++cb)
                         tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmV, vb, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                                    &tmV, vb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
+                                    w.sq.bc);
                 }
                 __syncwarp();
                 ++kt;
@@ -392,9 +637,10 @@ __global__ void __launch_bounds__(512, 1)
                             const uint32_t src = smem_u32(tile + cb * TL::BLOCK);
                             if (isq)
                                 tma_store_4d(&tmQs, src, cb * TL::BOX_COLS, wq.h0 + g,
-                                             wq.m * kRows, wq.b);
+                                             wq.sq.base + wq.m * kRows, wq.sq.bc);
                             else
-                                tma_store_4d(&tmKs, src, cb * TL::BOX_COLS, w.j, jk * kRows, w.b);
+                                tma_store_4d(&tmKs, src, cb * TL::BOX_COLS, w.j,
+                                             w.sq.base + jk * kRows, w.sq.bc);
                         }
                         bulk_commit();
                         bulk_wait_read0();
@@ -525,10 +771,23 @@ __global__ void __launch_bounds__(512, 1)
         // ------------------------------------------------------ RoPE ---
         regs_release<80>();
         const int r = threadIdx.x - 256;
+        const int rw = warp - 8;              // warp within the RoPE warpgroup
+        uint32_t *qbal = reinterpret_cast<uint32_t *>(smem + C::OFF_BAL);   // [2][GC][4]
+        uint32_t *kbal = qbal + 2 * GC * 4;                                  // [ST][4]
         float mx = 0.f;
         bool ok = true;
         int kt = 0;
-        uint32_t nsv = 0;   // tiles handed to warp 15 (training path)
+        uint32_t nsv = 0;     // tiles handed to warp 15 (training path)
+        uint32_t nsync = 0;   // uses of bar_rsync
+        // bounded barrier of the four RoPE warps (all take the same path)
+        auto rsync = [&]() {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&bar_rsync));
+            const bool r_ok = mbar_wait_warp(smem_u32(&bar_rsync), nsync & 1, wc);
+            ++nsync;
+            return r_ok;
+        };
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
@@ -540,7 +799,7 @@ __global__ void __launch_bounds__(512, 1)
             const int nq0 = (QB == 1 || k == 0) ? GC : 0;
             const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
             const int nq1 = has_next ? GC : 0;
-            const int mnext = has_next ? fwd_unit<VAR>(snake_unit(k + 1, cta, P), GC, p).m : 0;
+            const FwdUnit wn = has_next ? fwd_unit<VAR>(snake_unit(k + 1, cta, P), GC, p) : w;
             for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
                 const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
                 const int qunit = t < nq0 ? k : k + 1;
@@ -555,10 +814,22 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 uint8_t *tile = smem + (isq ? C::OFF_Q + (qb * GC + g) * TL::BYTES
                                             : C::OFF_K + st * TL::BYTES);
-                const int row0 = isq ? (qunit == k ? w.m : mnext) : jk;
-                mx = fmaxf(mx, rope_row_ilp<D>(tile, r, static_cast<uint32_t>(row0 * kRows + r),
-                                               p.rope));
+                const FwdUnit &tu = (isq && qunit != k) ? wn : w;   // the tile's unit
+                const int row0 = isq ? tu.m : jk;
+                const uint32_t pos = static_cast<uint32_t>(row0 * kRows + r);
+                float ss;
+                mx = fmaxf(mx, rope_row_ilp<D>(tile, r, pos, p.rope, ss));
                 fence_proxy_async_smem();
+                // rows whose rotated vector is large get exact scores
+                const int limit = tu.sq.len;
+                const uint32_t bal =
+                    __ballot_sync(0xffffffffu, static_cast<int>(pos) < limit && ss > 2.f * D);
+                if (lane == 0) {
+                    if (isq)
+                        qbal[((qunit & 1) * GC + g) * 4 + rw] = bal;
+                    else
+                        kbal[st * 4 + rw] = bal;
+                }
                 __syncwarp();
                 const uint32_t ready =
                     isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]);
@@ -569,8 +840,20 @@ __global__ void __launch_bounds__(512, 1)
                         mbar_arrive(smem_u32(&bar_sv[nsv % 16]));
                     ++nsv;
                 }
-                if (!isq)
+                if (!isq) {
+                    // k_ready completes once all four warps have rotated the
+                    // tile and posted their ballots
+                    if (!mbar_wait_warp(smem_u32(&bar_k_ready[st]), (kt / ST) & 1, wc) ||
+                        !patch_tile<D, GC, ST, VAR>(smem, r, st, jk, w, k % QB, k & 1, qbal, kbal,
+                                                    p, rsync)) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&bar_patch[st]));
                     ++kt;
+                }
             }
         }
         if (mx > kFp16Max)
@@ -595,6 +878,7 @@ __global__ void __launch_bounds__(512, 1)
     float *split_ml = reinterpret_cast<float *>(smem + C::OFF_SPL);   // [m | l][row]
     bool ok = true;
     uint32_t n = 0;          // this group's items so far
+    uint32_t kts = 0;        // key tiles this group has started (K stage kts % ST)
     uint32_t nepi = 0;       // O stores this group has issued
     float mr0 = 0.f, mr1 = 0.f, lr0 = 0.f, lr1 = 0.f;   // running max (log2 units) / sum per slot
     // Writes O_slot / l of head h (rows of this thread) and its lse.  With a
@@ -602,58 +886,10 @@ __global__ void __launch_bounds__(512, 1)
     auto store_head = [&](const FwdUnit &un, int h, uint32_t oa, bool merge, uint32_t ob, float sa,
                           float sb, float inv_l, float lse2) -> bool {
         const int t = un.m * kRows + r;
-        if constexpr (C::STAGE) {
-            // the staging block is free once this group's previous store
-            // has read it
-            if (nepi >= 1) {
-                if (warp == 4 * wg && lane == 0) {
-                    bulk_wait_read0();
-                    mbar_arrive(smem_u32(&bar_stg_free[wg]));
-                }
-                if (!mbar_wait_warp(smem_u32(&bar_stg_free[wg]), (nepi - 1) & 1, wc))
-                    return false;
-            }
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(oa + c, o);
-                tmem_ld_wait(o);
-                float x[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    x[e] = __uint_as_float(o[e]) * sa;
-                if (merge) {
-                    tmem_ld32(ob + c, o);
-                    tmem_ld_wait(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        x[e] = fmaf(__uint_as_float(o[e]), sb, x[e]);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c / 8 + q)) =
-                        make_uint4(pack_bf16x2(x[8 * q + 0] * inv_l, x[8 * q + 1] * inv_l),
-                                   pack_bf16x2(x[8 * q + 2] * inv_l, x[8 * q + 3] * inv_l),
-                                   pack_bf16x2(x[8 * q + 4] * inv_l, x[8 * q + 5] * inv_l),
-                                   pack_bf16x2(x[8 * q + 6] * inv_l, x[8 * q + 7] * inv_l));
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_stg_full[wg]));
-            if (warp == 4 * wg) {
-                if (!mbar_wait_warp(smem_u32(&bar_stg_full[wg]), nepi & 1, wc))
-                    return false;
-                if (lane == 0) {
-                    tma_store_4d(&tmO, smem_u32(stage), 0, h, un.m * kRows, un.b);
-                    bulk_commit();
-                }
-                __syncwarp();
-            }
-            ++nepi;
-        } else {
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out0) +
-                                 ((static_cast<size_t>(un.b) * p.T + t) * p.Hq + h) * D;
+        // O row by row from registers (rows past the sequence skipped)
+        auto store_direct = [&]() {
+            __nv_bfloat16 *dst =
+                static_cast<__nv_bfloat16 *>(p.out0) + (seq_row(p, un.sq, t) * p.Hq + h) * D;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
@@ -673,12 +909,71 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     x[e] *= inv_l;
-                if (t < p.T)
+                if (t < un.sq.len)
                     store_row32_bf16(dst + c, x);
             }
+        };
+        if constexpr (C::STAGE) {
+            // The last tile of a packed sequence goes out row by row: a tile
+            // store would overwrite the next sequence's first rows.
+            if (VAR && p.cu != nullptr && (un.m + 1) * kRows > un.sq.len) {
+                store_direct();
+            } else {
+                // the staging block is free once this group's previous store
+                // has read it
+                if (nepi >= 1) {
+                    if (warp == 4 * wg && lane == 0) {
+                        bulk_wait_read0();
+                        mbar_arrive(smem_u32(&bar_stg_free[wg]));
+                    }
+                    if (!mbar_wait_warp(smem_u32(&bar_stg_free[wg]), (nepi - 1) & 1, wc))
+                        return false;
+                }
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(oa + c, o);
+                    tmem_ld_wait(o);
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        x[e] = __uint_as_float(o[e]) * sa;
+                    if (merge) {
+                        tmem_ld32(ob + c, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            x[e] = fmaf(__uint_as_float(o[e]), sb, x[e]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c / 8 + q)) =
+                            make_uint4(pack_bf16x2(x[8 * q + 0] * inv_l, x[8 * q + 1] * inv_l),
+                                       pack_bf16x2(x[8 * q + 2] * inv_l, x[8 * q + 3] * inv_l),
+                                       pack_bf16x2(x[8 * q + 4] * inv_l, x[8 * q + 5] * inv_l),
+                                       pack_bf16x2(x[8 * q + 6] * inv_l, x[8 * q + 7] * inv_l));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&bar_stg_full[wg]));
+                if (warp == 4 * wg) {
+                    if (!mbar_wait_warp(smem_u32(&bar_stg_full[wg]), nepi & 1, wc))
+                        return false;
+                    if (lane == 0) {
+                        tma_store_4d(&tmO, smem_u32(stage), 0, h, un.sq.base + un.m * kRows,
+                                     un.sq.bc);
+                        bulk_commit();
+                    }
+                    __syncwarp();
+                }
+                ++nepi;
+            }
+        } else {
+            store_direct();
         }
-        if (t < p.T)
-            p.lse[(static_cast<size_t>(un.b) * p.Hq + h) * p.T + t] = lse2 * kLn2;
+        if (t < un.sq.len)
+            p.lse[(static_cast<size_t>(un.sq.bc) * p.Hq + h) * p.T + un.sq.base + t] = lse2 * kLn2;
         return true;
     };
     for (int k = 0; ok; ++k) {
@@ -686,7 +981,17 @@ __global__ void __launch_bounds__(512, 1)
         if (u >= p.num_units)
             break;
         const FwdUnit un = fwd_unit<VAR>(u, GC, p);
-        for (int jk = un.lo; jk <= un.m && ok; ++jk) {
+        for (int jk = un.lo; jk <= un.m && ok; ++jk, ++kts) {
+            // the K stage's patch record (exact scores of large rows): its
+            // counts are read once per key tile
+            const int pst = kts % ST;
+            if (!mbar_wait_warp(smem_u32(&bar_patch[pst]), (kts / ST) & 1, wc)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *prec = smem + C::OFF_PREC + pst * C::PL::PREC_BYTES;
+            const PatchHdr *phdr = reinterpret_cast<const PatchHdr *>(prec);
+            const int pkc = phdr->kcnt;
             for (int pi = 0; pi < GC; ++pi, ++n) {
                 const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
                 const int slot = hrel - ((wg * GC) >> 1);
@@ -709,6 +1014,10 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_s_empty[wg]));
+                const int pqc = phdr->qcnt[hrel];
+                if (pkc > 0 || pqc > 0)
+                    apply_patches<C::NOUT, GC>(s, prec + C::PL::PHDR_BYTES, phdr, pkc, pqc, hrel,
+                                               half, r);
 
                 // causal mask on the diagonal tile (key > query row); with a
                 // sliding window also keys at or below row - W (local index

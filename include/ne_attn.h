@@ -50,10 +50,23 @@
  * T: about 2e-7 radians from the float conversion, plus the hardware
  * sine/cosine error.
  *
+ * Score precision.  The forward rounds q' and k' to fp16 for the tensor
+ * cores, so a score carries a rounding error proportional to |q'| |k'|.  A
+ * row whose rotated vector has mean square above 2 (|x'|^2 > 2 d, e.g. a row
+ * drawn at several times the scale of the others) is scored exactly instead:
+ * for every pair with such a query or key row the forward adds the fp32
+ * difference between the exact score and the fp16 one.  Up to 2 (d = 64) or
+ * 4 (d = 32, 128) such rows per 128-row query tile and per 128-key tile are
+ * handled; a tile with more records NE_WARN_PRECISION (its results are
+ * complete, with the fp16 error on the pairs beyond that count).  Within
+ * these limits lse is within 1e-3 absolute of the exact result for
+ * unit-scale inputs, the stated tolerance.  The backward uses the fp16
+ * scores throughout.
+ *
  * Errors.  Argument errors are returned synchronously and launch nothing.
  * Launch failures return NE_ERR_CUDA.  Device-side errors (a bounded wait
- * that ran out, a value out of fp16 range) are recorded in the device
- * status word and reported by ne_attn_get_error.  Nothing aborts, prints or
+ * that ran out, a value out of fp16 range) and the precision warning are
+ * recorded in the device status word and reported by ne_attn_get_error.  Nothing aborts, prints or
  * throws across this interface, and there is no CPU fallback.
  */
 #ifndef NE_ATTN_H
@@ -77,7 +90,9 @@ typedef enum {
     NE_ERR_TIMEOUT = 7,     /* a device-side bounded wait ran out (reported by get_error) */
     NE_ERR_RANGE = 8,       /* an fp16 tensor-core operand overflowed (reported by get_error) */
     NE_ERR_ARG = 9,         /* another invalid argument (rope_theta <= 0, NaN, ...) */
-    NE_ERR_TOO_LARGE = 10   /* ne_attn_bwd_noalloc: shape exceeds its fixed scratch */
+    NE_ERR_TOO_LARGE = 10,  /* ne_attn_bwd_noalloc: shape exceeds its fixed scratch */
+    NE_WARN_PRECISION = 11  /* a forward tile held more large-norm rows than it scores exactly
+                               (reported by get_error; see "Score precision" above) */
 } ne_status;
 
 /*
@@ -234,7 +249,7 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
  * token's activations do): tiles that straddle a sequence's end compute over
  * them, with zero weight, before the padding is overwritten.  Query tiles
  * (and, in the backward, key tiles) wholly past a sequence's end are
- * skipped; the backward's preprocess still covers every row.  The library
+ * skipped, and the backward's preprocess does not read padding rows.  The library
  * builds the tables of live work
  * units on the host and copies them into the workspace with an asynchronous
  * copy from pageable memory, so these calls cannot be captured into a CUDA
@@ -253,6 +268,41 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
                        int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
 
 /*
+ * Packed variable-length batches: the sequences concatenated along the rows,
+ * with no padding (the layout an SFT batch takes when its pairs are packed
+ * instead of padded to the context).  Sequence b is rows cu_seqlens[b] ..
+ * cu_seqlens[b+1]-1 of the pack, a causal problem of its own whose positions
+ * (for RoPE) restart at 0.
+ *   q, o, dO, dq  bf16 [total][Hq][d]
+ *   k, v, dk, dv  bf16 [total][Hkv][d]
+ *   lse           fp32 [Hq][total]
+ *   cu_seqlens    int32 [nseq + 1], HOST memory, read during the call only:
+ *                 cu_seqlens[0] = 0, non-decreasing, cu_seqlens[nseq] = total
+ *                 (empty sequences are allowed)
+ *   workspace     caller-owned device memory (16-byte aligned, no initial
+ *                 contents) of at least ne_attn_packed_workspace_size() bytes;
+ *                 the forward uses only its first part (the work-unit tables)
+ * Results equal those of the padded entry points on the same sequences, row
+ * for row; every row of the pack is a valid row.  The library builds the
+ * tables of work units on the host and copies them into the workspace from
+ * pageable memory, so these calls cannot be captured into a CUDA graph;
+ * calls that share a workspace must not overlap on the GPU.  Errors as for
+ * the padded entry points; cu_seqlens NULL gives NE_ERR_NULL, nseq < 1 or
+ * total < 1 NE_ERR_SHAPE, an inconsistent cu_seqlens NE_ERR_ARG.
+ * ne_attn_packed_workspace_size returns 0 for an invalid shape.
+ */
+size_t ne_attn_packed_workspace_size(int nseq, int total, int Hq, int Hkv, int d);
+int ne_attn_fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
+                       void *stream);
+int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
+                       void *stream);
+
+/*
  * The work units a padded variable-length batch launches (host only; no GPU
  * needed): per-sequence lengths seqlens[B] (host) give counts[0..2], the
  * live units of the forward, dq and dk/dv kernels, and each non-NULL table
@@ -268,9 +318,9 @@ int ne_attn_varlen_plan(const int32_t *seqlens, int B, int T, int Hq, int Hkv, i
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status of
- * the current device: NE_ERR_TIMEOUT or NE_ERR_RANGE if a kernel recorded
- * one since the last call, NE_ERR_CUDA if the stream reports a CUDA error,
- * else NE_OK.
+ * the current device: NE_ERR_TIMEOUT, NE_ERR_RANGE or NE_WARN_PRECISION (in
+ * that order of precedence) if a kernel recorded one since the last call,
+ * NE_ERR_CUDA if the stream reports a CUDA error, else NE_OK.
  */
 int ne_attn_get_error(void *stream);
 

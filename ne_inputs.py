@@ -137,6 +137,13 @@ def make_inputs(w: Workload, layer: int = 0) -> dict[str, torch.Tensor]:
             for name, x in (("q", q), ("k", k), ("v", v), ("do", do))}
 
 
+# q and k scale of the GPU tests' edge-case shapes: the 116M layer's
+# (gpt116m_b16_t512: q and k x 0.5).  Those cases cover shapes (ragged T,
+# head dims, groups, windows, lengths); unit-scale precision is covered by the
+# unit-scale workloads above.
+CUSTOM_QK_SCALE = 0.5
+
+
 def make_custom(B: int, T: int, Hq: int, Hkv: int, d: int, seed: int,
                 scale: float = 1.0) -> dict[str, torch.Tensor]:
     """Draw an arbitrary-shape case with the same recipe (used for edge-case tests)."""

@@ -5,12 +5,11 @@ tolerances.
 Tolerances (the stated bounds for bf16 inputs and tensor-core operands):
   O           norm-wise max relative error <= 1e-2
   dq, dk, dv  norm-wise max relative error <= 2e-2
-  lse         absolute error <= 1e-3 * max(1, |q_t| max_s |k_s| / d)
-The lse bound is 1e-3 absolute for unit-variance rows (|q||k|/d ~ 1) and
-grows in proportion to the row's score scale, because the score-side
-operands are rounded to fp16 before the tensor cores and the rounding error
-of a score is proportional to |q'| |k'|; only the 8x-scaled outlier rows of
-the stress shape see a bound above 1e-3.
+  lse         absolute error <= 1e-3, on every row
+Norm-wise relative error is max|g - r| / max|r| over the tensor.  Beside it
+compare() reports, as a diagnostic with no bound, the element-wise error
+max |g - r| / max(|r|, 1e-3 max|r|), which also sees errors on entries far
+smaller than the tensor's largest.
 """
 from __future__ import annotations
 
@@ -32,15 +31,21 @@ def rel_err(gpu, ref) -> float:
     return float(np.abs(gpu - ref).max() / (den if den > 0 else 1.0))
 
 
-def lse_bound(q, k):
-    """Per-row lse tolerance [B, Hq, T] (see module docstring)."""
-    qn = np.linalg.norm(q, axis=-1)                      # [B, T, Hq]
-    kn = np.linalg.norm(k, axis=-1)                      # [B, T, Hkv]
-    kmax = np.maximum.accumulate(kn, axis=1)             # max over s <= t
-    G = q.shape[2] // k.shape[2]
-    kmax = np.repeat(kmax, G, axis=2)                    # per query head
-    scale = qn * kmax / q.shape[-1]
-    return TOL_LSE * np.maximum(1.0, scale).transpose(0, 2, 1)
+def elementwise_err(gpu, ref) -> float:
+    """max |g - r| / max(|r|, 1e-3 max|r|): the element-wise diagnostic."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    top = np.abs(ref).max()
+    if top == 0:
+        return float(np.abs(gpu).max())
+    return float((np.abs(gpu - ref) / np.maximum(np.abs(ref), 1e-3 * top)).max())
+
+
+def custom_inputs(**kw):
+    """An edge-case shape drawn with the workload recipe at the 116M layer's
+    q/k scale (ne_inputs.CUSTOM_QK_SCALE)."""
+    kw.setdefault("scale", ne_inputs.CUSTOM_QK_SCALE)
+    return ne_inputs.make_custom(**kw)
 
 
 def to_dev(x: dict, device="cuda"):
@@ -60,20 +65,23 @@ def gpu_fwd_bwd(xd: dict, theta: float, with_bwd: bool = True):
     return out
 
 
-def compare(gpu: dict, ref: dict, q64, k64, what=("o", "lse", "dq", "dk", "dv")):
+def compare(gpu: dict, ref: dict, q64=None, k64=None, what=("o", "lse", "dq", "dk", "dv")):
+    """Checks every tensor in `what` against the oracle; returns the errors
+    (norm-wise, lse absolute) and, under "<name>_elem", the element-wise
+    diagnostic.  q64, k64 are accepted for older callers and unused."""
     errs = {}
     for n in what:
         g = gpu[n].float().cpu().double().numpy() if isinstance(gpu[n], torch.Tensor) else gpu[n]
         r = ref[n]
         assert np.isfinite(g).all(), f"{n} has non-finite values"
         if n == "lse":
-            bound = lse_bound(q64, k64)
-            errs[n] = float(np.abs(g - r).max())
-            ratio = np.abs(g - r) / bound
-            assert ratio.max() <= 1.0, (
-                f"lse error {errs[n]:.3e} exceeds the bound at {np.unravel_index(ratio.argmax(), ratio.shape)}")
+            diff = np.abs(g - r)
+            errs[n] = float(diff.max())
+            assert errs[n] <= TOL_LSE, (
+                f"lse error {errs[n]:.3e} > {TOL_LSE} at {np.unravel_index(diff.argmax(), diff.shape)}")
         else:
             errs[n] = rel_err(g, r)
+            errs[n + "_elem"] = elementwise_err(g, r)
             tol = TOL_O if n == "o" else TOL_GRAD
             assert errs[n] <= tol, f"{n}: max relative error {errs[n]:.3e} > {tol}"
     return errs

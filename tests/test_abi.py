@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(11):
+    for code in range(12):
         s = ne.ne_attn_status_string(code)
         assert s and s != "unknown status"
     assert ne.ne_attn_status_string(99) == "unknown status"
@@ -128,3 +128,37 @@ def test_window_argument_errors(lib):
     a = (ctypes.addressof(buf) + 15) // 16 * 16
     assert lib.ne_attn_fwd_window(a, a, a, a, a, 1, 8, 2, 2, 64, 10000.0, -1, None) == 9
     assert lib.ne_attn_bwd_window(*([a] * 10), 1 << 20, 1, 8, 2, 2, 64, 10000.0, -3, None) == 9
+
+
+def test_packed_workspace_size_and_argument_errors(lib):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    # [lengths][cu][fwd units][dq units][dk/dv units] + the backward workspace of
+    # a [1][total] batch; live tiles per kv head <= total // 128 + nseq
+    nseq, total, Hq, Hkv, d = 3, 300, 12, 4, 64
+    tiles = (total // 128 + nseq) * Hkv
+    want = (r256(4 * nseq) + r256(4 * (nseq + 1)) + r256(4 * tiles) + r256(4 * tiles) +
+            r256(4 * tiles) + ne.ne_attn_bwd_workspace_size(1, total, Hq, Hkv, d))
+    assert ne.ne_attn_packed_workspace_size(nseq, total, Hq, Hkv, d) == want
+    assert ne.ne_attn_packed_workspace_size(0, total, Hq, Hkv, d) == 0
+    assert ne.ne_attn_packed_workspace_size(1, 0, Hq, Hkv, d) == 0
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    ws = 1 << 15
+
+    def fwd(cu, nseq, total, wsb=ws, d=64):
+        arr = (ctypes.c_int32 * len(cu))(*cu) if cu is not None else None
+        return lib.ne_attn_fwd_packed(a, a, a, a, a, arr, a, wsb, nseq, total, 2, 2, d,
+                                      10000.0, None)
+
+    assert fwd(None, 2, 10) == 1                 # NE_ERR_NULL
+    assert fwd([0, 10], 0, 10) == 2              # no sequences
+    assert fwd([0, 0], 1, 0) == 2                # empty pack
+    assert fwd([1, 10], 1, 10) == 9              # cu[0] != 0
+    assert fwd([0, 6, 4, 10], 3, 10) == 9        # decreasing
+    assert fwd([0, 4, 9], 2, 10) == 9            # cu[nseq] != total
+    assert fwd([0, 4, 10], 2, 10, d=48) == 3     # head dim
+    assert fwd([0, 4, 10], 2, 10, wsb=0) == 5    # workspace
+    cu = (ctypes.c_int32 * 3)(0, 4, 10)
+    assert lib.ne_attn_bwd_packed(a, a, a, a, a, a, a, a, a, cu, a, 0, 2, 10, 2, 2, 64,
+                                  10000.0, None) == 5

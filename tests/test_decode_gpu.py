@@ -9,7 +9,7 @@ import torch
 
 import ne_inputs
 import oracle
-from parity_util import TOL_LSE, TOL_O, rel_err
+from parity_util import TOL_LSE, TOL_O, custom_inputs, rel_err
 
 pytestmark = pytest.mark.gpu
 THETA = ne_inputs.ROPE_THETA
@@ -24,7 +24,7 @@ def ne():
 
 
 def _case(B, Tk, Hq, Hkv, d, seed):
-    x = ne_inputs.make_custom(B=B, T=Tk, Hq=Hq, Hkv=Hkv, d=d, seed=seed)
+    x = custom_inputs(B=B, T=Tk, Hq=Hq, Hkv=Hkv, d=d, seed=seed)
     q1 = x["q"][:, -1].contiguous()          # [B, Hq, d]: the new token's query
     return q1, x["k"], x["v"]
 

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import ne_inputs
-from parity_util import compare, gpu_fwd_bwd, oracle_all, slice_gpu, to_dev
+from parity_util import compare, custom_inputs, gpu_fwd_bwd, oracle_all, slice_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 THETA = ne_inputs.ROPE_THETA
@@ -52,32 +52,40 @@ def test_step_workload_one_layer_sampled():
 
 
 def test_stress_workload_sampled():
-    """B4 T4096 16/4 d128 with 8x outlier rows; the oracle checks 2 groups."""
+    """B4 T4096 16/4 d128 with one 8x row per (tensor, batch, head); the oracle
+    checks four (batch, kv head) groups, one per batch row, each holding 8x
+    rows of q, k and v, with the flat lse bound on every row."""
     w = ne_inputs.STRESS
-    print(_sampled_case(w, 0, [(0, 0), (3, 2)]))
+    groups = [(0, 0), (1, 3), (2, 1), (3, 2)]
+    x = ne_inputs.make_inputs(w, 0)
+    for (b, j) in groups:
+        for name, heads in (("q", range(j * w.G, (j + 1) * w.G)), ("k", [j]), ("v", [j])):
+            ms = x[name][b, :, list(heads)].float().pow(2).mean(-1)
+            assert (ms > 16).any(), (name, b, j, "no 8x row in the checked group")
+    print(_sampled_case(w, 0, groups))
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 17, 127, 128, 129, 200, 255, 256, 300, 383])
 def test_ragged_lengths_d64(T):
-    _full_case(ne_inputs.make_custom(B=2, T=T, Hq=6, Hkv=2, d=64, seed=100 + T))
+    _full_case(custom_inputs(B=2, T=T, Hq=6, Hkv=2, d=64, seed=100 + T))
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 2), (6, 2), (8, 2), (5, 1), (12, 4)])
 def test_head_dims_and_groups(d, Hq, Hkv):
-    _full_case(ne_inputs.make_custom(B=1, T=260, Hq=Hq, Hkv=Hkv, d=d, seed=7 * d + Hq + Hkv))
+    _full_case(custom_inputs(B=1, T=260, Hq=Hq, Hkv=Hkv, d=d, seed=7 * d + Hq + Hkv))
 
 
 @pytest.mark.parametrize("d", [32, 128])
 def test_ragged_other_dims(d):
     for T in (1, 5, 131):
-        _full_case(ne_inputs.make_custom(B=2, T=T, Hq=4, Hkv=2, d=d, seed=300 + T + d))
+        _full_case(custom_inputs(B=2, T=T, Hq=4, Hkv=2, d=d, seed=300 + T + d))
 
 
 def test_deterministic():
     """Two backward calls on the same inputs are bitwise equal (no float atomics)."""
     import causal_gqa_attention_ne_gb300 as ne
-    xd = to_dev(ne_inputs.make_custom(B=3, T=400, Hq=12, Hkv=4, d=64, seed=5))
+    xd = to_dev(custom_inputs(B=3, T=400, Hq=12, Hkv=4, d=64, seed=5))
     o, lse = ne.attention_forward(xd["q"], xd["k"], xd["v"], THETA)
     o2, lse2 = ne.attention_forward(xd["q"], xd["k"], xd["v"], THETA)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
@@ -91,7 +99,7 @@ def test_outputs_stay_in_bounds():
     """Guard regions around every output keep their fill pattern (odd T)."""
     import causal_gqa_attention_ne_gb300 as ne
     B, T, Hq, Hkv, d = 2, 133, 6, 2, 64
-    xd = to_dev(ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=9))
+    xd = to_dev(custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=9))
     G = 4096
 
     def guarded(shape, dtype):
@@ -122,7 +130,7 @@ def test_timeout_path_reports_and_recovers():
     ne.ne_attn_selftest_timeout(2_000_000)   # 2 ms
     assert ne.ne_attn_get_error() == 7
     assert ne.ne_attn_get_error() == 0       # cleared
-    _full_case(ne_inputs.make_custom(B=1, T=64, Hq=2, Hkv=1, d=64, seed=3))
+    _full_case(custom_inputs(B=1, T=64, Hq=2, Hkv=1, d=64, seed=3))
 
 
 def test_rejects_bad_arguments_on_device():
@@ -149,7 +157,7 @@ def test_substeps_match_full_backward(d):
     bitwise, also when kernels of other head dims ran in between."""
     import causal_gqa_attention_ne_gb300 as ne
     B, T, Hq, Hkv = 2, 300, 6, 2
-    xd = to_dev(ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=40 + d))
+    xd = to_dev(custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=40 + d))
     o, lse = ne.attention_forward(xd["q"], xd["k"], xd["v"], THETA)
     dq, dk, dv = ne.attention_backward(xd["q"], xd["k"], xd["v"], o, lse, xd["do"], THETA)
     ws = torch.empty(ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8,

@@ -11,7 +11,7 @@ import torch
 
 import ne_inputs
 import oracle
-from parity_util import compare, to_dev
+from parity_util import compare, custom_inputs, to_dev
 
 pytestmark = pytest.mark.gpu
 THETA = ne_inputs.ROPE_THETA
@@ -73,7 +73,7 @@ def _check_sequences(got, x, lens, which):
     (3, 520, 16, 4, 128, [520, 391, 9]),
 ])
 def test_varlen_matches_oracle(ne, B, T, Hq, Hkv, d, lens):
-    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=2100 + T + Hq)
+    x = custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=2100 + T + Hq)
     got = _run(ne, to_dev(x), lens)
     _check_padding(got, lens)
     _check_sequences(got, x, lens, range(B))
@@ -82,7 +82,7 @@ def test_varlen_matches_oracle(ne, B, T, Hq, Hkv, d, lens):
 def test_varlen_all_full_is_the_causal_path(ne):
     """Every length T: the unit tables are the full enumerations in launch
     order, so the results are the causal entry points' bit for bit."""
-    x = to_dev(ne_inputs.make_custom(B=3, T=300, Hq=12, Hkv=4, d=64, seed=2200))
+    x = to_dev(custom_inputs(B=3, T=300, Hq=12, Hkv=4, d=64, seed=2200))
     got = _run(ne, x, [300, 300, 300])
     o, lse = ne.attention_forward(x["q"], x["k"], x["v"], THETA)
     dq, dk, dv = ne.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], THETA)
@@ -95,8 +95,8 @@ def test_varlen_padding_contents_do_not_matter(ne):
     """Other (finite) values in the padding rows of q, k, v and dO leave every
     output bit unchanged: masked probabilities are exact zeros."""
     lens = [150, 300, 1, 257]
-    x = ne_inputs.make_custom(B=4, T=300, Hq=6, Hkv=2, d=64, seed=2300)
-    y = ne_inputs.make_custom(B=4, T=300, Hq=6, Hkv=2, d=64, seed=2301)
+    x = custom_inputs(B=4, T=300, Hq=6, Hkv=2, d=64, seed=2300)
+    y = custom_inputs(B=4, T=300, Hq=6, Hkv=2, d=64, seed=2301)
     for b, L in enumerate(lens):
         for n in ("q", "k", "v", "do"):
             y[n][b, :L] = x[n][b, :L]

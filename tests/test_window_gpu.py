@@ -9,7 +9,7 @@ import torch
 
 import ne_inputs
 import oracle
-from parity_util import compare, to_dev
+from parity_util import compare, custom_inputs, to_dev
 
 pytestmark = pytest.mark.gpu
 THETA = ne_inputs.ROPE_THETA
@@ -44,7 +44,7 @@ def _run(ne, xd, W):
                                              (2, 130, 8, 2, 32, 300), (1, 512, 12, 4, 64, 256),
                                              (1, 640, 3, 1, 64, 191)])
 def test_window_matches_oracle(ne, B, T, Hq, Hkv, d, W):
-    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1600 + T + W)
+    x = custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1600 + T + W)
     got = _run(ne, to_dev(x), W)
     q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
     ref = oracle.attn_bwd(q, k, v, do, THETA, window=W)
@@ -53,7 +53,7 @@ def test_window_matches_oracle(ne, B, T, Hq, Hkv, d, W):
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,d,W", [(1, 384, 12, 4, 64, 129), (2, 300, 4, 2, 32, 64)])
 def test_window_training_pair_matches_oracle(ne, B, T, Hq, Hkv, d, W):
-    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1650 + T + W)
+    x = custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1650 + T + W)
     xd = to_dev(x)
     q, k, v, do = xd["q"], xd["k"], xd["v"], xd["do"]
     ws = torch.zeros(ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d), dtype=torch.uint8,
@@ -71,7 +71,7 @@ def test_window_training_pair_matches_oracle(ne, B, T, Hq, Hkv, d, W):
 
 
 def test_window_zero_is_the_causal_path(ne):
-    x = to_dev(ne_inputs.make_custom(B=2, T=300, Hq=6, Hkv=2, d=64, seed=1700))
+    x = to_dev(custom_inputs(B=2, T=300, Hq=6, Hkv=2, d=64, seed=1700))
     got = _run(ne, x, 0)
     o, lse = ne.attention_forward(x["q"], x["k"], x["v"], THETA)
     dq, dk, dv = ne.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], THETA)
@@ -85,7 +85,7 @@ def test_window_long_context_sampled(ne):
     window and are skipped; the oracle checks two (batch, kv head) groups."""
     from parity_util import slice_gpu
     B, T, Hq, Hkv, d, W = 2, 2048, 8, 2, 128, 300
-    x = ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1800)
+    x = custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=1800)
     got = _run(ne, to_dev(x), W)
     q, k, v, do = (ne_inputs.as_f64(x[n]) for n in ("q", "k", "v", "do"))
     G = Hq // Hkv

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import ne_inputs
-from parity_util import to_dev
+from parity_util import custom_inputs, to_dev
 
 pytestmark = pytest.mark.gpu
 THETA = ne_inputs.ROPE_THETA
@@ -27,7 +27,7 @@ def ne():
 
 
 def _compare_once(ne, seed, B, T, Hq, Hkv, d):
-    x = to_dev(ne_inputs.make_custom(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=seed))
+    x = to_dev(custom_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, seed=seed))
     o, lse = ne.attention_forward(x["q"], x["k"], x["v"], THETA)
     ref = ne.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], THETA)
     got = tuple(torch.empty_like(t) for t in ref)
