@@ -253,6 +253,7 @@ int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, v
     p.lse = lse;
     p.q_in = q;
     p.k_in = k;
+    p.v_in = v;
     p.save_rot = save ? 1 : 0;
     p.window = window;
     CUtensorMap mq, mk, mv, mo, mqs, mks;
@@ -793,6 +794,7 @@ int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, flo
     p.lse = lse;
     p.q_in = q;
     p.k_in = k;
+    p.v_in = v;
     CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
         make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
@@ -1015,6 +1017,7 @@ int ne_attn_fwd_packed(const void *q, const void *k, const void *v, void *o, flo
     p.lse = lse;
     p.q_in = q;
     p.k_in = k;
+    p.v_in = v;
     CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, 1, total, Hq, d) || make_map(&mk, k, 1, total, Hkv, d) ||
         make_map(&mv, v, 1, total, Hkv, d) || make_map(&mo, o, 1, total, Hq, d))

@@ -286,7 +286,7 @@ struct AttnParams {
     int GC, nchunks;             // query heads per CTA, CTAs per KV group (Q-major kernels)
     float scale_log2;            // log2(e) / sqrt(d)
     float scale;                 // 1 / sqrt(d)
-    const void *q_in, *k_in;     // forward: bf16 q, k (re-read for exact scores of large rows)
+    const void *q_in, *k_in, *v_in;   // forward: bf16 q, k, v (re-read to repair large rows)
     const void *o_in;            // backward: forward output O (preprocess)
     const void *do_in;           // backward: dO (preprocess)
     void *out0;                  // forward: O; backward: dq / dk

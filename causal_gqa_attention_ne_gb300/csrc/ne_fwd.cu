@@ -26,7 +26,9 @@
 //               as the group has loaded it (so S(n+1) is computed while the
 //               group works on item n), and two P buffers.
 //   warps 8-11  RoPE: rotate the unit's Q tiles and each K tile in place
-//               (bf16 in, fp16 out), in the order the MMAs first need them.
+//               (bf16 in, fp16 out), in the order the MMAs first need them,
+//               and record rows of large norm (see "exact scores of large
+//               rows" below).
 //   warp 12     TMA producer.
 //   warps 13, 14  MMA issuers of softmax groups 0 and 1 (warp 13 also
 //               allocates TMEM): S(n) into the group's S buffer, then
@@ -34,6 +36,8 @@
 //   warp 15     training path only: stores each rotated Q' tile and each K'
 //               tile once into the backward's workspace, and tells the
 //               producer when a buffer it stored from may be reloaded.
+// After the loop the softmax warps repair the rows of the CTA's units that
+// see a recorded large row (rare; nothing happens on ordinary inputs).
 // TMEM: one 64-column S buffer per group (columns 0-127), two 32-column P
 // buffers per group (bf16 pairs, columns 128-255), then the groups' O
 // accumulators (COL_O + (w*NSL + slot)*D).
@@ -47,33 +51,21 @@ namespace ne {
 
 // Shared-memory plan: QB Q-tile sets of GC heads (two for D <= 64, so the
 // next unit's Q' is loaded and rotated while the current unit runs), ST K/V
-// stages (as many as fit, at most four), two O staging blocks (D <= 64), the
-// running max / sum of a split head, and the exact-score bookkeeping of
-// large-norm rows: per Q slot the ballot of its large rows and their exact
-// rotated vectors, the exact vectors of one K tile's large rows, and per K
-// stage a patch record (see below).
+// stages (as many as fit, at most four), two O staging blocks (D <= 64) and
+// the running max / sum of a split head.
 template <int D, int GC>
 struct FwdPlan {
     using TL = Tile<D>;
     static constexpr bool STAGE = (D <= 64);
     static constexpr int QB = (D <= 64) ? 2 : 1;
-    // large-norm rows scored exactly per Q tile and per K tile
-    static constexpr int NOUT = (D == 64) ? 2 : 4;
-    static constexpr int BALLOT_BYTES = 256;                    // [2][GC][4] + [ST][4] words
-    static constexpr int QOV_BYTES = 2 * GC * NOUT * D * 4;     // exact q' of large rows
-    static constexpr int KOV_BYTES = NOUT * D * 4;              // exact k' of large rows
-    static constexpr int PHDR_BYTES = 256;                      // counts and row indices
-    // per stage: header, then dS_k [NOUT][GC][128] and dS_q [GC][NOUT][128] (fp16)
-    static constexpr int PREC_BYTES = PHDR_BYTES + 2 * NOUT * GC * kRows * 2;
     static constexpr int fixed_bytes()
     {
-        return QB * GC * TL::BYTES + (STAGE ? 2 * TL::BLOCK : 0) + 2 * kRows * 4 + BALLOT_BYTES +
-               QOV_BYTES + KOV_BYTES + 1024;
+        return QB * GC * TL::BYTES + (STAGE ? 2 * TL::BLOCK : 0) + 2 * kRows * 4 + 1024;
     }
     static constexpr int stages()
     {
         int st = 4;
-        while (st > 1 && fixed_bytes() + st * (2 * TL::BYTES + PREC_BYTES) > 232448 - 1024)
+        while (st > 1 && fixed_bytes() + st * 2 * TL::BYTES > 232448 - 1024)
             --st;
         return st;
     }
@@ -86,20 +78,13 @@ struct FwdCfg {
     using PL = FwdPlan<D, GC>;
     static constexpr bool STAGE = PL::STAGE;                 // O leaves by TMA store
     static constexpr int QB = PL::QB;
-    static constexpr int NOUT = PL::NOUT;
     static constexpr int OFF_Q = 0;                          // [QB][GC] tiles
     static constexpr int OFF_K = OFF_Q + QB * GC * TL::BYTES;
     static constexpr int OFF_V = OFF_K + ST * TL::BYTES;
     static constexpr int OFF_O = OFF_V + ST * TL::BYTES;      // [2] staging blocks
     // group 1's running max and sum of the split head: float [2][128]
     static constexpr int OFF_SPL = OFF_O + (STAGE ? 2 * TL::BLOCK : 0);
-    // uint32 ballots of large rows (one word per RoPE warp): the Q tiles of
-    // units of each parity [2][GC][4], then the K stages [ST][4]
-    static constexpr int OFF_BAL = OFF_SPL + 2 * kRows * 4;
-    static constexpr int OFF_QOV = OFF_BAL + PL::BALLOT_BYTES;   // float [2][GC][NOUT][D]
-    static constexpr int OFF_KOV = OFF_QOV + PL::QOV_BYTES;      // float [NOUT][D]
-    static constexpr int OFF_PREC = OFF_KOV + PL::KOV_BYTES;     // [ST] patch records
-    static constexpr int SMEM_BYTES = smem_one_cta(OFF_PREC + ST * PL::PREC_BYTES + 1024);
+    static constexpr int SMEM_BYTES = smem_one_cta(OFF_SPL + 2 * kRows * 4 + 1024);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NSL = (GC + 1) / 2;          // O accumulators per softmax group
     static constexpr bool SPLIT = (GC & 1) != 0;      // one head's key halves in both groups
@@ -110,25 +95,6 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448 - 1024, "shared memory budget");
     static_assert(ST >= 2, "K/V double buffering");
     static_assert(!STAGE || TL::NB == 1, "staged epilogue stores one column block per head");
-    static_assert(2 * GC * 4 * 4 + ST * 4 * 4 <= PL::BALLOT_BYTES, "ballot words");
-    static_assert(4 * (1 + NOUT + GC + GC * NOUT) <= PL::PHDR_BYTES, "patch record header");
-};
-
-// Patch record of one K stage, written by the RoPE warpgroup once it has
-// rotated the stage's K tile, read by the softmax groups for every item of
-// that tile.  A row whose rotated vector has mean square above 2 (sum of
-// squares > 2 D) is "large": its scores' fp16 rounding error, proportional to
-// |q'||k'|, would exceed what the 1e-3 lse tolerance allows.  For the pairs
-// with a large key row (column kcol[i] of the tile) or a large query row
-// (row qrow[g][i] of head g's Q tile) the record holds
-//   delta = <q', k'> exact (fp32 from the bf16 inputs) - <fp16 q', fp16 k'>
-// which the softmax thread adds to the score the tensor cores computed from
-// the fp16 operands.
-struct PatchHdr {
-    int kcnt;        // large key rows in the tile (<= NOUT)
-    int qcnt[4];     // per head of the unit: large query rows (<= NOUT)
-    int kcol[4];     // their key indices in the tile
-    int qrow[4][4];  // [head][i]: their row indices in the Q tile
 };
 
 struct FwdUnit {
@@ -157,237 +123,315 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
     return w;
 }
 
+// ------------------------------------------------ exact scores of large rows ---
+//
+// A row of a Q or K tile is "large" when its rotated vector has mean square
+// above 4 (sum of squares > 4 D): the fp16 rounding error of its scores,
+// proportional to |q'||k'|, would exceed what the 1e-3 lse tolerance allows.
+// A unit-variance row passes that bound with probability below 1e-12 at
+// d = 32 (chi-squared tail), so ordinary inputs never take this path.
+//
+// The RoPE thread that rotates such a row records it in the CTA's flag list:
+// a query row under its unit, a key row once per (sequence, kv head).  After
+// the persistent loop, when the list is not empty, the CTA's softmax warps
+// repair the rows of their own units from global memory (every O tile of the
+// CTA is stored by then; no other CTA writes these rows):
+//   - a large query row is recomputed exactly: fp32 scores from the bf16
+//     inputs over all its visible keys, then its O row and lse;
+//   - every other row t of the unit that sees large keys s_i is corrected.
+//     With p(S) = exp(S / sqrt(d) - lse_t), S_i the exact fp32 score and
+//     F_i the product of the fp16 operands the tensor cores saw:
+//         delta_i = p(S_i) - p(F_i),   Delta = sum_i delta_i
+//         lse_t' = lse_t + log1p(Delta)
+//         O_t'   = (O_t + sum_i delta_i v_i) / (1 + Delta)
+//     which is the softmax with those pairs' scores made exact.
+// A CTA records up to kFlagCap rows; more set NE_WARN_PRECISION (the rows
+// left out keep the fp16 error on their pairs).
+constexpr int kFlagCap = 48;
+constexpr uint32_t kFlagKey = 15u;   // entry kind of a key row (a query row: its head g < 4)
 
-// ---------------------------------------------- exact scores of large rows ---
-
-// The rotated row of the bf16 vector at `row` (global memory) in fp32:
-// f(i, x'_i, x'_{i + D/2}) for every rotate-half pair i, position pos.  One
-// pair per iteration, so the few registers of the RoPE warps suffice (this
-// runs only for tiles with large rows).
-template <int D, typename F>
-__device__ __forceinline__ void exact_pairs(const __nv_bfloat16 *row, uint32_t pos,
-                                            const RopeFreqs &fr, F &&f)
+// Entry: bits 0-23 the row's position in its sequence, 24-27 the kind,
+// 32-63 the unit index (query rows) or b * Hkv + j (key rows).
+__device__ __forceinline__ uint64_t flag_entry(uint32_t hi, uint32_t kind, uint32_t pos)
 {
-#pragma unroll 1
-    for (int i = 0; i < D / 2; ++i) {
-        float sn, cs;
-        rope_sincos(pos, fr, i, sn, cs);
-        const float x = __bfloat162float(row[i]);
-        const float y = __bfloat162float(row[i + D / 2]);
-        float u, w;
-        rope_rotate(x, y, cs, sn, u, w);
-        f(i, u, w);
-    }
+    return (static_cast<uint64_t>(hi) << 32) | (kind << 24) | pos;
+}
+__device__ __forceinline__ uint32_t flag_hi(uint64_t e) { return static_cast<uint32_t>(e >> 32); }
+__device__ __forceinline__ uint32_t flag_kind(uint64_t e)
+{
+    return (static_cast<uint32_t>(e) >> 24) & 15u;
+}
+__device__ __forceinline__ int flag_pos(uint64_t e)
+{
+    return static_cast<int>(static_cast<uint32_t>(e) & 0xFFFFFFu);
 }
 
-// Element (r, col) of a rotated fp16 tile in shared memory.
+// Records entry e; a key row only once (every unit that reads its tile
+// rotates it again, always in the same thread, which sees its own entry).
+// Free slots hold ~0, which no entry equals.
+__device__ __forceinline__ void flag_row(uint64_t *list, uint32_t *cnt, uint64_t e, bool once,
+                                         uint32_t *status)
+{
+    volatile uint64_t *vl = list;
+    if (once) {
+        const uint32_t n = *reinterpret_cast<volatile uint32_t *>(cnt);
+        for (uint32_t i = 0; i < n && i < static_cast<uint32_t>(kFlagCap); ++i)
+            if (vl[i] == e)
+                return;
+    }
+    const uint32_t i = atomicAdd(cnt, 1u);
+    if (i < static_cast<uint32_t>(kFlagCap))
+        vl[i] = e;
+    else
+        atomicOr(status, kDevPrecision);
+}
+
+// Pair i (elements i and i + D/2) of the bf16 row at `row`, rotated exactly
+// as the RoPE warps rotate it, in fp32.
+__device__ __forceinline__ void exact_pair(const __nv_bfloat16 *row, int half_d, uint32_t pos,
+                                           const RopeFreqs &fr, int i, float &u, float &w)
+{
+    float sn, cs;
+    rope_sincos(pos, fr, i, sn, cs);
+    rope_rotate(__bfloat162float(row[i]), __bfloat162float(row[i + half_d]), cs, sn, u, w);
+}
+
+// The value the tensor cores see for x (the fp16 operand of a score).
+__device__ __forceinline__ float as_f16(float x) { return __half2float(__float2half_rn(x)); }
+
+// Scratch (floats, in the CTA's idle tile buffers) of the repair below.
 template <int D>
-__device__ __forceinline__ float tile_f16(const uint8_t *tile, int r, int col)
-{
-    return __half2float(
-        *reinterpret_cast<const __half *>(tile + tile_chunk<D>(r, col >> 3) + (col & 7) * 2));
-}
+struct FixScratch {
+    static constexpr int NT = 256;                    // the softmax threads
+    static constexpr int QV = 0;                      // exact q' of the row recomputed [D]
+    static constexpr int PART = QV + D;               // per warp: max, sum, O [8][D + 2]
+    static constexpr int KPOS = PART + 8 * (D + 2);   // int: the unit's large keys, ascending
+    static constexpr int NK = KPOS + kFlagCap;        // int: how many
+    static constexpr int KDAT = NK + 4;               // per key: exact k', fp16 k', v [3][D]
+    static constexpr int DPS = KDAT + kFlagCap * 3 * D;   // delta_i per thread [kFlagCap][NT]
+    static constexpr int BYTES = (DPS + kFlagCap * NT) * 4;
+};
 
-// Row index (32 w + lane) of the o-th set bit of four ballot words, in
-// increasing row order; -1 if there are not that many.
-__device__ __forceinline__ int nth_row(const uint32_t *bal, int o)
+// The repair of the rows of this CTA's units (the comment block above).  Run
+// by the 256 softmax threads, which meet at named barrier 1; every branch
+// around a barrier depends only on the list and the unit, so it is uniform.
+template <int D, int GC, bool WIN, bool VAR>
+__device__ __noinline__ void fix_large_rows(float *scr, const uint64_t *list, int nflag, int cta,
+                                            int P, const AttnParams &p)
 {
-    for (int w = 0; w < 4; ++w) {
-        uint32_t m = bal[w];
-        const int c = __popc(m);
-        if (o < c) {
-            for (int i = 0; i < o; ++i)
-                m &= m - 1u;
-            return 32 * w + __ffs(m) - 1;
-        }
-        o -= c;
-    }
-    return -1;
-}
-
-// Rank of row r among the set bits of four ballot words (rows below it), or
-// -1 if its bit is clear.
-__device__ __forceinline__ int row_rank(const uint32_t *bal, int r)
-{
-    const int wr = r >> 5;
-    if (!((bal[wr] >> (r & 31)) & 1u))
-        return -1;
-    int rank = __popc(bal[wr] & ((1u << (r & 31)) - 1u));
-    for (int i = 0; i < wr; ++i)
-        rank += __popc(bal[i]);
-    return rank;
-}
-
-// Builds the patch record of K stage st (key tile jk of unit w, whose Q
-// tiles sit in slot qslot and whose ballots are those of unit parity up).
-// Runs in all 128 threads of the RoPE warpgroup after the ballots of the K
-// tile are visible; thread r stands for query row r of the Q tiles and key
-// row r of the K tile.  Without large rows it only clears the counts.
-template <int D, int GC, int ST, bool VAR, typename Sync>
-__device__ __forceinline__ bool patch_tile(uint8_t *smem, int r, int st, int jk, const FwdUnit &w,
-                                        int qslot, int up, const uint32_t *qbal,
-                                        const uint32_t *kbal, const AttnParams &p, Sync &rsync)
-{
-    using C = FwdCfg<D, GC, ST>;
-    using TL = Tile<D>;
-    constexpr int NOUT = C::NOUT;
-    uint8_t *rec = smem + C::OFF_PREC + st * C::PL::PREC_BYTES;
-    PatchHdr *hdr = reinterpret_cast<PatchHdr *>(rec);
-    __half *dk = reinterpret_cast<__half *>(rec + C::PL::PHDR_BYTES);   // [NOUT][GC][128]
-    __half *dq = dk + NOUT * GC * kRows;                               // [GC][NOUT][128]
-    const uint32_t *kb = kbal + st * 4;
-    const uint32_t *qb0 = qbal + up * GC * 4;
-    const int nk = __popc(kb[0]) + __popc(kb[1]) + __popc(kb[2]) + __popc(kb[3]);
-    int anyq = 0, overq = 0;
-#pragma unroll
-    for (int g = 0; g < GC; ++g) {
-        const uint32_t *qg = qb0 + g * 4;
-        const int n = __popc(qg[0]) + __popc(qg[1]) + __popc(qg[2]) + __popc(qg[3]);
-        anyq |= n;
-        overq |= n > NOUT ? 1 : 0;
-    }
-    if (nk == 0 && anyq == 0) {
-        if (r == 0) {
-            hdr->kcnt = 0;
-#pragma unroll
-            for (int g = 0; g < GC; ++g)
-                hdr->qcnt[g] = 0;
-        }
-        return true;
-    }
-    // ---- a tile with large rows: exact scores for their pairs ----
-    const int kc = nk < NOUT ? nk : NOUT;
-    if (r == 0 && (nk > NOUT || overq))
-        atomicOr(p.status, kDevPrecision);
-    const uint8_t *ktile = smem + C::OFF_K + st * TL::BYTES;
-    float *kov = reinterpret_cast<float *>(smem + C::OFF_KOV);                        // [NOUT][D]
-    float *qov = reinterpret_cast<float *>(smem + C::OFF_QOV) + up * GC * NOUT * D;   // [GC][NOUT][D]
+    using FS = FixScratch<D>;
+    constexpr int NT = FS::NT, D2 = D / 2, PPL = (D2 + 31) / 32;   // pairs per lane
+    const int tid = static_cast<int>(threadIdx.x), warp = tid / 32, lane = tid % 32;
     const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(p.q_in);
     const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(p.k_in);
-    const int t = w.m * kRows + r;   // this thread's query row
-    const int s = jk * kRows + r;    // this thread's key row
-    const __nv_bfloat16 *krow = kin + (seq_row(p, w.sq, s) * p.Hkv + w.j) * D;
-    auto qrow_ptr = [&](int g) { return qin + (seq_row(p, w.sq, t) * p.Hq + w.h0 + g) * D; };
-    // 1. the owners of large rows write their exact rotated vectors
-    const int krank = row_rank(kb, r);
-    if (krank >= 0 && krank < NOUT)
-        exact_pairs<D>(krow, static_cast<uint32_t>(s), p.rope, [&](int i, float x, float y) {
-            kov[krank * D + i] = x;
-            kov[krank * D + i + D / 2] = y;
-        });
-#pragma unroll 1
-    for (int g = 0; g < GC; ++g) {
-        const int qrank = row_rank(qb0 + g * 4, r);
-        if (qrank >= 0 && qrank < NOUT) {
-            float *dst = qov + (g * NOUT + qrank) * D;
-            exact_pairs<D>(qrow_ptr(g), static_cast<uint32_t>(t), p.rope,
-                           [&](int i, float x, float y) {
-                               dst[i] = x;
-                               dst[i + D / 2] = y;
-                           });
+    const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(p.v_in);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out0);
+    const float sl2 = p.scale_log2;
+    float *qv = scr + FS::QV, *part = scr + FS::PART, *kdat = scr + FS::KDAT, *dps = scr + FS::DPS;
+    int *kpos = reinterpret_cast<int *>(scr + FS::KPOS);
+    int *nkp = reinterpret_cast<int *>(scr + FS::NK);
+    for (int k = 0;; ++k) {
+        const int u = snake_unit(k, cta, P);
+        if (u >= p.num_units)
+            break;
+        const FwdUnit w = fwd_unit<VAR>(u, GC, p);
+        const uint32_t kvid = static_cast<uint32_t>(w.b * p.Hkv + w.j);
+        const int s_lo = w.lo * kRows, s_hi = w.m * kRows + kRows - 1;
+        bool anyq = false, anyk = false;
+        for (int i = 0; i < nflag; ++i) {
+            const uint64_t e = list[i];
+            const uint32_t kind = flag_kind(e);
+            anyq = anyq || (kind < static_cast<uint32_t>(GC) && flag_hi(e) == static_cast<uint32_t>(k));
+            anyk = anyk || (kind == kFlagKey && flag_hi(e) == kvid && flag_pos(e) >= s_lo &&
+                            flag_pos(e) <= s_hi);
         }
-    }
-    if (!rsync())
-        return false;
-    if (r == 0) {
-        hdr->kcnt = kc;
-        for (int o = 0; o < kc; ++o)
-            hdr->kcol[o] = nth_row(kb, o);
-        for (int g = 0; g < GC; ++g) {
-            const uint32_t *qg = qb0 + g * 4;
-            const int n = __popc(qg[0]) + __popc(qg[1]) + __popc(qg[2]) + __popc(qg[3]);
-            hdr->qcnt[g] = n < NOUT ? n : NOUT;
-            for (int o = 0; o < NOUT && o < n; ++o)
-                hdr->qrow[g][o] = nth_row(qg, o);
-        }
-    }
-    float dmax = 0.f;
-    // 2. pairs (query row r, large key o), every head: the exact score minus
-    //    the product of the fp16 operands the tensor cores see.  One pair
-    //    list entry at a time, so few registers stay live.
-#pragma unroll 1
-    for (int g = 0; g < GC; ++g) {
-        const uint8_t *qtile = smem + C::OFF_Q + (qslot * GC + g) * TL::BYTES;
-#pragma unroll 1
-        for (int o = 0; o < kc; ++o) {
-            const int kr = nth_row(kb, o);
-            const float *kv = kov + o * D;
-            float ae = 0.f, ah = 0.f;
-            if (t < w.sq.len)
-                exact_pairs<D>(qrow_ptr(g), static_cast<uint32_t>(t), p.rope,
-                               [&](int i, float x, float y) {
-                                   ae = fmaf(x, kv[i], fmaf(y, kv[i + D / 2], ae));
-                                   ah = fmaf(tile_f16<D>(qtile, r, i), tile_f16<D>(ktile, kr, i),
-                                             fmaf(tile_f16<D>(qtile, r, i + D / 2),
-                                                  tile_f16<D>(ktile, kr, i + D / 2), ah));
-                               });
-            dmax = fmaxf(dmax, fabsf(ae - ah));
-            dk[(o * GC + g) * kRows + r] = __float2half_rn(ae - ah);
-        }
-    }
-    // 3. pairs (large query row o of head g, key row r); a key that is itself
-    //    corrected in step 2 gets 0 here, so no pair is corrected twice
-    const bool key_patched = krank >= 0 && krank < NOUT;
-#pragma unroll 1
-    for (int g = 0; g < GC; ++g) {
-        const uint32_t *qg = qb0 + g * 4;
-        const int n = __popc(qg[0]) + __popc(qg[1]) + __popc(qg[2]) + __popc(qg[3]);
-        const int qc = n < NOUT ? n : NOUT;
-        const uint8_t *qtile = smem + C::OFF_Q + (qslot * GC + g) * TL::BYTES;
-#pragma unroll 1
-        for (int o = 0; o < qc; ++o) {
-            const int qr = nth_row(qg, o);
-            const float *qv = qov + (g * NOUT + o) * D;
-            float ae = 0.f, ah = 0.f;
-            if (s < w.sq.len && !key_patched)
-                exact_pairs<D>(krow, static_cast<uint32_t>(s), p.rope,
-                               [&](int i, float x, float y) {
-                                   ae = fmaf(x, qv[i], fmaf(y, qv[i + D / 2], ae));
-                                   ah = fmaf(tile_f16<D>(ktile, r, i), tile_f16<D>(qtile, qr, i),
-                                             fmaf(tile_f16<D>(ktile, r, i + D / 2),
-                                                  tile_f16<D>(qtile, qr, i + D / 2), ah));
-                               });
-            dmax = fmaxf(dmax, fabsf(ae - ah));
-            dq[(g * NOUT + o) * kRows + r] = __float2half_rn(ae - ah);
-        }
-    }
-    if (dmax > kFp16Max)
-        atomicOr(p.status, kDevRange);
-    return true;
-}
+        if (!anyq && !anyk)
+            continue;
 
-// Adds a K stage's exact-score corrections to the 64 raw scores a softmax
-// thread holds for query row r and key half `half` of head hrel: the column
-// of every large key row in this half, and every column if r is a large
-// query row of that head.
-template <int NOUT, int GC>
-__device__ __forceinline__ void apply_patches(uint32_t (&s)[2][32], const uint8_t *deltas,
-                                              const PatchHdr *hdr, int kc, int qc, int hrel,
-                                              int half, int r)
-{
-    const __half *dk = reinterpret_cast<const __half *>(deltas);   // [NOUT][GC][128]
-    const __half *dq = dk + NOUT * GC * kRows;                     // [GC][NOUT][128]
-    for (int o = 0; o < kc; ++o) {
-        const int col = hdr->kcol[o] - 64 * half;
-        if (col < 0 || col >= 64)
+        // ---- large query rows of the unit: recomputed exactly.  Keys are
+        // dealt to the 8 warps in turn, rotate-half pairs to the lanes; each
+        // warp keeps an online max / sum / O, merged in warp order.
+        for (int i = 0; i < nflag && anyq; ++i) {
+            const uint64_t e = list[i];
+            const int g = static_cast<int>(flag_kind(e));
+            if (g >= GC || flag_hi(e) != static_cast<uint32_t>(k))
+                continue;
+            const int t = flag_pos(e), h = w.h0 + g;
+            const size_t orow = static_cast<size_t>(seq_row(p, w.sq, t)) * p.Hq + h;
+            for (int pi = tid; pi < D2; pi += NT)
+                exact_pair(qin + orow * D, D2, static_cast<uint32_t>(t), p.rope, pi, qv[pi],
+                           qv[pi + D2]);
+            named_bar_sync(1, NT);
+            float qa[PPL], qb[PPL], acc[2 * PPL];
+#pragma unroll
+            for (int c = 0; c < PPL; ++c) {
+                const int pi = lane + 32 * c;
+                qa[c] = pi < D2 ? qv[pi] : 0.f;
+                qb[c] = pi < D2 ? qv[pi + D2] : 0.f;
+                acc[2 * c] = acc[2 * c + 1] = 0.f;
+            }
+            float m = -INFINITY, l = 0.f;
+            const int s0 = WIN ? max(0, t - p.window + 1) : 0;
+            for (int s = s0 + warp; s <= t; s += 8) {
+                const size_t krow = (static_cast<size_t>(seq_row(p, w.sq, s)) * p.Hkv + w.j) * D;
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < PPL; ++c) {
+                    const int pi = lane + 32 * c;
+                    if (pi < D2) {
+                        float a, b;
+                        exact_pair(kin + krow, D2, static_cast<uint32_t>(s), p.rope, pi, a, b);
+                        dot = fmaf(qa[c], a, fmaf(qb[c], b, dot));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    dot += __shfl_down_sync(0xffffffffu, dot, o);
+                const float sc = __shfl_sync(0xffffffffu, dot, 0) * sl2;   // log2 units
+                const float mn = fmaxf(m, sc);
+                const float a = exp2f(m - mn), pp = exp2f(sc - mn);
+                l = fmaf(l, a, pp);
+#pragma unroll
+                for (int c = 0; c < PPL; ++c) {
+                    const int pi = lane + 32 * c;
+                    if (pi < D2) {
+                        acc[2 * c] = fmaf(acc[2 * c], a, pp * __bfloat162float(vin[krow + pi]));
+                        acc[2 * c + 1] =
+                            fmaf(acc[2 * c + 1], a, pp * __bfloat162float(vin[krow + pi + D2]));
+                    }
+                }
+                m = mn;
+            }
+            float *pw = part + warp * (D + 2);
+            if (lane == 0) {
+                pw[0] = m;
+                pw[1] = l;
+            }
+#pragma unroll
+            for (int c = 0; c < PPL; ++c) {
+                const int pi = lane + 32 * c;
+                if (pi < D2) {
+                    pw[2 + pi] = acc[2 * c];
+                    pw[2 + pi + D2] = acc[2 * c + 1];
+                }
+            }
+            named_bar_sync(1, NT);
+            if (tid < D) {
+                float mt = -INFINITY;
+                for (int v = 0; v < 8; ++v)
+                    mt = fmaxf(mt, part[v * (D + 2)]);
+                float lt = 0.f, ot = 0.f;
+                for (int v = 0; v < 8; ++v) {
+                    const float mv = part[v * (D + 2)];
+                    if (mv == -INFINITY)
+                        continue;   // a warp that saw no key
+                    const float f = exp2f(mv - mt);
+                    lt = fmaf(part[v * (D + 2) + 1], f, lt);
+                    ot = fmaf(part[v * (D + 2) + 2 + tid], f, ot);
+                }
+                out[orow * D + tid] = __float2bfloat16_rn(ot / lt);
+                if (tid == 0)
+                    p.lse[(static_cast<size_t>(w.sq.bc) * p.Hq + h) * p.T + w.sq.base + t] =
+                        (mt + __log2f(lt)) * kLn2;
+            }
+            named_bar_sync(1, NT);   // qv and part are reused
+        }
+
+        // ---- rows that see the unit's large keys
+        if (!anyk)
             continue;
-        const float d = __half2float(dk[(o * GC + hrel) * kRows + r]);
+        if (tid == 0) {   // the keys in ascending order: a fixed summation order
+            int nk = 0;
+            for (int i = 0; i < nflag; ++i) {
+                const uint64_t e = list[i];
+                const int s = flag_pos(e);
+                if (flag_kind(e) != kFlagKey || flag_hi(e) != kvid || s < s_lo || s > s_hi)
+                    continue;
+                int j = nk++;
+                for (; j > 0 && kpos[j - 1] > s; --j)
+                    kpos[j] = kpos[j - 1];
+                kpos[j] = s;
+            }
+            *nkp = nk;
+        }
+        named_bar_sync(1, NT);
+        const int nk = *nkp;
+        for (int it = tid; it < nk * D2; it += NT) {
+            const int i = it / D2, pi = it % D2, s = kpos[i];
+            const size_t krow = (static_cast<size_t>(seq_row(p, w.sq, s)) * p.Hkv + w.j) * D;
+            float *kd = kdat + i * 3 * D;
+            float a, b;
+            exact_pair(kin + krow, D2, static_cast<uint32_t>(s), p.rope, pi, a, b);
+            kd[pi] = a;
+            kd[pi + D2] = b;
+            kd[D + pi] = as_f16(a);
+            kd[D + pi + D2] = as_f16(b);
+            kd[2 * D + pi] = __bfloat162float(vin[krow + pi]);
+            kd[2 * D + pi + D2] = __bfloat162float(vin[krow + pi + D2]);
+        }
+        named_bar_sync(1, NT);
+        for (int rr = tid; rr < GC * kRows; rr += NT) {
+            const int g = rr / kRows, t = w.m * kRows + rr % kRows, h = w.h0 + g;
+            if (t >= w.sq.len)
+                continue;
+            bool exact = false;   // a large query row, already recomputed
+            for (int i = 0; i < nflag; ++i)
+                exact = exact || list[i] == flag_entry(static_cast<uint32_t>(k),
+                                                        static_cast<uint32_t>(g),
+                                                        static_cast<uint32_t>(t));
+            if (exact)
+                continue;
+            const size_t orow = static_cast<size_t>(seq_row(p, w.sq, t)) * p.Hq + h;
+            float *lp = p.lse + (static_cast<size_t>(w.sq.bc) * p.Hq + h) * p.T + w.sq.base + t;
+            const float lse = __ldcg(lp), lse2 = lse * kLog2e;
+            float delta = 0.f;
+            bool any = false;
+            for (int i = 0; i < nk; ++i) {
+                const int s = kpos[i];
+                float dp = 0.f;
+                if (s <= t && (!WIN || t - s < p.window)) {
+                    const float *kd = kdat + i * 3 * D;
+                    float se = 0.f, sh = 0.f;
+                    for (int pi = 0; pi < D2; ++pi) {
+                        float a, b;
+                        exact_pair(qin + orow * D, D2, static_cast<uint32_t>(t), p.rope, pi, a, b);
+                        se = fmaf(a, kd[pi], fmaf(b, kd[pi + D2], se));
+                        sh = fmaf(as_f16(a), kd[D + pi], fmaf(as_f16(b), kd[D + pi + D2], sh));
+                    }
+                    dp = exp2f(se * sl2 - lse2) - exp2f(sh * sl2 - lse2);
+                    any = true;
+                }
+                dps[i * NT + tid] = dp;
+                delta += dp;
+            }
+            if (!any)
+                continue;
+            const float inv = 1.f / (1.f + delta);
+            uint4 *o4 = reinterpret_cast<uint4 *>(out + orow * D);
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v4 = __ldcg(o4 + c);
+                const uint32_t wv[4] = {v4.x, v4.y, v4.z, v4.w};
+                float x[8];
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+                for (int e = 0; e < 4; ++e) {
+                    x[2 * e] = bf16_lo(wv[e]);
+                    x[2 * e + 1] = bf16_hi(wv[e]);
+                }
+                for (int i = 0; i < nk; ++i) {
+                    const float dp = dps[i * NT + tid];
+                    const float *vv = kdat + i * 3 * D + 2 * D + 8 * c;
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-                if (32 * c + e == col)
-                    s[c][e] = __float_as_uint(__uint_as_float(s[c][e]) + d);
-    }
-    for (int o = 0; o < qc; ++o) {
-        if (hdr->qrow[hrel][o] != r)
-            continue;
-        const __half *row = dq + (hrel * NOUT + o) * kRows + 64 * half;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                s[c][e] = __float_as_uint(__uint_as_float(s[c][e]) + __half2float(row[32 * c + e]));
+                    for (int e = 0; e < 8; ++e)
+                        x[e] = fmaf(dp, vv[e], x[e]);
+                }
+                o4[c] = make_uint4(pack_bf16x2(x[0] * inv, x[1] * inv),
+                                   pack_bf16x2(x[2] * inv, x[3] * inv),
+                                   pack_bf16x2(x[4] * inv, x[5] * inv),
+                                   pack_bf16x2(x[6] * inv, x[7] * inv));
+            }
+            *lp = lse + log1pf(delta);
+        }
+        named_bar_sync(1, NT);   // kpos and kdat are reused
     }
 }
 
@@ -405,6 +449,7 @@ __global__ void __launch_bounds__(512, 1)
 {
     using C = FwdCfg<D, GC, ST>;
     using TL = Tile<D>;
+    static_assert(FixScratch<D>::BYTES <= C::OFF_SPL, "repair scratch fits the tile buffers");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -416,15 +461,16 @@ __global__ void __launch_bounds__(512, 1)
     // MMA (commit)
     __shared__ uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[2][2], bar_p_free[2][2];
     __shared__ uint64_t bar_o_free[2][C::NSL], bar_split, bar_drain;
+    // O staging block of group w written (its four warps) / read by its store
     __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
     // training path: the RoPE warps finished the n-th tile to be stored
     // (ring of 16: they are never 16 such tiles ahead of warp 15, which must
     // release a Q slot or a stored K stage before it is reloaded), and warp
     // 15's store has read a Q slot / K stage
     __shared__ uint64_t bar_sv[16], bar_q_rd[QB][GC], bar_k_rd[ST];
-    // patch record of stage st written (four RoPE warps); barrier of the RoPE
-    // warpgroup for the exact-score path
-    __shared__ uint64_t bar_patch[ST], bar_rsync;
+    // rows of large norm recorded by the RoPE warps
+    __shared__ uint64_t flag_list[kFlagCap];
+    __shared__ uint32_t flag_cnt;
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
 
@@ -447,9 +493,10 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(smem_u32(&bar_v_full[s]), 1);
             mbar_init(smem_u32(&bar_kv_empty[s]), 2);
             mbar_init(smem_u32(&bar_k_rd[s]), 1);
-            mbar_init(smem_u32(&bar_patch[s]), 4);
         }
-        mbar_init(smem_u32(&bar_rsync), 4);
+        flag_cnt = 0;
+        for (int i = 0; i < kFlagCap; ++i)
+            flag_list[i] = ~0ull;
         for (int w = 0; w < 2; ++w) {
             mbar_init(smem_u32(&bar_s_full[w]), 1);
             mbar_init(smem_u32(&bar_s_empty[w]), 4);
@@ -771,23 +818,10 @@ __global__ void __launch_bounds__(512, 1)
         // ------------------------------------------------------ RoPE ---
         regs_release<80>();
         const int r = threadIdx.x - 256;
-        const int rw = warp - 8;              // warp within the RoPE warpgroup
-        uint32_t *qbal = reinterpret_cast<uint32_t *>(smem + C::OFF_BAL);   // [2][GC][4]
-        uint32_t *kbal = qbal + 2 * GC * 4;                                  // [ST][4]
         float mx = 0.f;
         bool ok = true;
         int kt = 0;
         uint32_t nsv = 0;     // tiles handed to warp 15 (training path)
-        uint32_t nsync = 0;   // uses of bar_rsync
-        // bounded barrier of the four RoPE warps (all take the same path)
-        auto rsync = [&]() {
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&bar_rsync));
-            const bool r_ok = mbar_wait_warp(smem_u32(&bar_rsync), nsync & 1, wc);
-            ++nsync;
-            return r_ok;
-        };
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
             if (u >= p.num_units)
@@ -820,17 +854,14 @@ __global__ void __launch_bounds__(512, 1)
                 float ss;
                 mx = fmaxf(mx, rope_row_ilp<D>(tile, r, pos, p.rope, ss));
                 fence_proxy_async_smem();
-                // rows whose rotated vector is large get exact scores
-                const int limit = tu.sq.len;
-                const uint32_t bal =
-                    __ballot_sync(0xffffffffu, static_cast<int>(pos) < limit && ss > 2.f * D);
-                if (lane == 0) {
-                    if (isq)
-                        qbal[((qunit & 1) * GC + g) * 4 + rw] = bal;
-                    else
-                        kbal[st * 4 + rw] = bal;
-                }
-                __syncwarp();
+                // rows of large norm (rare): recorded for the repair
+                if (static_cast<int>(pos) < tu.sq.len && ss > 4.f * D)
+                    flag_row(flag_list, &flag_cnt,
+                             isq ? flag_entry(static_cast<uint32_t>(qunit), static_cast<uint32_t>(g),
+                                              pos)
+                                 : flag_entry(static_cast<uint32_t>(w.b * p.Hkv + w.j), kFlagKey,
+                                              pos),
+                             !isq, p.status);
                 const uint32_t ready =
                     isq ? smem_u32(&bar_q_ready[qb][g]) : smem_u32(&bar_k_ready[st]);
                 if (lane == 0)
@@ -840,20 +871,8 @@ __global__ void __launch_bounds__(512, 1)
                         mbar_arrive(smem_u32(&bar_sv[nsv % 16]));
                     ++nsv;
                 }
-                if (!isq) {
-                    // k_ready completes once all four warps have rotated the
-                    // tile and posted their ballots
-                    if (!mbar_wait_warp(smem_u32(&bar_k_ready[st]), (kt / ST) & 1, wc) ||
-                        !patch_tile<D, GC, ST, VAR>(smem, r, st, jk, w, k % QB, k & 1, qbal, kbal,
-                                                    p, rsync)) {
-                        ok = false;
-                        break;
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&bar_patch[st]));
+                if (!isq)
                     ++kt;
-                }
             }
         }
         if (mx > kFp16Max)
@@ -874,11 +893,10 @@ __global__ void __launch_bounds__(512, 1)
     const int r = threadIdx.x & 127;        // query row == TMEM lane
     const uint32_t lane_base = tmem_addr(tbase, q4 * 32, 0);
     const float sl2 = p.scale_log2;
-    uint8_t *stage = smem + C::OFF_O + wg * TL::BLOCK;
     float *split_ml = reinterpret_cast<float *>(smem + C::OFF_SPL);   // [m | l][row]
     bool ok = true;
     uint32_t n = 0;          // this group's items so far
-    uint32_t kts = 0;        // key tiles this group has started (K stage kts % ST)
+    uint8_t *stage = smem + C::OFF_O + wg * TL::BLOCK;
     uint32_t nepi = 0;       // O stores this group has issued
     float mr0 = 0.f, mr1 = 0.f, lr0 = 0.f, lr1 = 0.f;   // running max (log2 units) / sum per slot
     // Writes O_slot / l of head h (rows of this thread) and its lse.  With a
@@ -981,17 +999,7 @@ __global__ void __launch_bounds__(512, 1)
         if (u >= p.num_units)
             break;
         const FwdUnit un = fwd_unit<VAR>(u, GC, p);
-        for (int jk = un.lo; jk <= un.m && ok; ++jk, ++kts) {
-            // the K stage's patch record (exact scores of large rows): its
-            // counts are read once per key tile
-            const int pst = kts % ST;
-            if (!mbar_wait_warp(smem_u32(&bar_patch[pst]), (kts / ST) & 1, wc)) {
-                ok = false;
-                break;
-            }
-            const uint8_t *prec = smem + C::OFF_PREC + pst * C::PL::PREC_BYTES;
-            const PatchHdr *phdr = reinterpret_cast<const PatchHdr *>(prec);
-            const int pkc = phdr->kcnt;
+        for (int jk = un.lo; jk <= un.m && ok; ++jk) {
             for (int pi = 0; pi < GC; ++pi, ++n) {
                 const int pair = wg * GC + pi, hrel = pair >> 1, half = pair & 1;
                 const int slot = hrel - ((wg * GC) >> 1);
@@ -1014,10 +1022,6 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_u32(&bar_s_empty[wg]));
-                const int pqc = phdr->qcnt[hrel];
-                if (pkc > 0 || pqc > 0)
-                    apply_patches<C::NOUT, GC>(s, prec + C::PL::PHDR_BYTES, phdr, pkc, pqc, hrel,
-                                               half, r);
 
                 // causal mask on the diagonal tile (key > query row); with a
                 // sliding window also keys at or below row - W (local index
@@ -1207,10 +1211,16 @@ __global__ void __launch_bounds__(512, 1)
         }
     }
     if constexpr (C::STAGE) {
-        if (warp == 4 * wg && lane == 0)
-            bulk_wait0();
+        if (warp == 4 * wg && lane == 0) {
+            bulk_wait0();               // this group's O tiles are in global memory
+            fence_proxy_async_global();  // and visible to the generic loads below
+        }
     }
     teardown();
+    const int nflag = static_cast<int>(flag_cnt < kFlagCap ? flag_cnt : kFlagCap);
+    if (nflag > 0 && abort_s == 0u)
+        fix_large_rows<D, GC, WIN, VAR>(reinterpret_cast<float *>(smem), flag_list, nflag, cta, P,
+                                        p);
 }
 // ------------------------------------------------------------- launch ---
 

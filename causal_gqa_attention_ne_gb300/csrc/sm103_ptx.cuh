@@ -14,7 +14,7 @@ namespace ne {
 // Device status bits (the word is OR-ed; the host maps them to ne_status).
 constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevRange = 2u;
-constexpr uint32_t kDevPrecision = 4u;   // more large-norm rows in a tile than are scored exactly
+constexpr uint32_t kDevPrecision = 4u;   // more large-norm rows than a CTA records
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -147,6 +147,13 @@ __device__ __forceinline__ bool elect_one()
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's async-proxy (TMA) writes to global memory, already
+// complete, before its later generic accesses and those it synchronises with.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before()

@@ -52,16 +52,18 @@
  *
  * Score precision.  The forward rounds q' and k' to fp16 for the tensor
  * cores, so a score carries a rounding error proportional to |q'| |k'|.  A
- * row whose rotated vector has mean square above 2 (|x'|^2 > 2 d, e.g. a row
- * drawn at several times the scale of the others) is scored exactly instead:
- * for every pair with such a query or key row the forward adds the fp32
- * difference between the exact score and the fp16 one.  Up to 2 (d = 64) or
- * 4 (d = 32, 128) such rows per 128-row query tile and per 128-key tile are
- * handled; a tile with more records NE_WARN_PRECISION (its results are
- * complete, with the fp16 error on the pairs beyond that count).  Within
- * these limits lse is within 1e-3 absolute of the exact result for
- * unit-scale inputs, the stated tolerance.  The backward uses the fp16
- * scores throughout.
+ * row whose rotated vector has mean square above 4 (|x'|^2 > 4 d, e.g. a row
+ * drawn at several times the scale of the others; unit-variance rows reach
+ * it with probability below 1e-12) is scored exactly instead: the forward
+ * recomputes such a query row in fp32 from the bf16 inputs, and corrects
+ * every row that sees such a key row by the exact softmax weight of that
+ * pair.  The persistent forward runs one CTA per SM, each on a fixed share
+ * of the query tiles; each CTA handles up to 48 such rows (the large query
+ * rows of its tiles and the distinct large key rows they see).  Beyond that
+ * the call records NE_WARN_PRECISION (the results are complete, with the
+ * fp16 error on the pairs of the rows left over).  Within these limits lse
+ * is within 1e-3 absolute of the exact result for unit-scale inputs, the
+ * stated tolerance.  The backward uses the fp16 scores throughout.
  *
  * Errors.  Argument errors are returned synchronously and launch nothing.
  * Launch failures return NE_ERR_CUDA.  Device-side errors (a bounded wait
