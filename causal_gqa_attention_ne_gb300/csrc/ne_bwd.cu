@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const AttnParams p, const 
 // one warp-wide load covers 32 / (D/8) whole rows; RU such loads of O and of
 // dO are in flight per lane before the row sums are reduced with shuffles.
 // Persistent: four CTAs per SM (the register budget of RU loads in flight),
-// all resident at once, striding over the rows.
+// all resident at once, striding over the rows.  (Two rounds in flight per
+// warp, or bulk asynchronous copies into shared memory, measured slower.)
 constexpr int kDCtasPerSm = 4;
 template <int D>
 __global__ void __launch_bounds__(256, kDCtasPerSm) bwd_d_kernel(const AttnParams p)
@@ -195,6 +196,8 @@ __global__ void __launch_bounds__(256, kDCtasPerSm) bwd_d_kernel(const AttnParam
     const int lane = threadIdx.x % 32;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const size_t nwarps = static_cast<size_t>(gridDim.x) * blockDim.x / 32;
+    const bool small = nrows <= 0xFFFFFFFFull;
+    const uint32_t hq32 = static_cast<uint32_t>(p.Hq), t32 = static_cast<uint32_t>(p.T);
     griddep_wait();   // O comes from the previous grid
     for (size_t r0 = warp * RPW * RU; r0 < nrows; r0 += nwarps * RPW * RU) {
         uint4 ov[RU], gv[RU];
@@ -218,11 +221,21 @@ __global__ void __launch_bounds__(256, kDCtasPerSm) bwd_d_kernel(const AttnParam
                 acc += __shfl_xor_sync(0xffffffffu, acc, off);
             const size_t row = r0 + i * RPW + lane / LPR;   // ((b*T + t)*Hq + h)
             if (lane % LPR == 0 && row < nrows) {
-                const int h = static_cast<int>(row % p.Hq);
-                const size_t bt = row / p.Hq;
-                const int t = static_cast<int>(bt % p.T);
-                const int b = static_cast<int>(bt / p.T);
-                p.Dws[(static_cast<size_t>(b) * p.Hq + h) * p.T + t] = acc;
+                size_t h, t, b;
+                if (small) {   // 32-bit division where the row count allows it
+                    const uint32_t r32 = static_cast<uint32_t>(row);
+                    const uint32_t bt32 = r32 / hq32;
+                    const uint32_t b32 = bt32 / t32;
+                    h = r32 - bt32 * hq32;
+                    t = bt32 - b32 * t32;
+                    b = b32;
+                } else {
+                    h = row % p.Hq;
+                    const size_t bt = row / p.Hq;
+                    t = bt % p.T;
+                    b = bt / p.T;
+                }
+                p.Dws[(b * p.Hq + h) * p.T + t] = acc;
             }
         }
     }
