@@ -581,8 +581,13 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
     p.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                           ((rows * d * sizeof(float) + 255) &
                                            ~static_cast<size_t>(255)));
+    p.status = status;
+    p.wait_limit_ns = g_wait_limit_ns;
     fill_rope(p.rope, d, rope_theta);
-    return ne::launch_decode(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+    CUtensorMap mk, mv;
+    if (make_map(&mk, k_cache, B, Tk, Hkv, d) || make_map(&mv, v_cache, B, Tk, Hkv, d))
+        return NE_ERR_CUDA;
+    return ne::launch_decode(d, mk, mv, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? NE_OK
                : NE_ERR_CUDA;
 }

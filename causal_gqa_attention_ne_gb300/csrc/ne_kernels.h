@@ -49,9 +49,14 @@ struct DecodeParams {
     void *o;
     float *lse;
     float *part_o, *part_ml;
+    uint32_t *status;          // device status word (bounded waits)
+    uint64_t wait_limit_ns;
     RopeFreqs rope;
 };
-cudaError_t launch_decode(int d, const DecodeParams &p, cudaStream_t stream);
+// `k`, `v`: 4-D tensor maps of the caches (the layout of the training
+// kernels' k and v maps, T = Tk).
+cudaError_t launch_decode(int d, const CUtensorMap &k, const CUtensorMap &v,
+                          const DecodeParams &p, cudaStream_t stream);
 int decode_chunk_keys();
 
 // Padded variable-length batches.  varlen_plan lists the live work units of
