@@ -568,11 +568,14 @@ def run_window(args):
 def run_varlen(args):
     """The 116M SFT step: 16 layers of B64 sequences padded to T=512 (12/4
     heads, d64), each sequence with its own seeded valid length (ne_inputs:
-    uniform on [16, 512]); per layer ne_attn_fwd_varlen then ne_attn_bwd_varlen,
-    launched eagerly (the calls copy their unit tables from host memory, which
-    a CUDA graph cannot capture).  Algorithmic flops count the causal pairs of
-    the valid rows only.  The padded causal step (ne_attn_fwd + ne_attn_bwd on
-    the same buffers, also eager) is timed beside it."""
+    uniform on [16, 512]); per layer ne_attn_fwd_varlen_dev then
+    ne_attn_bwd_varlen_dev with the lengths in device memory, the 16 layers
+    captured as one CUDA graph (the unit tables are planned on the GPU).
+    Algorithmic flops count the causal pairs of the valid rows only.  Timed
+    beside it: the padded causal step (ne_attn_fwd + ne_attn_bwd on the same
+    buffers, also one graph) and the host-length entry points launched
+    eagerly (their tables are copied from host memory, which a graph cannot
+    capture)."""
     import numpy as np
     import torch
 
@@ -592,6 +595,14 @@ def run_varlen(args):
                               dtype=torch.uint8, device=dev)
         layers.append(x)
     sl = np.asarray(lens, dtype=np.int32)
+    sl_dev = torch.from_numpy(sl).to(dev)
+
+    def step_varlen_dev():
+        for d in layers:
+            ne.ne_attn_fwd_varlen_dev(d["q"], d["k"], d["v"], d["o"], d["lse"], sl_dev, d["ws"],
+                                      w.theta)
+            ne.ne_attn_bwd_varlen_dev(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"],
+                                      d["dq"], d["dk"], d["dv"], sl_dev, d["ws"], w.theta)
 
     def step_varlen():
         for d in layers:
@@ -604,6 +615,14 @@ def run_varlen(args):
             ne.ne_attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], w.theta)
             ne.ne_attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"],
                            d["dv"], d["ws"], w.theta)
+
+    def as_graph(step):
+        step()                                  # eager once: kernel attributes, checks
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+            step()
+        return g.replay
 
     def timed(step, sampler=None):
         for _ in range(max(args.warmup, 3)):
@@ -624,11 +643,12 @@ def run_varlen(args):
             sampler.mark(False)
         return e0.elapsed_time(e1) / args.steps
 
-    ms_pad = timed(step_padded)
+    ms_pad = timed(as_graph(step_padded))
+    ms_eager = timed(step_varlen)
     sampler = ClockSampler(0)
     sampler.start()
     time.sleep(0.3)
-    ms = timed(step_varlen, sampler)
+    ms = timed(as_graph(step_varlen_dev), sampler)
     sampler.stop()
     pairs = w.valid_pairs()
     flops = 14.0 * w.d * pairs * w.Hq * w.layers
@@ -644,12 +664,14 @@ def run_varlen(args):
         "config": {"workload": w.name, "valid_tokens": int(sum(lens)),
                    "padded_tokens": w.B * w.T, "valid_pair_fraction": pairs / (w.B * w.pairs),
                    "live_units": counts,
-                   "path": "ne_attn_fwd_varlen + ne_attn_bwd_varlen, eager"},
+                   "path": "ne_attn_fwd_varlen_dev + ne_attn_bwd_varlen_dev (lengths in device "
+                           "memory), one CUDA graph per step"},
         "valid_tokens_per_s": sum(lens) * w.layers / (ms * 1e-3),
         "padded_causal_ms_per_step": ms_pad,
         "speedup_vs_padded": ms_pad / ms,
+        "host_lengths_eager_ms_per_step": ms_eager,
         "pct_bf16_peak": value / peaks["bf16_tflops"] * 100.0,
-        "gpu_launches": 6 * w.layers * args.steps,
+        "gpu_launches": 8 * w.layers * args.steps,
         "clocks": sampler.summary(),
     }
 

@@ -31,6 +31,8 @@ from ._binding import (  # noqa: F401
     ne_attn_bwd_window,
     ne_attn_fwd_varlen,
     ne_attn_bwd_varlen,
+    ne_attn_fwd_varlen_dev,
+    ne_attn_bwd_varlen_dev,
     ne_attn_varlen_plan,
     ne_attn_varlen_workspace_size,
     ne_attn_packed_workspace_size,
@@ -46,6 +48,7 @@ __all__ = [
     "NE_STATUS", "NeAttnError", "attention_backward", "attention_decode", "attention_forward",
     "lib_path", "ne_attn_decode", "ne_attn_decode_workspace_size", "ne_attn_fwd_window",
     "ne_attn_bwd_window", "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan",
+    "ne_attn_fwd_varlen_dev", "ne_attn_bwd_varlen_dev",
     "ne_attn_varlen_workspace_size", "ne_attn_packed_workspace_size", "ne_attn_fwd_packed",
     "ne_attn_bwd_packed",
     "load_library", "ne_attn_bwd", "ne_attn_bwd_dkdv", "ne_attn_bwd_dq",

@@ -28,7 +28,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn
             "ne_attn_bwd_preprocess_d", "ne_attn_decode", "ne_attn_decode_workspace_size",
             "ne_attn_fwd_window", "ne_attn_bwd_window", "ne_attn_varlen_workspace_size",
             "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan",
-            "ne_attn_packed_workspace_size", "ne_attn_fwd_packed", "ne_attn_bwd_packed")
+            "ne_attn_packed_workspace_size", "ne_attn_fwd_packed", "ne_attn_bwd_packed",
+            "ne_attn_fwd_varlen_dev", "ne_attn_bwd_varlen_dev")
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +103,10 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_fwd_varlen.restype = i
         lib.ne_attn_bwd_varlen.argtypes = [vp] * 11 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd_varlen.restype = i
+        lib.ne_attn_fwd_varlen_dev.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd_varlen_dev.restype = i
+        lib.ne_attn_bwd_varlen_dev.argtypes = [vp] * 11 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_varlen_dev.restype = i
         lib.ne_attn_varlen_plan.argtypes = [vp] + [i] * 5 + [vp] * 3 + [sz, vp]
         lib.ne_attn_varlen_plan.restype = i
         lib.ne_attn_packed_workspace_size.argtypes = [i] * 5
@@ -491,6 +496,56 @@ def ne_attn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, seqlens, workspace,
                                            float(rope_theta), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd_varlen")
+
+
+def _dev_seqlens(seqlens, B: int):
+    """Lengths already in device memory: an int32 CUDA tensor of B entries."""
+    if not isinstance(seqlens, torch.Tensor) or seqlens.device.type != "cuda" or \
+            seqlens.dtype != torch.int32 or seqlens.numel() != B or not seqlens.is_contiguous():
+        raise ValueError(f"seqlens must be a contiguous int32 CUDA tensor of {B} lengths")
+    return seqlens.data_ptr()
+
+
+def ne_attn_fwd_varlen_dev(q, k, v, o, lse, seqlens, workspace, rope_theta: float = 10000.0,
+                           stream=None) -> None:
+    """ne_attn_fwd_varlen with the lengths in device memory (an int32 CUDA tensor):
+    the unit tables are planned on the GPU, so the call can be captured into a
+    CUDA graph and replayed with other lengths in the same tensor."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (B, T, Hq, d), bf)
+    _check(k, "k", (B, T, Hkv, d), bf)
+    _check(v, "v", (B, T, Hkv, d), bf)
+    _check(o, "o", (B, T, Hq, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    sp = _dev_seqlens(seqlens, B)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_fwd_varlen_dev(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), sp, wp, wbytes, B,
+                                               T, Hq, Hkv, d, float(rope_theta),
+                                               _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd_varlen_dev")
+
+
+def ne_attn_bwd_varlen_dev(q, k, v, o, lse, do, dq, dk, dv, seqlens, workspace,
+                           rope_theta: float = 10000.0, stream=None) -> None:
+    """ne_attn_bwd_varlen with the lengths in device memory (see ne_attn_fwd_varlen_dev)."""
+    B, T, Hq, Hkv, d = _dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (B, T, h, d), bf)
+    _check(lse, "lse", (B, Hq, T), torch.float32)
+    sp = _dev_seqlens(seqlens, B)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_varlen_dev(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), sp,
+                                               wp, wbytes, B, T, Hq, Hkv, d, float(rope_theta),
+                                               _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_varlen_dev")
 
 
 def _host_cu(cu_seqlens, total: int):

@@ -612,6 +612,8 @@ int ne_attn_get_error(void *stream)
         return NE_ERR_TIMEOUT;
     if (word & ne::kDevRange)
         return NE_ERR_RANGE;
+    if (word & ne::kDevArg)
+        return NE_ERR_ARG;
     if (word & ne::kDevPrecision)
         return NE_WARN_PRECISION;
     return NE_OK;
@@ -629,11 +631,13 @@ const char *ne_attn_status_string(int status)
     case NE_ERR_CUDA: return "CUDA call or kernel launch failed";
     case NE_ERR_TIMEOUT: return "a device-side bounded wait ran out";
     case NE_ERR_RANGE: return "an fp16 tensor-core operand exceeded 65504";
-    case NE_ERR_ARG: return "invalid argument (rope_theta must be finite and > 0)";
+    case NE_ERR_ARG:
+        return "invalid argument (rope_theta must be finite and > 0; a window, sequence length "
+               "or cu_seqlens out of range)";
     case NE_ERR_TOO_LARGE:
         return "shape needs more scratch than ne_attn_bwd_noalloc's fixed buffer holds";
     case NE_WARN_PRECISION:
-        return "a forward tile held more large-norm rows than are scored exactly";
+        return "a CTA of the forward met more large-norm rows than it repairs";
     default: return "unknown status";
     }
 }
@@ -659,12 +663,13 @@ int ne_attn_selftest_timeout(uint64_t limit_ns, void *stream)
 // ------------------------------------------------------------------------
 // Padded variable-length batches.  Workspace: the unit tables [seqlen: int32
 // B][forward units][dq units][dk/dv units], each region 256-byte aligned and
-// sized for every unit of the padded shape, then (backward) the backward
-// workspace of ne_attn_bwd.
+// sized for every unit of the padded shape, then the device-side plan's
+// counts (int32 [4]) and scratch (int32 [2 B + 2 (M + 2)]), then (backward)
+// the backward workspace of ne_attn_bwd.
 namespace {
 
 struct VarlenLayout {
-    size_t off_fwd, off_dq, off_dkv, tables, total;
+    size_t off_fwd, off_dq, off_dkv, off_cnt, off_scr, tables, total;
 };
 
 VarlenLayout varlen_layout(int B, int T, int Hq, int Hkv, int d)
@@ -678,7 +683,10 @@ VarlenLayout varlen_layout(int B, int T, int Hq, int Hkv, int d)
     L.off_fwd = al(sizeof(int32_t) * static_cast<size_t>(B));
     L.off_dq = L.off_fwd + al(sizeof(int32_t) * nf);
     L.off_dkv = L.off_dq + al(sizeof(int32_t) * nq);
-    L.tables = L.off_dkv + al(sizeof(int32_t) * tiles);
+    L.off_cnt = L.off_dkv + al(sizeof(int32_t) * tiles);
+    L.off_scr = L.off_cnt + al(sizeof(int32_t) * 4);
+    const size_t M = static_cast<size_t>((T + 127) / 128);
+    L.tables = L.off_scr + al(sizeof(int32_t) * (2 * static_cast<size_t>(B) + 2 * (M + 2)));
     L.total = L.tables + ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d);
     return L;
 }
@@ -732,6 +740,30 @@ const int *ws_int(void *workspace, size_t off)
     return reinterpret_cast<const int *>(static_cast<uint8_t *>(workspace) + off);
 }
 
+// The plan kernel: the tables, counts and lengths of `seqlens` (device
+// memory) into the workspace on `st`.
+int plan_on_device(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
+                   const VarlenLayout &L, void *workspace, uint32_t *status, cudaStream_t st)
+{
+    auto at = [&](size_t off) { return const_cast<int *>(ws_int(workspace, off)); };
+    const int G = Hq / Hkv;
+    ne::DevicePlanParams q;
+    q.seqlens_in = seqlens;
+    q.seqlen_out = at(0);
+    q.fwd_units = at(L.off_fwd);
+    q.dq_units = at(L.off_dq);
+    q.dkv_units = at(L.off_dkv);
+    q.counts = at(L.off_cnt);
+    q.scratch = at(L.off_scr);
+    q.B = B;
+    q.T = T;
+    q.Hkv = Hkv;
+    q.nch_fwd = G / ne::fwd_heads_per_cta(d, G);
+    q.nch_dq = G / ne::dq_heads_per_cta(d, G);
+    q.status = status;
+    return ne::launch_varlen_plan(q, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
 } // namespace
 
 extern "C" {
@@ -771,22 +803,35 @@ int ne_attn_varlen_plan(const int32_t *seqlens, int B, int T, int Hq, int Hkv, i
     return NE_OK;
 }
 
-int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
-                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
-                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+} // extern "C"
+
+namespace {
+
+// The padded variable-length forward and backward.  With dev_lengths the
+// lengths are in device memory and the plan kernel builds the tables (the
+// calls can be captured into a graph); otherwise the host builds them from
+// host lengths and copies them in.
+int fwd_varlen_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int32_t *seqlens, bool dev_lengths, void *workspace,
+                    size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                    float rope_theta, void *stream)
 {
     if (!q || !k || !v || !o || !lse || !workspace)
         return NE_ERR_NULL;
     int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
-    if ((rc = check_seqlens(seqlens, B, T)) != NE_OK)
+    // device lengths are checked by the plan kernel (NE_ERR_ARG through
+    // ne_attn_get_error)
+    if (dev_lengths && !seqlens)
+        return NE_ERR_NULL;
+    if (!dev_lengths && (rc = check_seqlens(seqlens, B, T)) != NE_OK)
         return rc;
     const VarlenLayout L = varlen_layout(B, T, Hq, Hkv, d);
     if (workspace_bytes < L.tables)
         return NE_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (dev_lengths && !aligned4(seqlens)))
         return NE_ERR_ALIGN;
     uint32_t *status = nullptr;
     if ((rc = device_state(&status)) != NE_OK)
@@ -804,12 +849,18 @@ int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, flo
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
         make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
         return NE_ERR_CUDA;
-    int counts[3];
-    if ((rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts)) != NE_OK)
+    int counts[3] = {1, 1, 1};
+    if (dev_lengths)
+        rc = plan_on_device(seqlens, B, T, Hq, Hkv, d, L, workspace, status, st);
+    else
+        rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts);
+    if (rc != NE_OK)
         return rc;
     p.seqlen = ws_int(workspace, 0);
     p.units = ws_int(workspace, L.off_fwd);
     p.num_units = counts[0];
+    if (dev_lengths)
+        p.unit_count = ws_int(workspace, L.off_cnt);
     if (counts[0] > 0 && ne::launch_fwd(d, mq, mk, mv, mo, mq, mk, p, st) != cudaSuccess)
         return NE_ERR_CUDA;
     ne::PadFillParams f;
@@ -825,23 +876,26 @@ int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, flo
     return ne::launch_pad_fill(f, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
-int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
-                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
-                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
-                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+int bwd_varlen_impl(const void *q, const void *k, const void *v, const void *o,
+                    const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                    const int32_t *seqlens, bool dev_lengths, void *workspace,
+                    size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                    float rope_theta, void *stream)
 {
     if (!o || !dq || !dk || !dv || !workspace)
         return NE_ERR_NULL;
     int rc = check_shape(B, T, Hq, Hkv, d, rope_theta);
     if (rc != NE_OK)
         return rc;
-    if ((rc = check_seqlens(seqlens, B, T)) != NE_OK)
+    if (dev_lengths && !seqlens)
+        return NE_ERR_NULL;
+    if (!dev_lengths && (rc = check_seqlens(seqlens, B, T)) != NE_OK)
         return rc;
     const VarlenLayout L = varlen_layout(B, T, Hq, Hkv, d);
     if (workspace_bytes < L.total)
         return NE_ERR_WORKSPACE;
     if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (dev_lengths && !aligned4(seqlens)))
         return NE_ERR_ALIGN;
     void *bws = static_cast<uint8_t *>(workspace) + L.tables;
     ne::AttnParams p;
@@ -851,8 +905,12 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
     if (rc != NE_OK)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int counts[3];
-    if ((rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts)) != NE_OK)
+    int counts[3] = {1, 1, 1};
+    if (dev_lengths)
+        rc = plan_on_device(seqlens, B, T, Hq, Hkv, d, L, workspace, p.status, st);
+    else
+        rc = upload_tables(seqlens, B, T, Hq, Hkv, d, L, workspace, st, counts);
+    if (rc != NE_OK)
         return rc;
     p.o_in = o;
     // the lengths let the preprocess skip padding rows
@@ -863,10 +921,14 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
         return NE_ERR_CUDA;
     p.units = ws_int(workspace, L.off_dq);
     p.num_units = counts[1];
+    if (dev_lengths)
+        p.unit_count = ws_int(workspace, L.off_cnt) + 1;
     if (counts[1] > 0 && (rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
         return rc;
     p.units = ws_int(workspace, L.off_dkv);
     p.num_units = counts[2];
+    if (dev_lengths)
+        p.unit_count = ws_int(workspace, L.off_cnt) + 2;
     if (counts[2] > 0 && (rc = run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st)) != NE_OK)
         return rc;
     ne::PadFillParams f;
@@ -883,6 +945,44 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
     f.Hq = Hq;
     f.seqlen = p.seqlen;
     return ne::launch_pad_fill(f, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+int ne_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    return fwd_varlen_impl(q, k, v, o, lse, seqlens, false, workspace, workspace_bytes, B, T, Hq,
+                           Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
+                       int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    return bwd_varlen_impl(q, k, v, o, lse, dO, dq, dk, dv, seqlens, false, workspace,
+                           workspace_bytes, B, T, Hq, Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_fwd_varlen_dev(const void *q, const void *k, const void *v, void *o, float *lse,
+                           const int32_t *seqlens_dev, void *workspace, size_t workspace_bytes,
+                           int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    return fwd_varlen_impl(q, k, v, o, lse, seqlens_dev, true, workspace, workspace_bytes, B, T,
+                           Hq, Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_bwd_varlen_dev(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                           const int32_t *seqlens_dev, void *workspace, size_t workspace_bytes,
+                           int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream)
+{
+    return bwd_varlen_impl(q, k, v, o, lse, dO, dq, dk, dv, seqlens_dev, true, workspace,
+                           workspace_bytes, B, T, Hq, Hkv, d, rope_theta, stream);
 }
 
 } // extern "C"

@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(384, 1)
     // memory is read and written, so wait for the previous grid in the stream
     // (programmatic dependent launch).
     griddep_wait();
+    const int NU = unit_total<VAR>(p);   // work units of the launch
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
     auto teardown = [&]() {
         tc_fence_before();
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(384, 1)
             int kt = 0, k = 0;
             for (; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
-                if (u >= p.num_units)
+                if (u >= NU)
                     break;
                 const DqUnit w = dq_unit<VAR>(u, GC, p);
                 for (int g = 0; g < GC && ok; ++g) {
@@ -575,7 +576,7 @@ __global__ void __launch_bounds__(384, 1)
                 const uint64_t dV0 = desc_kmajor_base<D>(sbase + C::OFF_V);
                 for (int k = 0; ok; ++k) {
                     const int u = snake_unit(k, cta, P);
-                    if (u >= p.num_units)
+                    if (u >= NU)
                         break;
                     const DqUnit w = dq_unit<VAR>(u, GC, p);
                     const int nitems = (w.m - w.lo + 1) * GC;
@@ -613,7 +614,7 @@ __global__ void __launch_bounds__(384, 1)
                 const uint64_t dKm0 = desc_mnmajor_base<D>(sbase + C::OFF_K);
                 for (int k = 0; ok; ++k) {
                     const int u = snake_unit(k, cta, P);
-                    if (u >= p.num_units)
+                    if (u >= NU)
                         break;
                     const DqUnit w = dq_unit<VAR>(u, GC, p);
                     const int nitems = (w.m - w.lo + 1) * GC;
@@ -674,7 +675,7 @@ __global__ void __launch_bounds__(384, 1)
             l2[g] = 0.f;
             dd[g] = 0.f;
         }
-        if (u >= p.num_units)
+        if (u >= NU)
             return;
         const DqUnit un = dq_unit<VAR>(u, GC, p);
         const int t = un.m * kRows + r;
@@ -770,7 +771,7 @@ __global__ void __launch_bounds__(384, 1)
     fetch(0, nl2, nD);
     for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, P);
-        if (u >= p.num_units)
+        if (u >= NU)
             break;
         const DqUnit un = dq_unit<VAR>(u, GC, p);
         float l2[GC], dd[GC];
@@ -1016,6 +1017,7 @@ __global__ void __launch_bounds__(512, 1)
     // memory is read and written, so wait for the previous grid in the stream
     // (programmatic dependent launch).
     griddep_wait();
+    const int NU = unit_total<VAR>(p);   // work units of the launch
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
     // Each role ends with its own copy of the teardown: warps run under
     // different register budgets after setmaxnreg, so their code paths never
@@ -1050,7 +1052,7 @@ __global__ void __launch_bounds__(512, 1)
             int gi = 0, k = 0;
             for (; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
-                if (u >= p.num_units)
+                if (u >= NU)
                     break;
                 const DkvUnit w = dkv_unit<VAR>(u, p);
                 const int kb = k % KB, ku = k / KB;
@@ -1129,7 +1131,7 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t b_pds_empty = smem_u32(&bar_pds_empty);
                 for (int k = 0; ok; ++k) {
                     const int u = snake_unit(k, cta, P);
-                    if (u >= p.num_units)
+                    if (u >= NU)
                         break;
                     const DkvUnit w = dkv_unit<VAR>(u, p);
                     const int kb = k % KB, ku = k / KB;
@@ -1180,7 +1182,7 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t b_pds_empty = smem_u32(&bar_pds_empty);
                 for (int k = 0; ok; ++k) {
                     const int u = snake_unit(k, cta, P);
-                    if (u >= p.num_units)
+                    if (u >= NU)
                         break;
                     const DkvUnit w = dkv_unit<VAR>(u, p);
                     const int kb = k % KB;
@@ -1240,7 +1242,7 @@ __global__ void __launch_bounds__(512, 1)
         float mx = 0.f;
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
-            if (u >= p.num_units)
+            if (u >= NU)
                 break;
             const DkvUnit w = dkv_unit<VAR>(u, p);
             // lse and D of the item's queries are fetched one item ahead so the
@@ -1332,7 +1334,7 @@ __global__ void __launch_bounds__(512, 1)
         };
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
-            if (u >= p.num_units)
+            if (u >= NU)
                 break;
             const DkvUnit un = dkv_unit<VAR>(u, p);
             for (int it = 0; it < un.nitems; ++it, ++gi) {
@@ -1450,7 +1452,9 @@ static cudaError_t launch_dq_w(const CUtensorMap &q, const CUtensorMap &k, const
     AttnParams p = p0;
     if (!VAR)
         p.num_units = p.M * p.B * p.Hkv * p.nchunks;   // varlen: the table's length
-    const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
+    // a count in device memory is unknown here: one CTA per SM
+    const int nu = (VAR && p.unit_count != nullptr) ? sms : p.num_units;
+    const unsigned grid = static_cast<unsigned>(nu < sms ? nu : sms);
     return launch_pdl(kern, grid, 384, C::SMEM_BYTES, stream, q, k, v, dO, dq, p);
 }
 
@@ -1514,7 +1518,9 @@ static cudaError_t launch_dkdv_w(const CUtensorMap &q, const CUtensorMap &k, con
     AttnParams p = p0;
     if (!VAR)
         p.num_units = p.M * p.B * p.Hkv;   // varlen: the table's length
-    const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
+    // a count in device memory is unknown here: one CTA per SM
+    const int nu = (VAR && p.unit_count != nullptr) ? sms : p.num_units;
+    const unsigned grid = static_cast<unsigned>(nu < sms ? nu : sms);
     return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, dO, p);
 }
 

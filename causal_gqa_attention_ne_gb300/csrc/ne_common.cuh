@@ -295,6 +295,7 @@ struct AttnParams {
     float *Dws;                  // backward: D = rowsum(dO * O), [B][Hq][T]
     uint32_t *status;            // device status word
     int num_units;               // persistent kernels: work units in the launch
+    const int *unit_count;       // varlen planned on the device: num_units there instead
     uint64_t wait_limit_ns;
     int save_rot;                // forward: also store Q' and K' (fp16) for the backward
     int window;                  // 0: causal; W > 0: query t sees keys t-W+1 .. t
@@ -311,6 +312,19 @@ struct AttnParams {
     int nseq;                    // packed: the number of sequences (cu has nseq + 1 entries)
     RopeFreqs rope;
 };
+
+// Work units of a persistent launch: num_units, or (variable-length batches
+// planned on the device) the count the plan kernel wrote.  Read after the
+// grid dependency wait.
+template <bool VAR>
+__device__ __forceinline__ int unit_total(const AttnParams &p)
+{
+    if constexpr (VAR) {
+        if (p.unit_count != nullptr)
+            return *p.unit_count;
+    }
+    return p.num_units;
+}
 
 // Where sequence b of a launch lives: the TMA batch coordinate bc and first
 // row base of its rows, and its valid rows len.  Plain and padded batches:

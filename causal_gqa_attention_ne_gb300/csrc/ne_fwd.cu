@@ -217,7 +217,7 @@ struct FixScratch {
 // around a barrier depends only on the list and the unit, so it is uniform.
 template <int D, int GC, bool WIN, bool VAR>
 __device__ __noinline__ void fix_large_rows(float *scr, const uint64_t *list, int nflag, int cta,
-                                            int P, const AttnParams &p)
+                                            int P, int NU, const AttnParams &p)
 {
     using FS = FixScratch<D>;
     constexpr int NT = FS::NT, D2 = D / 2, PPL = (D2 + 31) / 32;   // pairs per lane
@@ -232,7 +232,7 @@ __device__ __noinline__ void fix_large_rows(float *scr, const uint64_t *list, in
     int *nkp = reinterpret_cast<int *>(scr + FS::NK);
     for (int k = 0;; ++k) {
         const int u = snake_unit(k, cta, P);
-        if (u >= p.num_units)
+        if (u >= NU)
             break;
         const FwdUnit w = fwd_unit<VAR>(u, GC, p);
         const uint32_t kvid = static_cast<uint32_t>(w.b * p.Hkv + w.j);
@@ -527,6 +527,7 @@ __global__ void __launch_bounds__(512, 1)
     // memory is read and written, so wait for the previous grid in the stream
     // (programmatic dependent launch).
     griddep_wait();
+    const int NU = unit_total<VAR>(p);   // work units of the launch
     const WaitCtl wc{&abort_s, p.status, p.wait_limit_ns};
     // Each role ends with its own teardown: after setmaxnreg the warps run
     // under different register budgets, so their code paths never re-join.
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(512, 1)
             };
             for (int k = 0; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
-                if (u >= p.num_units)
+                if (u >= NU)
                     break;
                 const FwdUnit w = fwd_unit<VAR>(u, GC, p);
                 // order: [Q of this unit if not prefetched], K/V lo, [Q of the
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(512, 1)
                 if (QB == 1 || k == 0)
                     ok = load_q(k);
                 ok = ok && load_kv(w, w.lo);
-                if (QB == 2 && ok && snake_unit(k + 1, cta, P) < p.num_units)
+                if (QB == 2 && ok && snake_unit(k + 1, cta, P) < NU)
                     ok = load_q(k + 1);
                 for (int jk = w.lo + 1; jk <= w.m && ok; ++jk)
                     ok = load_kv(w, jk);
@@ -654,11 +655,11 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t nsv = 0;
             for (int k = 0; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
-                if (u >= p.num_units)
+                if (u >= NU)
                     break;
                 const FwdUnit w = fwd_unit<VAR>(u, GC, p);
                 const int nq0 = (QB == 1 || k == 0) ? GC : 0;
-                const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
+                const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < NU;
                 const int nq1 = has_next ? GC : 0;
                 for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
                     const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
@@ -754,7 +755,7 @@ __global__ void __launch_bounds__(512, 1)
             };
             for (int k = 0; ok; ++k) {
                 const int u = snake_unit(k, cta, P);
-                if (u >= p.num_units)
+                if (u >= NU)
                     break;
                 const FwdUnit w = fwd_unit<VAR>(u, GC, p);
                 const int qb = k % QB;
@@ -824,14 +825,14 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t nsv = 0;     // tiles handed to warp 15 (training path)
         for (int k = 0; ok; ++k) {
             const int u = snake_unit(k, cta, P);
-            if (u >= p.num_units)
+            if (u >= NU)
                 break;
             const FwdUnit w = fwd_unit<VAR>(u, GC, p);
             // Tiles in the order the producer loads them: [Q of this unit
             // unless prefetched], K 0, [Q of the next unit], K 1..m.  One call
             // site keeps the unrolled rotation in the instruction cache once.
             const int nq0 = (QB == 1 || k == 0) ? GC : 0;
-            const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < p.num_units;
+            const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < NU;
             const int nq1 = has_next ? GC : 0;
             const FwdUnit wn = has_next ? fwd_unit<VAR>(snake_unit(k + 1, cta, P), GC, p) : w;
             for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
@@ -996,7 +997,7 @@ __global__ void __launch_bounds__(512, 1)
     };
     for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, P);
-        if (u >= p.num_units)
+        if (u >= NU)
             break;
         const FwdUnit un = fwd_unit<VAR>(u, GC, p);
         for (int jk = un.lo; jk <= un.m && ok; ++jk) {
@@ -1220,7 +1221,7 @@ __global__ void __launch_bounds__(512, 1)
     const int nflag = static_cast<int>(flag_cnt < kFlagCap ? flag_cnt : kFlagCap);
     if (nflag > 0 && abort_s == 0u)
         fix_large_rows<D, GC, WIN, VAR>(reinterpret_cast<float *>(smem), flag_list, nflag, cta, P,
-                                        p);
+                                        NU, p);
 }
 // ------------------------------------------------------------- launch ---
 
@@ -1242,7 +1243,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap &q, const CUtensorMap &k, cons
     AttnParams p = p0;
     if (!VAR)
         p.num_units = p.M * p.B * p.Hkv * p.nchunks;   // varlen: the table's length
-    const unsigned grid = static_cast<unsigned>(p.num_units < sms ? p.num_units : sms);
+    // a count in device memory is unknown here: one CTA per SM
+    const int nu = (VAR && p.unit_count != nullptr) ? sms : p.num_units;
+    const unsigned grid = static_cast<unsigned>(nu < sms ? nu : sms);
     return launch_pdl(kern, grid, 512, C::SMEM_BYTES, stream, q, k, v, o, qs, ks, p);
 }
 

@@ -78,6 +78,18 @@ struct PadFillParams {
 };
 int varlen_plan(const int *seqlen, int B, int T, int Hq, int Hkv, int d, int *fwd_units,
                 int *dq_units, int *dkv_units, const size_t caps[3], int counts[3]);
+// Device-side plan of a padded variable-length batch: the tables of
+// varlen_plan (forward, dq, dk/dv, same contents and order) and the three
+// counts, from lengths in device memory, clamped to [0, T] (kDevArg recorded
+// for a length outside), copied to seqlen_out.  scratch holds 2 B + 2 (M + 2)
+// ints.
+struct DevicePlanParams {
+    const int *seqlens_in;
+    int *seqlen_out, *fwd_units, *dq_units, *dkv_units, *counts, *scratch;
+    int B, T, Hkv, nch_fwd, nch_dq;
+    uint32_t *status;
+};
+cudaError_t launch_varlen_plan(const DevicePlanParams &p, cudaStream_t stream);
 cudaError_t launch_pad_fill(const PadFillParams &p, cudaStream_t stream);
 
 // One-block kernel whose wait can never complete (checks the timeout path).

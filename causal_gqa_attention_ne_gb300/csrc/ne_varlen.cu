@@ -123,4 +123,164 @@ int varlen_plan(const int *seqlen, int B, int T, int Hq, int Hkv, int d, int *fw
     return 0;
 }
 
+// ----------------------------------------------------- device-side plan ---
+// The same tables, built on the GPU from lengths in device memory, so a
+// variable-length call can be captured into a CUDA graph and replayed with
+// other lengths.  One CTA of kPlanThreads threads.  Forward and dq tables:
+// the live units of each enumeration, compacted in order (a block-wide
+// scan per slice of the enumeration).  dk/dv table: the stable sort by
+// decreasing work has a closed form.  Unit u = n (B Hkv) + b Hkv + j is live
+// iff n < mt_b (mt_b = ceil(L_b / 128)) and has work w = mt_b - n; among the
+// units of work w, ordered by u, the one of (b, j) comes after the units of
+// every b' with w <= mt_b' < mt_b, then those of every b' < b with
+// mt_b' = mt_b, then j of its own.  With C(w) = #{b : mt_b >= w}:
+//   pos = Hkv sum_{w' > w} C(w') + Hkv (C(w) - C(mt_b) + eq_b) + j,
+// eq_b = #{b' < b : mt_b' = mt_b}.  Lengths outside [0, T] are clamped and
+// recorded in the status word.
+constexpr int kPlanThreads = 1024;
+
+// Exclusive scan of one int per thread over the block; returns the block's
+// total through *total.
+__device__ int block_excl_scan(int x, int *warp_sums, int *total)
+{
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = kPlanThreads / 32;
+        int v = lane < nw ? warp_sums[lane] : 0;
+        int w_incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w_incl, o);
+            if (lane >= o)
+                w_incl += y;
+        }
+        if (lane < nw)
+            warp_sums[lane] = w_incl - v;   // exclusive
+        if (lane == nw - 1)
+            *total = w_incl;
+    }
+    __syncthreads();
+    const int r = warp_sums[warp] + incl - x;
+    __syncthreads();   // warp_sums is reused by the next call
+    return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) varlen_plan_kernel(const DevicePlanParams p)
+{
+    __shared__ int warp_sums[kPlanThreads / 32];
+    __shared__ int total_s;
+    const int tid = threadIdx.x;
+    const int M = (p.T + kRows - 1) / kRows;
+    int *mt = p.scratch;                  // [B]
+    int *eq = mt + p.B;                   // [B]
+    int *cge = eq + p.B;                  // [M + 2]: C(w)
+    int *start = cge + (M + 2);           // [M + 2]: Hkv sum_{w' > w} C(w')
+    griddep_wait();
+    // lengths (clamped), tiles, and the histogram of tiles (into cge)
+    for (int i = tid; i < M + 2; i += kPlanThreads)
+        cge[i] = 0;
+    __syncthreads();
+    for (int b = tid; b < p.B; b += kPlanThreads) {
+        int L = p.seqlens_in[b];
+        if (L < 0 || L > p.T) {
+            atomicOr(p.status, kDevArg);
+            L = L < 0 ? 0 : p.T;
+        }
+        p.seqlen_out[b] = L;
+        mt[b] = (L + kRows - 1) / kRows;
+        atomicAdd(cge + mt[b], 1);
+    }
+    __syncthreads();
+    // eq_b: earlier sequences with as many tiles
+    for (int b = tid; b < p.B; b += kPlanThreads) {
+        int c = 0;
+        for (int b2 = 0; b2 < b; ++b2)
+            c += mt[b2] == mt[b] ? 1 : 0;
+        eq[b] = c;
+    }
+    // C(w) = sum_{L >= w} hist(L): a suffix scan (reversed exclusive scan
+    // plus the element), slice by slice from the top
+    {
+        int carry = 0;
+        for (int i0 = 0; i0 < M + 2; i0 += kPlanThreads) {
+            const int w = M + 1 - (i0 + tid);           // descending
+            const int h = w >= 0 ? cge[w] : 0;
+            const int ex = block_excl_scan(h, warp_sums, &total_s);
+            if (w >= 0)
+                cge[w] = carry + ex + h;
+            carry += total_s;
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+    // start(w) = Hkv sum_{w' > w, w' >= 1} C(w') (works 1..M)
+    {
+        int carry = 0;
+        for (int i0 = 0; i0 < M + 2; i0 += kPlanThreads) {
+            const int w = M + 1 - (i0 + tid);
+            const int c = (w >= 1 && w <= M) ? cge[w] : 0;
+            const int ex = block_excl_scan(c, warp_sums, &total_s);
+            if (w >= 0)
+                start[w] = p.Hkv * (carry + ex);
+            carry += total_s;
+            __syncthreads();
+        }
+        if (tid == 0)
+            p.counts[2] = p.Hkv * carry;
+    }
+    __syncthreads();
+    // forward and dq tables: the live units in enumeration order
+    for (int k = 0; k < 2; ++k) {
+        const int nch = k == 0 ? p.nch_fwd : p.nch_dq;
+        int *table = k == 0 ? p.fwd_units : p.dq_units;
+        const long long per_m = static_cast<long long>(p.B) * p.Hkv * nch;
+        const long long n = per_m * M;
+        int base = 0;
+        for (long long i0 = 0; i0 < n; i0 += kPlanThreads) {
+            const long long u = i0 + tid;
+            bool live = false;
+            if (u < n) {
+                const int m = M - 1 - static_cast<int>(u / per_m);
+                const int b = static_cast<int>((u % per_m) / nch / p.Hkv);
+                live = m < mt[b];
+            }
+            const int ex = block_excl_scan(live ? 1 : 0, warp_sums, &total_s);
+            if (live)
+                table[base + ex] = static_cast<int>(u);
+            base += total_s;
+            __syncthreads();
+        }
+        if (tid == 0)
+            p.counts[k] = base;
+    }
+    // dk/dv table: each live unit straight to its position
+    const long long per_n = static_cast<long long>(p.B) * p.Hkv;
+    for (long long u = tid; u < per_n * M; u += kPlanThreads) {
+        const int n = static_cast<int>(u / per_n);
+        const int b = static_cast<int>((u % per_n) / p.Hkv);
+        const int j = static_cast<int>(u % p.Hkv);
+        if (n < mt[b]) {
+            const int w = mt[b] - n;
+            p.dkv_units[start[w] + p.Hkv * (cge[w] - cge[mt[b]] + eq[b]) + j] =
+                static_cast<int>(u);
+        }
+    }
+    griddep_launch_dependents();
+}
+
+cudaError_t launch_varlen_plan(const DevicePlanParams &p, cudaStream_t stream)
+{
+    return launch_pdl(varlen_plan_kernel, 1, kPlanThreads, 0, stream, p);
+}
+
 } // namespace ne

@@ -15,6 +15,7 @@ namespace ne {
 constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevRange = 2u;
 constexpr uint32_t kDevPrecision = 4u;   // more large-norm rows than a CTA records
+constexpr uint32_t kDevArg = 8u;         // a device-resident argument out of range
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

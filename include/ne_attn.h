@@ -91,7 +91,8 @@ typedef enum {
     NE_ERR_CUDA = 6,        /* a CUDA runtime / driver call or a launch failed */
     NE_ERR_TIMEOUT = 7,     /* a device-side bounded wait ran out (reported by get_error) */
     NE_ERR_RANGE = 8,       /* an fp16 tensor-core operand overflowed (reported by get_error) */
-    NE_ERR_ARG = 9,         /* another invalid argument (rope_theta <= 0, NaN, ...) */
+    NE_ERR_ARG = 9,         /* another invalid argument (rope_theta <= 0, NaN, a length
+                               out of range, ...) */
     NE_ERR_TOO_LARGE = 10,  /* ne_attn_bwd_noalloc: shape exceeds its fixed scratch */
     NE_WARN_PRECISION = 11  /* a forward tile held more large-norm rows than it scores exactly
                                (reported by get_error; see "Score precision" above) */
@@ -240,7 +241,8 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
  *   seqlens    int32 [B], HOST memory, read during the call only
  *   workspace  caller-owned device memory (16-byte aligned, no initial
  *              contents) of at least ne_attn_varlen_workspace_size() bytes;
- *              the forward uses only its first part (the work-unit tables)
+ *              the forward uses only its first part (the work-unit tables,
+ *              with room for the device-side plan's counts and scratch)
  * ne_attn_fwd_varlen writes o and lse like ne_attn_fwd on valid rows, and
  * o = 0, lse = -inf on padding rows.  ne_attn_bwd_varlen takes o and lse
  * from ne_attn_fwd_varlen and writes the gradients of the sum of O * dO over
@@ -252,10 +254,10 @@ int ne_attn_decode(const void *q, const void *k_cache, const void *v_cache, void
  * them, with zero weight, before the padding is overwritten.  Query tiles
  * (and, in the backward, key tiles) wholly past a sequence's end are
  * skipped, and the backward's preprocess does not read padding rows.  The library
- * builds the tables of live work
- * units on the host and copies them into the workspace with an asynchronous
- * copy from pageable memory, so these calls cannot be captured into a CUDA
- * graph; calls that share a workspace must not overlap on the GPU.
+ * builds the tables of live work units on the host and copies them into the
+ * workspace with an asynchronous copy from pageable memory, so these calls
+ * cannot be captured into a CUDA graph (the _dev variants below can); calls
+ * that share a workspace must not overlap on the GPU.
  * Errors as for ne_attn_fwd / ne_attn_bwd; seqlens NULL gives NE_ERR_NULL, a
  * length outside [0, T] NE_ERR_ARG.  ne_attn_varlen_workspace_size returns 0
  * for an invalid shape.
@@ -268,6 +270,27 @@ int ne_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *
                        const float *lse, const void *dO, void *dq, void *dk, void *dv,
                        const int32_t *seqlens, void *workspace, size_t workspace_bytes, int B,
                        int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+
+/*
+ * The same with the lengths in DEVICE memory: seqlens_dev int32 [B], 4-byte
+ * aligned, read by the GPU in stream order (so a preceding kernel may write
+ * it).  A planning kernel builds the tables of live work units in the
+ * workspace (the same tables, in the same order, as the host entry points)
+ * and the persistent kernels read their unit counts from there, launching
+ * one CTA per SM; the host never needs the lengths, so these calls can be
+ * captured into a CUDA graph and the graph replayed with other lengths
+ * written into the same buffer.  Results equal the host-length entry
+ * points' bit for bit.  A length outside [0, T] is clamped into it and
+ * reported as NE_ERR_ARG by ne_attn_get_error; seqlens_dev NULL gives
+ * NE_ERR_NULL.  Workspace and everything else as above.
+ */
+int ne_attn_fwd_varlen_dev(const void *q, const void *k, const void *v, void *o, float *lse,
+                           const int32_t *seqlens_dev, void *workspace, size_t workspace_bytes,
+                           int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
+int ne_attn_bwd_varlen_dev(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                           const int32_t *seqlens_dev, void *workspace, size_t workspace_bytes,
+                           int B, int T, int Hq, int Hkv, int d, float rope_theta, void *stream);
 
 /*
  * Packed variable-length batches: the sequences concatenated along the rows,
@@ -320,8 +343,9 @@ int ne_attn_varlen_plan(const int32_t *seqlens, int B, int T, int Hq, int Hkv, i
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status of
- * the current device: NE_ERR_TIMEOUT, NE_ERR_RANGE or NE_WARN_PRECISION (in
- * that order of precedence) if a kernel recorded one since the last call,
+ * the current device: NE_ERR_TIMEOUT, NE_ERR_RANGE, NE_ERR_ARG (a length in
+ * device memory out of range) or NE_WARN_PRECISION (in that order of
+ * precedence) if a kernel recorded one since the last call,
  * NE_ERR_CUDA if the stream reports a CUDA error, else NE_OK.
  */
 int ne_attn_get_error(void *stream);

@@ -103,6 +103,20 @@ def test_backward_argument_errors(lib):
         assert lib.ne_attn_bwd(*bad, a, 1 << 20, 1, 8, 2, 2, 64, 10000.0, None) == 4
 
 
+def test_varlen_device_lengths_argument_errors(lib):
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    ws = ne.ne_attn_varlen_workspace_size(2, 8, 2, 2, 64)
+    args = (2, 8, 2, 2, 64, 10000.0, None)
+    fwd, bwd = lib.ne_attn_fwd_varlen_dev, lib.ne_attn_bwd_varlen_dev
+    assert fwd(a, a, a, a, a, None, a, ws, *args) == 1                # NE_ERR_NULL: seqlens
+    assert fwd(a, a, a, a, a, a + 2, a, ws, *args) == 4               # lengths 4-byte aligned
+    assert fwd(a, a, a, a, a, a, a, 16, *args) == 5                   # short workspace
+    assert fwd(a, a, a, a, a, a, a, ws, 2, 8, 3, 2, 64, 10000.0, None) == 2
+    assert bwd(*([a] * 9), None, a, ws, *args) == 1
+    assert bwd(*([a] * 9), a, a, ws - 1, *args) == 5
+
+
 def test_decode_workspace_size_and_argument_errors(lib):
     def r256(x):
         return (x + 255) // 256 * 256

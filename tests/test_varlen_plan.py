@@ -92,7 +92,10 @@ def test_workspace_size():
     for (B, T, Hq, Hkv, d) in ((64, 512, 12, 4, 64), (3, 7, 5, 1, 32), (2, 1000, 16, 4, 128)):
         G, tiles = Hq // Hkv, (T + 127) // 128 * B * Hkv
         nf, nq = chunks(d, G)
-        tables = r256(4 * B) + r256(4 * tiles * nf) + r256(4 * tiles * nq) + r256(4 * tiles)
+        M = (T + 127) // 128
+        # + the device-side plan's counts (int32 [4]) and scratch (int32 [2B + 2(M + 2)])
+        tables = r256(4 * B) + r256(4 * tiles * nf) + r256(4 * tiles * nq) + r256(4 * tiles) + \
+            r256(16) + r256(4 * (2 * B + 2 * (M + 2)))
         assert ne.ne_attn_varlen_workspace_size(B, T, Hq, Hkv, d) == \
             tables + ne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, d)
     assert ne.ne_attn_varlen_workspace_size(1, 8, 3, 2, 64) == 0      # Hq % Hkv != 0
