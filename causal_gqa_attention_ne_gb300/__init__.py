@@ -38,6 +38,8 @@ from ._binding import (  # noqa: F401
     ne_attn_packed_workspace_size,
     ne_attn_fwd_packed,
     ne_attn_bwd_packed,
+    ne_attn_fwd_packed_dev,
+    ne_attn_bwd_packed_dev,
     ne_attn_get_error,
     ne_attn_selftest_timeout,
     ne_attn_set_wait_limit_ns,
@@ -50,7 +52,7 @@ __all__ = [
     "ne_attn_bwd_window", "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan",
     "ne_attn_fwd_varlen_dev", "ne_attn_bwd_varlen_dev",
     "ne_attn_varlen_workspace_size", "ne_attn_packed_workspace_size", "ne_attn_fwd_packed",
-    "ne_attn_bwd_packed",
+    "ne_attn_bwd_packed", "ne_attn_fwd_packed_dev", "ne_attn_bwd_packed_dev",
     "load_library", "ne_attn_bwd", "ne_attn_bwd_dkdv", "ne_attn_bwd_dq",
     "ne_attn_bwd_noalloc", "ne_attn_bwd_noalloc_max_scratch", "ne_attn_fwd_save",
     "ne_attn_bwd_saved", "ne_attn_bwd_preprocess_d",

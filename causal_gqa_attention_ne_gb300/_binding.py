@@ -29,7 +29,8 @@ EXPORTED = ("ne_attn_fwd", "ne_attn_bwd", "ne_attn_bwd_workspace_size", "ne_attn
             "ne_attn_fwd_window", "ne_attn_bwd_window", "ne_attn_varlen_workspace_size",
             "ne_attn_fwd_varlen", "ne_attn_bwd_varlen", "ne_attn_varlen_plan",
             "ne_attn_packed_workspace_size", "ne_attn_fwd_packed", "ne_attn_bwd_packed",
-            "ne_attn_fwd_varlen_dev", "ne_attn_bwd_varlen_dev")
+            "ne_attn_fwd_varlen_dev", "ne_attn_bwd_varlen_dev", "ne_attn_fwd_packed_dev",
+            "ne_attn_bwd_packed_dev")
 
 _lock = threading.Lock()
 _lib = None
@@ -115,6 +116,10 @@ def load_library(build_if_missing: bool = True):
         lib.ne_attn_fwd_packed.restype = i
         lib.ne_attn_bwd_packed.argtypes = [vp] * 11 + [sz] + [i] * 5 + [f, vp]
         lib.ne_attn_bwd_packed.restype = i
+        lib.ne_attn_fwd_packed_dev.argtypes = [vp] * 7 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_fwd_packed_dev.restype = i
+        lib.ne_attn_bwd_packed_dev.argtypes = [vp] * 11 + [sz] + [i] * 5 + [f, vp]
+        lib.ne_attn_bwd_packed_dev.restype = i
         _lib = lib
         return lib
 
@@ -606,6 +611,57 @@ def ne_attn_bwd_packed(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, workspace,
                                            Hq, Hkv, d, float(rope_theta), _stream_ptr(stream))
     if rc:
         raise NeAttnError(rc, "ne_attn_bwd_packed")
+
+
+def _dev_cu(cu_seqlens):
+    """A prefix array already in device memory: an int32 CUDA tensor of nseq + 1 entries."""
+    if not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.device.type != "cuda" or \
+            cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or \
+            cu_seqlens.numel() < 2 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 CUDA tensor of nseq + 1 offsets")
+    return cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
+
+
+def ne_attn_fwd_packed_dev(q, k, v, o, lse, cu_seqlens, workspace, rope_theta: float = 10000.0,
+                           stream=None) -> None:
+    """ne_attn_fwd_packed with cu_seqlens in device memory (an int32 CUDA tensor):
+    the unit tables are planned on the GPU, so the call can be captured into a
+    CUDA graph and replayed with other offsets in the same tensor."""
+    total, Hq, Hkv, d = _packed_dims(q, k)
+    bf = torch.bfloat16
+    _check(q, "q", (total, Hq, d), bf)
+    _check(k, "k", (total, Hkv, d), bf)
+    _check(v, "v", (total, Hkv, d), bf)
+    _check(o, "o", (total, Hq, d), bf)
+    _check(lse, "lse", (Hq, total), torch.float32)
+    cp, nseq = _dev_cu(cu_seqlens)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_fwd_packed_dev(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), cp, wp, wbytes,
+                                               nseq, total, Hq, Hkv, d, float(rope_theta),
+                                               _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_fwd_packed_dev")
+
+
+def ne_attn_bwd_packed_dev(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens, workspace,
+                           rope_theta: float = 10000.0, stream=None) -> None:
+    """ne_attn_bwd_packed with cu_seqlens in device memory (see ne_attn_fwd_packed_dev)."""
+    total, Hq, Hkv, d = _packed_dims(q, k)
+    bf = torch.bfloat16
+    for x, n, h in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (do, "do", Hq),
+                    (dq, "dq", Hq), (dk, "dk", Hkv), (dv, "dv", Hkv)):
+        _check(x, n, (total, h, d), bf)
+    _check(lse, "lse", (Hq, total), torch.float32)
+    cp, nseq = _dev_cu(cu_seqlens)
+    wp, wbytes = _workspace_ptr(workspace)
+    rc = load_library().ne_attn_bwd_packed_dev(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cp,
+                                               wp, wbytes, nseq, total, Hq, Hkv, d,
+                                               float(rope_theta), _stream_ptr(stream))
+    if rc:
+        raise NeAttnError(rc, "ne_attn_bwd_packed_dev")
 
 
 def attention_forward(q, k, v, rope_theta: float = 10000.0, stream=None):

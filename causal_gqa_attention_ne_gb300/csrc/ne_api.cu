@@ -748,6 +748,7 @@ int plan_on_device(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
     auto at = [&](size_t off) { return const_cast<int *>(ws_int(workspace, off)); };
     const int G = Hq / Hkv;
     ne::DevicePlanParams q;
+    std::memset(&q, 0, sizeof(q));
     q.seqlens_in = seqlens;
     q.seqlen_out = at(0);
     q.fwd_units = at(L.off_fwd);
@@ -757,6 +758,7 @@ int plan_on_device(const int32_t *seqlens, int B, int T, int Hq, int Hkv, int d,
     q.scratch = at(L.off_scr);
     q.B = B;
     q.T = T;
+    q.M = (T + 127) / 128;
     q.Hkv = Hkv;
     q.nch_fwd = G / ne::fwd_heads_per_cta(d, G);
     q.nch_dq = G / ne::dq_heads_per_cta(d, G);
@@ -996,12 +998,13 @@ int ne_attn_bwd_varlen_dev(const void *q, const void *k, const void *v, const vo
 // rows past the sequence inside its last tile are masked like padding and
 // stored row by row, so a tile never writes the next sequence's rows.
 // Workspace: [lengths int32 nseq][cu int32 nseq+1][forward units][dq
-// units][dk/dv units], each region 256-byte aligned, then (backward) the
-// backward workspace of a [1][total] batch.
+// units][dk/dv units][device-side plan: counts, scratch], each region
+// 256-byte aligned, then (backward) the backward workspace of a [1][total]
+// batch.
 namespace {
 
 struct PackedLayout {
-    size_t off_cu, off_fwd, off_dq, off_dkv, tables, total;
+    size_t off_cu, off_fwd, off_dq, off_dkv, off_cnt, off_scr, tables, total;
 };
 
 PackedLayout packed_layout(int nseq, int total, int Hq, int Hkv, int d)
@@ -1018,7 +1021,11 @@ PackedLayout packed_layout(int nseq, int total, int Hq, int Hkv, int d)
     L.off_fwd = L.off_cu + al(sizeof(int32_t) * (static_cast<size_t>(nseq) + 1));
     L.off_dq = L.off_fwd + al(sizeof(int32_t) * nf);
     L.off_dkv = L.off_dq + al(sizeof(int32_t) * nq);
-    L.tables = L.off_dkv + al(sizeof(int32_t) * tiles);
+    // the device-side plan: counts, then scratch for M = ceil(total / 128)
+    L.off_cnt = L.off_dkv + al(sizeof(int32_t) * tiles);
+    L.off_scr = L.off_cnt + al(sizeof(int32_t) * 4);
+    const size_t M = static_cast<size_t>((total + 127) / 128);
+    L.tables = L.off_scr + al(sizeof(int32_t) * (2 * static_cast<size_t>(nseq) + 2 * (M + 2)));
     L.total = L.tables + ne_attn_bwd_workspace_size(1, total, Hq, Hkv, d);
     return L;
 }
@@ -1094,22 +1101,74 @@ size_t ne_attn_packed_workspace_size(int nseq, int total, int Hq, int Hkv, int d
     return packed_layout(nseq, total, Hq, Hkv, d).total;
 }
 
-int ne_attn_fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
-                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
-                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
-                       void *stream)
+} // extern "C"
+
+namespace {
+
+// The plan kernel on a packed batch's prefix array (device memory).
+int plan_packed_on_device(const int32_t *cu, int nseq, int total, int Hq, int Hkv, int d,
+                          const PackedLayout &L, void *workspace, uint32_t *status,
+                          cudaStream_t st)
+{
+    auto at = [&](size_t off) { return const_cast<int *>(ws_int(workspace, off)); };
+    const int G = Hq / Hkv;
+    ne::DevicePlanParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.cu_in = cu;
+    q.cu_out = at(L.off_cu);
+    q.seqlen_out = at(0);
+    q.fwd_units = at(L.off_fwd);
+    q.dq_units = at(L.off_dq);
+    q.dkv_units = at(L.off_dkv);
+    q.counts = at(L.off_cnt);
+    q.scratch = at(L.off_scr);
+    q.B = nseq;
+    q.T = total;
+    q.M = (total + 127) / 128;
+    q.Hkv = Hkv;
+    q.nch_fwd = G / ne::fwd_heads_per_cta(d, G);
+    q.nch_dq = G / ne::dq_heads_per_cta(d, G);
+    q.status = status;
+    return ne::launch_varlen_plan(q, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+// Host-side checks of a packed call; with a prefix array in device memory
+// only its pointer and the shape (the plan kernel checks the contents), and
+// the tile bound is that of one sequence of `total` rows.
+int check_packed_args(const int32_t *cu, bool dev_cu, int nseq, int total, int Hq, int Hkv,
+                      int d, float theta, int *maxlen)
+{
+    if (!dev_cu)
+        return check_packed(cu, nseq, total, Hq, Hkv, d, theta, maxlen);
+    if (!cu)
+        return NE_ERR_NULL;
+    if (nseq < 1)
+        return NE_ERR_SHAPE;
+    int rc = check_shape(1, total, Hq, Hkv, d, theta);
+    if (rc != NE_OK)
+        return rc;
+    if ((rc = check_shape(nseq, total, Hq, Hkv, d, theta)) != NE_OK)
+        return rc;
+    *maxlen = total;
+    return NE_OK;
+}
+
+int fwd_packed_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int32_t *cu_seqlens, bool dev_cu, void *workspace,
+                    size_t workspace_bytes, int nseq, int total, int Hq, int Hkv, int d,
+                    float rope_theta, void *stream)
 {
     if (!q || !k || !v || !o || !lse || !workspace)
         return NE_ERR_NULL;
     int maxlen = 0;
-    int rc = check_packed(cu_seqlens, nseq, total, Hq, Hkv, d, rope_theta, &maxlen);
+    int rc = check_packed_args(cu_seqlens, dev_cu, nseq, total, Hq, Hkv, d, rope_theta, &maxlen);
     if (rc != NE_OK)
         return rc;
     const PackedLayout L = packed_layout(nseq, total, Hq, Hkv, d);
     if (workspace_bytes < L.tables)
         return NE_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (dev_cu && !aligned4(cu_seqlens)))
         return NE_ERR_ALIGN;
     uint32_t *status = nullptr;
     if ((rc = device_state(&status)) != NE_OK)
@@ -1127,35 +1186,41 @@ int ne_attn_fwd_packed(const void *q, const void *k, const void *v, void *o, flo
     if (make_map(&mq, q, 1, total, Hq, d) || make_map(&mk, k, 1, total, Hkv, d) ||
         make_map(&mv, v, 1, total, Hkv, d) || make_map(&mo, o, 1, total, Hq, d))
         return NE_ERR_CUDA;
-    int counts[3];
-    if ((rc = upload_packed_tables(cu_seqlens, nseq, maxlen, Hq, Hkv, d, L, workspace, st,
-                                   counts)) != NE_OK)
+    int counts[3] = {1, 1, 1};
+    if (dev_cu)
+        rc = plan_packed_on_device(cu_seqlens, nseq, total, Hq, Hkv, d, L, workspace, status, st);
+    else
+        rc = upload_packed_tables(cu_seqlens, nseq, maxlen, Hq, Hkv, d, L, workspace, st,
+                                  counts);
+    if (rc != NE_OK)
         return rc;
     set_packed(p, workspace, L, nseq, maxlen);
     p.units = ws_int(workspace, L.off_fwd);
     p.num_units = counts[0];
+    if (dev_cu)
+        p.unit_count = ws_int(workspace, L.off_cnt);
     if (counts[0] > 0 && ne::launch_fwd(d, mq, mk, mv, mo, mq, mk, p, st) != cudaSuccess)
         return NE_ERR_CUDA;
     return NE_OK;
 }
 
-int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *o,
-                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
-                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
-                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
-                       void *stream)
+int bwd_packed_impl(const void *q, const void *k, const void *v, const void *o,
+                    const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                    const int32_t *cu_seqlens, bool dev_cu, void *workspace,
+                    size_t workspace_bytes, int nseq, int total, int Hq, int Hkv, int d,
+                    float rope_theta, void *stream)
 {
     if (!o || !dq || !dk || !dv || !workspace)
         return NE_ERR_NULL;
     int maxlen = 0;
-    int rc = check_packed(cu_seqlens, nseq, total, Hq, Hkv, d, rope_theta, &maxlen);
+    int rc = check_packed_args(cu_seqlens, dev_cu, nseq, total, Hq, Hkv, d, rope_theta, &maxlen);
     if (rc != NE_OK)
         return rc;
     const PackedLayout L = packed_layout(nseq, total, Hq, Hkv, d);
     if (workspace_bytes < L.total)
         return NE_ERR_WORKSPACE;
     if (!aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (dev_cu && !aligned4(cu_seqlens)))
         return NE_ERR_ALIGN;
     void *bws = static_cast<uint8_t *>(workspace) + L.tables;
     ne::AttnParams p;
@@ -1165,9 +1230,14 @@ int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *
     if (rc != NE_OK)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int counts[3];
-    if ((rc = upload_packed_tables(cu_seqlens, nseq, maxlen, Hq, Hkv, d, L, workspace, st,
-                                   counts)) != NE_OK)
+    int counts[3] = {1, 1, 1};
+    if (dev_cu)
+        rc = plan_packed_on_device(cu_seqlens, nseq, total, Hq, Hkv, d, L, workspace, p.status,
+                                   st);
+    else
+        rc = upload_packed_tables(cu_seqlens, nseq, maxlen, Hq, Hkv, d, L, workspace, st,
+                                  counts);
+    if (rc != NE_OK)
         return rc;
     // the preprocess streams over the pack's rows (B = 1 in memory) and
     // finds each row's position in its sequence through cu
@@ -1181,13 +1251,59 @@ int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *
     set_packed(p, workspace, L, nseq, maxlen);
     p.units = ws_int(workspace, L.off_dq);
     p.num_units = counts[1];
+    if (dev_cu)
+        p.unit_count = ws_int(workspace, L.off_cnt) + 1;
     if (counts[1] > 0 && (rc = run_dq(d, p, dq, mqr, mkr, mv, mdo, st)) != NE_OK)
         return rc;
     p.units = ws_int(workspace, L.off_dkv);
     p.num_units = counts[2];
+    if (dev_cu)
+        p.unit_count = ws_int(workspace, L.off_cnt) + 2;
     if (counts[2] > 0 && (rc = run_dkdv(d, p, dk, dv, mqr, mkr, mv, mdo, st)) != NE_OK)
         return rc;
     return NE_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+int ne_attn_fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
+                       void *stream)
+{
+    return fwd_packed_impl(q, k, v, o, lse, cu_seqlens, false, workspace, workspace_bytes, nseq,
+                           total, Hq, Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                       const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                       int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
+                       void *stream)
+{
+    return bwd_packed_impl(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, false, workspace,
+                           workspace_bytes, nseq, total, Hq, Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_fwd_packed_dev(const void *q, const void *k, const void *v, void *o, float *lse,
+                           const int32_t *cu_seqlens_dev, void *workspace,
+                           size_t workspace_bytes, int nseq, int total, int Hq, int Hkv, int d,
+                           float rope_theta, void *stream)
+{
+    return fwd_packed_impl(q, k, v, o, lse, cu_seqlens_dev, true, workspace, workspace_bytes,
+                           nseq, total, Hq, Hkv, d, rope_theta, stream);
+}
+
+int ne_attn_bwd_packed_dev(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                           const int32_t *cu_seqlens_dev, void *workspace,
+                           size_t workspace_bytes, int nseq, int total, int Hq, int Hkv, int d,
+                           float rope_theta, void *stream)
+{
+    return bwd_packed_impl(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens_dev, true, workspace,
+                           workspace_bytes, nseq, total, Hq, Hkv, d, rope_theta, stream);
 }
 
 } // extern "C"

@@ -81,12 +81,14 @@ int varlen_plan(const int *seqlen, int B, int T, int Hq, int Hkv, int d, int *fw
 // Device-side plan of a padded variable-length batch: the tables of
 // varlen_plan (forward, dq, dk/dv, same contents and order) and the three
 // counts, from lengths in device memory, clamped to [0, T] (kDevArg recorded
-// for a length outside), copied to seqlen_out.  scratch holds 2 B + 2 (M + 2)
-// ints.
+// for a length outside), copied to seqlen_out; or from a packed batch's
+// prefix array (sanitised into cu_out).  M: the tiles of the enumeration.
+// scratch holds 2 B + 2 (M + 2) ints.
 struct DevicePlanParams {
-    const int *seqlens_in;
-    int *seqlen_out, *fwd_units, *dq_units, *dkv_units, *counts, *scratch;
-    int B, T, Hkv, nch_fwd, nch_dq;
+    const int *seqlens_in;      // padded: lengths [B]
+    const int *cu_in;           // packed: prefix array [B + 1] (seqlens_in unused)
+    int *seqlen_out, *cu_out, *fwd_units, *dq_units, *dkv_units, *counts, *scratch;
+    int B, T, M, Hkv, nch_fwd, nch_dq;   // packed: B = sequences, T = total rows
     uint32_t *status;
 };
 cudaError_t launch_varlen_plan(const DevicePlanParams &p, cudaStream_t stream);

@@ -136,7 +136,10 @@ int varlen_plan(const int *seqlen, int B, int T, int Hq, int Hkv, int d, int *fw
 // mt_b' = mt_b, then j of its own.  With C(w) = #{b : mt_b >= w}:
 //   pos = Hkv sum_{w' > w} C(w') + Hkv (C(w) - C(mt_b) + eq_b) + j,
 // eq_b = #{b' < b : mt_b' = mt_b}.  Lengths outside [0, T] are clamped and
-// recorded in the status word.
+// recorded in the status word.  Packed batches (cu_in set): the prefix
+// array is made monotone within [0, T = total] (starting at 0, ending at
+// total; any change recorded) and written out, since the kernels address
+// rows through it, and the lengths are its differences.
 constexpr int kPlanThreads = 1024;
 
 // Exclusive scan of one int per thread over the block; returns the block's
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) varlen_plan_kernel(const Devi
     __shared__ int warp_sums[kPlanThreads / 32];
     __shared__ int total_s;
     const int tid = threadIdx.x;
-    const int M = (p.T + kRows - 1) / kRows;
+    const int M = p.M;
     int *mt = p.scratch;                  // [B]
     int *eq = mt + p.B;                   // [B]
     int *cge = eq + p.B;                  // [M + 2]: C(w)
@@ -189,15 +192,41 @@ __global__ void __launch_bounds__(kPlanThreads, 1) varlen_plan_kernel(const Devi
     // lengths (clamped), tiles, and the histogram of tiles (into cge)
     for (int i = tid; i < M + 2; i += kPlanThreads)
         cge[i] = 0;
+    if (p.cu_in != nullptr && tid == 0) {
+        // one pass: the running maximum, clipped to the pack
+        bool bad = p.cu_in[0] != 0 || p.cu_in[p.B] != p.T;
+        int prev = 0;
+        p.cu_out[0] = 0;
+        for (int b = 1; b <= p.B; ++b) {
+            int c = p.cu_in[b];
+            bad = bad || c < prev;
+            c = c < prev ? prev : (c > p.T ? p.T : c);
+            if (b == p.B)
+                c = p.T;
+            p.cu_out[b] = c;
+            prev = c;
+        }
+        if (bad)
+            atomicOr(p.status, kDevArg);
+    }
     __syncthreads();
     for (int b = tid; b < p.B; b += kPlanThreads) {
-        int L = p.seqlens_in[b];
-        if (L < 0 || L > p.T) {
-            atomicOr(p.status, kDevArg);
-            L = L < 0 ? 0 : p.T;
+        int L;
+        if (p.cu_in != nullptr) {
+            L = p.cu_out[b + 1] - p.cu_out[b];
+        } else {
+            L = p.seqlens_in[b];
+            if (L < 0 || L > p.T) {
+                atomicOr(p.status, kDevArg);
+                L = L < 0 ? 0 : p.T;
+            }
         }
         p.seqlen_out[b] = L;
         mt[b] = (L + kRows - 1) / kRows;
+        if (mt[b] > M) {   // a packed length above the tile bound cannot occur
+            atomicOr(p.status, kDevArg);
+            mt[b] = M;
+        }
         atomicAdd(cge + mt[b], 1);
     }
     __syncthreads();

@@ -310,7 +310,8 @@ int ne_attn_bwd_varlen_dev(const void *q, const void *k, const void *v, const vo
  * Results equal those of the padded entry points on the same sequences, row
  * for row; every row of the pack is a valid row.  The library builds the
  * tables of work units on the host and copies them into the workspace from
- * pageable memory, so these calls cannot be captured into a CUDA graph;
+ * pageable memory, so these calls cannot be captured into a CUDA graph (the
+ * _dev variants below can);
  * calls that share a workspace must not overlap on the GPU.  Errors as for
  * the padded entry points; cu_seqlens NULL gives NE_ERR_NULL, nseq < 1 or
  * total < 1 NE_ERR_SHAPE, an inconsistent cu_seqlens NE_ERR_ARG.
@@ -326,6 +327,27 @@ int ne_attn_bwd_packed(const void *q, const void *k, const void *v, const void *
                        const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
                        int nseq, int total, int Hq, int Hkv, int d, float rope_theta,
                        void *stream);
+
+/*
+ * The same with cu_seqlens in DEVICE memory (int32 [nseq + 1], 4-byte
+ * aligned, read by the GPU in stream order), for CUDA graph capture: the
+ * planning kernel of the _dev padded entry points builds the unit tables
+ * from it, with the tile bound of one sequence of `total` rows (the host
+ * never learns the longest sequence).  The kernels address rows through a
+ * sanitised copy in the workspace: a prefix array that does not start at 0,
+ * decreases or does not end at total is made monotone within [0, total]
+ * and reported as NE_ERR_ARG by ne_attn_get_error.  Results equal the
+ * host-array entry points' bit for bit for a valid prefix array.
+ */
+int ne_attn_fwd_packed_dev(const void *q, const void *k, const void *v, void *o, float *lse,
+                           const int32_t *cu_seqlens_dev, void *workspace,
+                           size_t workspace_bytes, int nseq, int total, int Hq, int Hkv, int d,
+                           float rope_theta, void *stream);
+int ne_attn_bwd_packed_dev(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                           const int32_t *cu_seqlens_dev, void *workspace,
+                           size_t workspace_bytes, int nseq, int total, int Hq, int Hkv, int d,
+                           float rope_theta, void *stream);
 
 /*
  * The work units a padded variable-length batch launches (host only; no GPU

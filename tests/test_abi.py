@@ -147,12 +147,15 @@ def test_window_argument_errors(lib):
 def test_packed_workspace_size_and_argument_errors(lib):
     def r256(x):
         return (x + 255) // 256 * 256
-    # [lengths][cu][fwd units][dq units][dk/dv units] + the backward workspace of
+    # [lengths][cu][fwd units][dq units][dk/dv units][plan counts][plan scratch]
+    # + the backward workspace of
     # a [1][total] batch; live tiles per kv head <= total // 128 + nseq
     nseq, total, Hq, Hkv, d = 3, 300, 12, 4, 64
     tiles = (total // 128 + nseq) * Hkv
+    M = (total + 127) // 128     # + the device-side plan's counts and scratch
     want = (r256(4 * nseq) + r256(4 * (nseq + 1)) + r256(4 * tiles) + r256(4 * tiles) +
-            r256(4 * tiles) + ne.ne_attn_bwd_workspace_size(1, total, Hq, Hkv, d))
+            r256(4 * tiles) + r256(16) + r256(4 * (2 * nseq + 2 * (M + 2))) +
+            ne.ne_attn_bwd_workspace_size(1, total, Hq, Hkv, d))
     assert ne.ne_attn_packed_workspace_size(nseq, total, Hq, Hkv, d) == want
     assert ne.ne_attn_packed_workspace_size(0, total, Hq, Hkv, d) == 0
     assert ne.ne_attn_packed_workspace_size(1, 0, Hq, Hkv, d) == 0
@@ -176,3 +179,10 @@ def test_packed_workspace_size_and_argument_errors(lib):
     cu = (ctypes.c_int32 * 3)(0, 4, 10)
     assert lib.ne_attn_bwd_packed(a, a, a, a, a, a, a, a, a, cu, a, 0, 2, 10, 2, 2, 64,
                                   10000.0, None) == 5
+    dev = lib.ne_attn_fwd_packed_dev
+    assert dev(a, a, a, a, a, None, a, ws, 2, 10, 2, 2, 64, 10000.0, None) == 1
+    assert dev(a, a, a, a, a, a + 2, a, ws, 2, 10, 2, 2, 64, 10000.0, None) == 4
+    assert dev(a, a, a, a, a, a, a, ws, 0, 10, 2, 2, 64, 10000.0, None) == 2
+    assert dev(a, a, a, a, a, a, a, 0, 2, 10, 2, 2, 64, 10000.0, None) == 5
+    assert lib.ne_attn_bwd_packed_dev(a, a, a, a, a, a, a, a, a, None, a, 1 << 15, 2, 10, 2, 2,
+                                      64, 10000.0, None) == 1

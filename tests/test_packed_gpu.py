@@ -132,3 +132,76 @@ def test_packed_writes_nothing_outside_the_pack(ne):
     for buf in (ob, lb, qb, kb, vb):
         assert (buf[:G] == 7.0).all() and (buf[-G:] == 7.0).all()
     assert torch.isfinite(o.float()).all() and torch.isfinite(dq.float()).all()
+
+
+def _run_packed_dev(ne, xd, cu_dev, ws):
+    q, k, v, do = xd["q"], xd["k"], xd["v"], xd["do"]
+    total, Hq, d = q.shape
+    nan = float("nan")
+    o = torch.full_like(q, nan)
+    lse = torch.full((Hq, total), nan, dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.full_like(x, nan) for x in (q, k, v))
+    ne.ne_attn_fwd_packed_dev(q, k, v, o, lse, cu_dev, ws, THETA)
+    ne.ne_attn_bwd_packed_dev(q, k, v, o, lse, do, dq, dk, dv, cu_dev, ws, THETA)
+    return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,d", CASES)
+def test_packed_device_offsets_equal_host(ne, lens, Hq, Hkv, d):
+    """cu_seqlens in device memory (tables planned on the GPU): every output
+    bitwise equal to the host-offset entry points."""
+    x, cu = _pack(lens, Hq, Hkv, d, seed=800 + sum(lens))
+    xd = to_dev(x)
+    ref = _run_packed(ne, xd, cu)
+    total = int(cu[-1])
+    ws = torch.full((ne.ne_attn_packed_workspace_size(len(cu) - 1, total, Hq, Hkv, d),), 0x33,
+                    dtype=torch.uint8, device="cuda")
+    got = _run_packed_dev(ne, xd, torch.from_numpy(cu).cuda(), ws)
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 0
+    for n in ref:
+        assert torch.equal(got[n], ref[n]), n
+
+
+def test_packed_graph_replays_with_new_offsets(ne):
+    """One capture; replays after writing other offsets (same sequence count
+    and total) into the same device tensor equal eager host-offset calls."""
+    Hq, Hkv, d = 6, 2, 64
+    x, cu0 = _pack([300, 100, 12], Hq, Hkv, d, seed=810)
+    xd = to_dev(x)
+    total = int(cu0[-1])
+    ws = torch.zeros(ne.ne_attn_packed_workspace_size(3, total, Hq, Hkv, d), dtype=torch.uint8,
+                     device="cuda")
+    cu_dev = torch.from_numpy(cu0).cuda()
+    out = _run_packed_dev(ne, xd, cu_dev, ws)            # warm-up outside the capture
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = _run_packed_dev(ne, xd, cu_dev, ws)
+    for lens in ([300, 100, 12], [1, 410, 1], [0, 0, 412], [129, 128, 155]):
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        cu_dev.copy_(torch.from_numpy(cu))
+        for t in out.values():
+            t.fill_(float("nan"))
+        graph.replay()
+        ref = _run_packed(ne, xd, cu)
+        for n in ref:
+            assert torch.equal(out[n], ref[n]), (lens, n)
+
+
+def test_packed_device_bad_offsets_report_and_sanitise(ne):
+    """A decreasing prefix array in device memory: NE_ERR_ARG, and the call
+    runs on the monotone array (running maximum), no fault."""
+    Hq, Hkv, d = 4, 2, 64
+    x, _ = _pack([6, 0, 4], Hq, Hkv, d, seed=811)
+    xd = to_dev(x)
+    ws = torch.zeros(ne.ne_attn_packed_workspace_size(3, 10, Hq, Hkv, d), dtype=torch.uint8,
+                     device="cuda")
+    got = _run_packed_dev(ne, xd, torch.tensor([0, 6, 4, 10], dtype=torch.int32,
+                                               device="cuda"), ws)
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 9              # NE_ERR_ARG
+    ref = _run_packed(ne, xd, np.asarray([0, 6, 6, 10], np.int32))
+    for n in ref:
+        assert torch.equal(got[n], ref[n]), n
