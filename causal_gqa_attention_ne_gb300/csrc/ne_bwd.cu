@@ -519,6 +519,27 @@ __global__ void __launch_bounds__(384, 1)
                 if (u >= NU)
                     break;
                 const DqUnit w = dq_unit<VAR>(u, GC, p);
+                auto load_kv = [&](int jk) {
+                    const int st = kt % ST, u2 = kt / ST;
+                    if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc))
+                        return false;
+                    const uint32_t kb = smem_u32(&bar_kv_full[st]);
+                    mbar_arrive_expect_tx(kb, 2 * TL::BYTES);
+                    for (int cb = 0; cb < TL::NB; ++cb) {
+                        tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmK, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
+                                    w.sq.bc);
+                        tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK),
+                                    &tmV, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
+                                    w.sq.bc);
+                    }
+                    ++kt;
+                    return true;
+                };
+                // The unit's first K/V tile goes first: a stage is free while
+                // the previous unit's last items run, but the Q'/dO slots only
+                // free at those items, so the tile lands during them.
+                ok = load_kv(w.lo);
                 for (int g = 0; g < GC && ok; ++g) {
                     if (k >= 1 && !mbar_wait(smem_u32(&bar_q_empty[g]), (k - 1) & 1, wc)) {
                         ok = false;
@@ -535,23 +556,8 @@ __global__ void __launch_bounds__(384, 1)
                                     w.sq.base + w.m * kRows, w.sq.bc);
                     }
                 }
-                for (int jk = w.lo; jk <= w.m && ok; ++jk, ++kt) {
-                    const int st = kt % ST, u2 = kt / ST;
-                    if (u2 >= 1 && !mbar_wait(smem_u32(&bar_kv_empty[st]), (u2 - 1) & 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t kb = smem_u32(&bar_kv_full[st]);
-                    mbar_arrive_expect_tx(kb, 2 * TL::BYTES);
-                    for (int cb = 0; cb < TL::NB; ++cb) {
-                        tma_load_4d(smem_u32(smem + C::OFF_K + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmK, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
-                                    w.sq.bc);
-                        tma_load_4d(smem_u32(smem + C::OFF_V + st * TL::BYTES + cb * TL::BLOCK),
-                                    &tmV, kb, cb * TL::BOX_COLS, w.j, w.sq.base + jk * kRows,
-                                    w.sq.bc);
-                    }
-                }
+                for (int jk = w.lo + 1; jk <= w.m && ok; ++jk)
+                    ok = load_kv(jk);
             }
             if (*wc.abort) {
                 for (int g = 0; g < GC; ++g)
