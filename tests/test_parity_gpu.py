@@ -51,12 +51,12 @@ def test_step_workload_one_layer_sampled():
     print(_sampled_case(w, 5, groups))
 
 
-def test_stress_workload_sampled():
-    """B4 T4096 16/4 d128 with one 8x row per (tensor, batch, head); the oracle
-    checks four (batch, kv head) groups, one per batch row, each holding 8x
-    rows of q, k and v, with the flat lse bound on every row."""
+def test_stress_workload_every_group():
+    """B4 T4096 16/4 d128 with one 8x row per (tensor, batch, head): the oracle
+    checks all 16 (batch, kv head) groups (every one holds 8x rows of q, k
+    and v), with the flat lse bound on every row."""
     w = ne_inputs.STRESS
-    groups = [(0, 0), (1, 3), (2, 1), (3, 2)]
+    groups = [(b, j) for b in range(w.B) for j in range(w.Hkv)]
     x = ne_inputs.make_inputs(w, 0)
     for (b, j) in groups:
         for name, heads in (("q", range(j * w.G, (j + 1) * w.G)), ("k", [j]), ("v", [j])):
