@@ -165,3 +165,31 @@ def test_fp16_range_overflow_reports_and_recovers(ne):
                       THETA)
     ref, _, _ = oracle_all(custom_inputs(B=1, T=64, Hq=2, Hkv=1, d=64, seed=37), THETA)
     compare(gpu, ref)
+
+
+def test_large_rows_packed(ne):
+    """A packed batch with 8x rows of q and k in several sequences: the repair
+    addresses rows through the pack's offsets; flat lse against the oracle's
+    packed forward."""
+    lens = [300, 1, 129, 200]
+    Hq, Hkv, d = 4, 2, 64
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    x = custom_inputs(B=1, T=total, Hq=Hq, Hkv=Hkv, d=d, seed=39)
+    # 8x rows at (sequence, position, head)
+    for (sq, t, h) in ((0, 5, 0), (0, 299, 3), (2, 128, 1), (3, 0, 2), (3, 150, 0)):
+        x["q"][0, cu[sq] + t, h] *= 8.0
+    for (sq, t, j) in ((0, 40, 0), (2, 3, 1), (3, 130, 0), (1, 0, 1)):
+        x["k"][0, cu[sq] + t, j] *= 8.0
+    xp = {n: t[0].contiguous() for n, t in x.items()}
+    xd = to_dev(xp)
+    ws = torch.empty(ne.ne_attn_packed_workspace_size(len(lens), total, Hq, Hkv, d),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(xd["q"])
+    lse = torch.empty(Hq, total, dtype=torch.float32, device="cuda")
+    ne.ne_attn_fwd_packed(xd["q"], xd["k"], xd["v"], o, lse, cu, ws, THETA)
+    torch.cuda.synchronize()
+    assert ne.ne_attn_get_error() == 0
+    q, k, v = (ne_inputs.as_f64(xp[n]) for n in ("q", "k", "v"))
+    ro, rl = oracle.attn_fwd_packed(q, k, v, cu, THETA)
+    print(compare({"o": o, "lse": lse}, {"o": ro, "lse": rl}, what=("o", "lse")))
