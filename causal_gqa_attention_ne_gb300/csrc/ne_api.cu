@@ -258,7 +258,8 @@ int fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, v
     p.window = window;
     CUtensorMap mq, mk, mv, mo, mqs, mks;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
-        make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
+        make_map(&mv, v, B, T, Hkv, d) ||
+        make_map(&mo, o, B, T, Hq, d, false, ne::kFwdOStoreRows))
         return NE_ERR_CUDA;
     if (save) {
         void *qrot = static_cast<uint8_t *>(workspace) + ws_d_bytes(B, T, Hq);
@@ -849,7 +850,8 @@ int fwd_varlen_impl(const void *q, const void *k, const void *v, void *o, float 
     p.v_in = v;
     CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, B, T, Hq, d) || make_map(&mk, k, B, T, Hkv, d) ||
-        make_map(&mv, v, B, T, Hkv, d) || make_map(&mo, o, B, T, Hq, d))
+        make_map(&mv, v, B, T, Hkv, d) ||
+        make_map(&mo, o, B, T, Hq, d, false, ne::kFwdOStoreRows))
         return NE_ERR_CUDA;
     int counts[3] = {1, 1, 1};
     if (dev_lengths)
@@ -1184,7 +1186,8 @@ int fwd_packed_impl(const void *q, const void *k, const void *v, void *o, float 
     p.v_in = v;
     CUtensorMap mq, mk, mv, mo;
     if (make_map(&mq, q, 1, total, Hq, d) || make_map(&mk, k, 1, total, Hkv, d) ||
-        make_map(&mv, v, 1, total, Hkv, d) || make_map(&mo, o, 1, total, Hq, d))
+        make_map(&mv, v, 1, total, Hkv, d) ||
+        make_map(&mo, o, 1, total, Hq, d, false, ne::kFwdOStoreRows))
         return NE_ERR_CUDA;
     int counts[3] = {1, 1, 1};
     if (dev_cu)

@@ -123,6 +123,39 @@ __device__ __forceinline__ FwdUnit fwd_unit(int u, int GC, const AttnParams &p)
     return w;
 }
 
+// The order in which the producer loads, the RoPE warps rotate and the store
+// warp saves a unit's tiles: [Q' of head 0], K lo, [Q' of heads 1..GC-1],
+// K lo+1..m, [Q' of the next unit].  The unit's own Q' tiles are listed only
+// when they were not loaded with the previous unit (nq0 = GC or 0); the next
+// unit's only when they are prefetched (nq1 = GC or 0).  K lo right after the
+// first Q' tile lets the first S start after two rotations; the next unit's
+// Q' tiles come last so that they never hold up this unit's K tiles.
+struct UnitTile {
+    bool isq;
+    int qunit;   // unit whose Q' tile it is (k or k + 1)
+    int g;       // head of the unit's chunk (Q' tiles)
+    int jk;      // key tile (K tiles)
+};
+
+__device__ __forceinline__ int unit_tiles(int nq0, int nq1, const FwdUnit &w)
+{
+    return nq0 + 1 + (w.m - w.lo) + nq1;
+}
+
+__device__ __forceinline__ UnitTile unit_tile(int t, int k, int nq0, const FwdUnit &w)
+{
+    const int a = nq0 > 0 ? 1 : 0, nk = w.m - w.lo;
+    if (t < a)
+        return UnitTile{true, k, 0, 0};
+    if (t == a)
+        return UnitTile{false, k, 0, w.lo};
+    if (t <= nq0)
+        return UnitTile{true, k, t - 1, 0};
+    if (t <= nq0 + nk)
+        return UnitTile{false, k, 0, w.lo + t - nq0};
+    return UnitTile{true, k + 1, t - nq0 - nk - 1, 0};
+}
+
 // ------------------------------------------------ exact scores of large rows ---
 //
 // A row of a Q or K tile is "large" when its rotated vector has mean square
@@ -462,7 +495,6 @@ __global__ void __launch_bounds__(512, 1)
     __shared__ uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[2][2], bar_p_free[2][2];
     __shared__ uint64_t bar_o_free[2][C::NSL], bar_split, bar_drain;
     // O staging block of group w written (its four warps) / read by its store
-    __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
     // training path: the RoPE warps finished the n-th tile to be stored
     // (ring of 16: they are never 16 such tiles ahead of warp 15, which must
     // release a Q slot or a stored K stage before it is reloaded), and warp
@@ -506,8 +538,6 @@ __global__ void __launch_bounds__(512, 1)
             }
             for (int sl = 0; sl < C::NSL; ++sl)
                 mbar_init(smem_u32(&bar_o_free[w][sl]), 4);
-            mbar_init(smem_u32(&bar_stg_full[w]), 4);
-            mbar_init(smem_u32(&bar_stg_free[w]), 1);
         }
         mbar_init(smem_u32(&bar_split), 4);
         mbar_init(smem_u32(&bar_drain), 2);
@@ -559,10 +589,10 @@ __global__ void __launch_bounds__(512, 1)
             int qloads[QB][GC] = {};   // loads issued per Q slot (for the abort drain)
             // Q' tiles of unit kk into set kk % QB, once the set's previous
             // unit has issued its last S
-            auto load_q = [&](int kk) {
+            auto load_q = [&](int kk, int g0, int g1) {
                 const FwdUnit w = fwd_unit<VAR>(snake_unit(kk, cta, P), GC, p);
                 const int qb = kk % QB, use = kk / QB;
-                for (int g = 0; g < GC; ++g) {
+                for (int g = g0; g < g1; ++g) {
                     if (use >= 1 && !mbar_wait_warp(smem_u32(&bar_q_empty[qb][g]), (use - 1) & 1, wc))
                         return false;
                     // training path: the previous tile of this slot was stored
@@ -619,15 +649,17 @@ __global__ void __launch_bounds__(512, 1)
                 if (u >= NU)
                     break;
                 const FwdUnit w = fwd_unit<VAR>(u, GC, p);
-                // order: [Q of this unit if not prefetched], K/V lo, [Q of the
-                // next unit], K/V lo+1..m
-                if (QB == 1 || k == 0)
-                    ok = load_q(k);
+                // tile order of unit_tile()
+                const bool own_q = QB == 1 || k == 0;
+                if (own_q)
+                    ok = load_q(k, 0, 1);
                 ok = ok && load_kv(w, w.lo);
-                if (QB == 2 && ok && snake_unit(k + 1, cta, P) < NU)
-                    ok = load_q(k + 1);
+                if (own_q && ok)
+                    ok = load_q(k, 1, GC);
                 for (int jk = w.lo + 1; jk <= w.m && ok; ++jk)
                     ok = load_kv(w, jk);
+                if (QB == 2 && ok && snake_unit(k + 1, cta, P) < NU)
+                    ok = load_q(k + 1, 0, GC);
             }
             if (*wc.abort && lane == 0) {
                 for (int qb = 0; qb < QB; ++qb)
@@ -661,11 +693,10 @@ __global__ void __launch_bounds__(512, 1)
                 const int nq0 = (QB == 1 || k == 0) ? GC : 0;
                 const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < NU;
                 const int nq1 = has_next ? GC : 0;
-                for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
-                    const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
-                    const int qunit = t < nq0 ? k : k + 1;
-                    const int g = t < nq0 ? t : t - nq0 - 1;
-                    const int jk = w.lo + (t == nq0 ? 0 : t - nq0 - nq1);
+                for (int t = 0; t < unit_tiles(nq0, nq1, w) && ok; ++t) {
+                    const UnitTile ut = unit_tile(t, k, nq0, w);
+                    const bool isq = ut.isq;
+                    const int qunit = ut.qunit, g = ut.g, jk = ut.jk;
                     const int qb = qunit % QB, st = kt % ST;
                     if (!isq)
                         ++kt;
@@ -828,18 +859,17 @@ __global__ void __launch_bounds__(512, 1)
             if (u >= NU)
                 break;
             const FwdUnit w = fwd_unit<VAR>(u, GC, p);
-            // Tiles in the order the producer loads them: [Q of this unit
-            // unless prefetched], K 0, [Q of the next unit], K 1..m.  One call
-            // site keeps the unrolled rotation in the instruction cache once.
+            // Tiles in the order the producer loads them (unit_tile()).  One
+            // call site keeps the unrolled rotation in the instruction cache
+            // once.
             const int nq0 = (QB == 1 || k == 0) ? GC : 0;
             const bool has_next = QB == 2 && snake_unit(k + 1, cta, P) < NU;
             const int nq1 = has_next ? GC : 0;
             const FwdUnit wn = has_next ? fwd_unit<VAR>(snake_unit(k + 1, cta, P), GC, p) : w;
-            for (int t = 0; t < nq0 + 1 + nq1 + w.m - w.lo && ok; ++t) {
-                const bool isq = t < nq0 || (t > nq0 && t <= nq0 + nq1);
-                const int qunit = t < nq0 ? k : k + 1;
-                const int g = t < nq0 ? t : t - nq0 - 1;
-                const int jk = w.lo + (t == nq0 ? 0 : t - nq0 - nq1);
+            for (int t = 0; t < unit_tiles(nq0, nq1, w) && ok; ++t) {
+                const UnitTile ut = unit_tile(t, k, nq0, w);
+                const bool isq = ut.isq;
+                const int qunit = ut.qunit, g = ut.g, jk = ut.jk;
                 const int qb = qunit % QB, st = kt % ST;
                 const uint32_t full = isq ? smem_u32(&bar_q_full[qb][g]) : smem_u32(&bar_k_full[st]);
                 const uint32_t par = isq ? ((qunit / QB) & 1) : ((kt / ST) & 1);
@@ -891,6 +921,7 @@ __global__ void __launch_bounds__(512, 1)
     regs_claim<184>();
     const int wg = warp >> 2;               // softmax group
     const int q4 = warp & 3;                // TMEM lane quarter
+    static_assert(kFwdOStoreRows == 32, "a warp stores the rows of its TMEM lane quarter");
     const int r = threadIdx.x & 127;        // query row == TMEM lane
     const uint32_t lane_base = tmem_addr(tbase, q4 * 32, 0);
     const float sl2 = p.scale_log2;
@@ -900,36 +931,54 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t *stage = smem + C::OFF_O + wg * TL::BLOCK;
     uint32_t nepi = 0;       // O stores this group has issued
     float mr0 = 0.f, mr1 = 0.f, lr0 = 0.f, lr1 = 0.f;   // running max (log2 units) / sum per slot
-    // Writes O_slot / l of head h (rows of this thread) and its lse.  With a
-    // second accumulator (merge), O = (O_a * sa + O_b * sb) * inv_l.
-    auto store_head = [&](const FwdUnit &un, int h, uint32_t oa, bool merge, uint32_t ob, float sa,
-                          float sb, float inv_l, float lse2) -> bool {
+    // Writes O_slot / l of head h (rows of this thread) and its lse.  The
+    // caller folds 1 / l into the scales: O = O_a * fa (+ O_b * fb with a
+    // second accumulator, merge), on packed fp32 pairs.
+    auto store_head = [&](const FwdUnit &un, int h, uint32_t oa, bool merge, uint32_t ob, float fa,
+                          float fb, float lse2) -> bool {
         const int t = un.m * kRows + r;
+        // columns c .. c + 31 of this thread's row, scaled, as bf16 pairs
+        auto chunk = [&](int c, uint32_t (&pk)[16]) {
+            uint32_t o[32];
+            tmem_ld32(oa + c, o);
+            tmem_ld_wait(o);
+            uint64_t x2[16];
+            const uint64_t fa2 = f32x2(fa, fa);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                x2[e] = mul_f32x2(f32x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])),
+                                  fa2);
+            if (merge) {
+                tmem_ld32(ob + c, o);
+                tmem_ld_wait(o);
+                const uint64_t fb2 = f32x2(fb, fb);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    x2[e] = fma_f32x2(
+                        f32x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), fb2,
+                        x2[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float x0, x1;
+                f32x2_split(x2[e], x0, x1);
+                pk[e] = pack_bf16x2(x0, x1);
+            }
+        };
         // O row by row from registers (rows past the sequence skipped)
         auto store_direct = [&]() {
             __nv_bfloat16 *dst =
                 static_cast<__nv_bfloat16 *>(p.out0) + (seq_row(p, un.sq, t) * p.Hq + h) * D;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(oa + c, o);
-                tmem_ld_wait(o);
-                float x[32];
+                uint32_t pk[16];
+                chunk(c, pk);
+                if (t < un.sq.len) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    x[e] = __uint_as_float(o[e]) * sa;
-                if (merge) {
-                    tmem_ld32(ob + c, o);
-                    tmem_ld_wait(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        x[e] = fmaf(__uint_as_float(o[e]), sb, x[e]);
+                    for (int q = 0; q < 4; ++q)
+                        d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    x[e] *= inv_l;
-                if (t < un.sq.len)
-                    store_row32_bf16(dst + c, x);
             }
         };
         if constexpr (C::STAGE) {
@@ -938,54 +987,32 @@ __global__ void __launch_bounds__(512, 1)
             if (VAR && p.cu != nullptr && (un.m + 1) * kRows > un.sq.len) {
                 store_direct();
             } else {
-                // the staging block is free once this group's previous store
-                // has read it
+                // Each warp sends its own 32 rows out with its own TMA store
+                // (the output map's box is kFwdOStoreRows rows), so no warp
+                // waits for another; its rows of the staging block are free
+                // once the warp's previous store has read them.
                 if (nepi >= 1) {
-                    if (warp == 4 * wg && lane == 0) {
+                    if (lane == 0)
                         bulk_wait_read0();
-                        mbar_arrive(smem_u32(&bar_stg_free[wg]));
-                    }
-                    if (!mbar_wait_warp(smem_u32(&bar_stg_free[wg]), (nepi - 1) & 1, wc))
-                        return false;
+                    __syncwarp();
                 }
 #pragma unroll
                 for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(oa + c, o);
-                    tmem_ld_wait(o);
-                    float x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        x[e] = __uint_as_float(o[e]) * sa;
-                    if (merge) {
-                        tmem_ld32(ob + c, o);
-                        tmem_ld_wait(o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            x[e] = fmaf(__uint_as_float(o[e]), sb, x[e]);
-                    }
+                    uint32_t pk[16];
+                    chunk(c, pk);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         *reinterpret_cast<uint4 *>(stage + tile_chunk<D>(r, c / 8 + q)) =
-                            make_uint4(pack_bf16x2(x[8 * q + 0] * inv_l, x[8 * q + 1] * inv_l),
-                                       pack_bf16x2(x[8 * q + 2] * inv_l, x[8 * q + 3] * inv_l),
-                                       pack_bf16x2(x[8 * q + 4] * inv_l, x[8 * q + 5] * inv_l),
-                                       pack_bf16x2(x[8 * q + 6] * inv_l, x[8 * q + 7] * inv_l));
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&bar_stg_full[wg]));
-                if (warp == 4 * wg) {
-                    if (!mbar_wait_warp(smem_u32(&bar_stg_full[wg]), nepi & 1, wc))
-                        return false;
-                    if (lane == 0) {
-                        tma_store_4d(&tmO, smem_u32(stage), 0, h, un.sq.base + un.m * kRows,
-                                     un.sq.bc);
-                        bulk_commit();
-                    }
-                    __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&tmO, smem_u32(stage + q4 * kFwdOStoreRows * TL::SWB), 0, h,
+                                 un.sq.base + un.m * kRows + q4 * kFwdOStoreRows, un.sq.bc);
+                    bulk_commit();
                 }
+                __syncwarp();
                 ++nepi;
             }
         } else {
@@ -1198,7 +1225,7 @@ __global__ void __launch_bounds__(512, 1)
                 ob = lane_base + C::COL_O + (og * C::NSL + oss) * D;
             }
             const float inv_l = 1.f / l_tot;
-            if (!store_head(un, h, oa, split, ob, sa, sb, inv_l, m_tot + __log2f(l_tot))) {
+            if (!store_head(un, h, oa, split, ob, sa * inv_l, sb * inv_l, m_tot + __log2f(l_tot))) {
                 ok = false;
                 break;
             }
@@ -1212,8 +1239,8 @@ __global__ void __launch_bounds__(512, 1)
         }
     }
     if constexpr (C::STAGE) {
-        if (warp == 4 * wg && lane == 0) {
-            bulk_wait0();               // this group's O tiles are in global memory
+        if (lane == 0) {
+            bulk_wait0();               // this warp's O rows are in global memory
             fence_proxy_async_global();  // and visible to the generic loads below
         }
     }

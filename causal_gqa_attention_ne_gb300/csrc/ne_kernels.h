@@ -9,9 +9,11 @@
 namespace ne {
 
 // Forward: persistent CTAs of 512 threads over M * B * Hkv * nchunks units;
-// `o` is the tensor map of the output (same layout as q), used for its store.
+// `o` is the tensor map of the output (same layout as q) with a box of
+// kFwdOStoreRows rows: each softmax warp stores its own rows of a head.
 // `qs` / `ks` map the fp16 Q' / K' regions of a backward workspace; they are
 // written only when p.save_rot is set.
+constexpr int kFwdOStoreRows = 32;
 cudaError_t launch_fwd(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const CUtensorMap &o, const CUtensorMap &qs, const CUtensorMap &ks,
                        const AttnParams &p, cudaStream_t stream);
