@@ -352,7 +352,7 @@ int run_dq(int d, const ne::AttnParams &base, void *dq, const CUtensorMap &mq,
     p.out0 = dq;
     CUtensorMap mdq;
     // packed batches: one batch entry in memory (p.B counts the sequences)
-    if (make_map(&mdq, dq, p.cu != nullptr ? 1 : p.B, p.T, p.Hq, d))
+    if (make_map(&mdq, dq, p.cu != nullptr ? 1 : p.B, p.T, p.Hq, d, false, ne::kDqStoreRows))
         return NE_ERR_CUDA;
     return ne::launch_bwd_dq(d, mq, mk, mv, mdo, mdq, p, st) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }

@@ -378,8 +378,12 @@ __device__ __forceinline__ void epilogue_inverse_rope(uint32_t taddr, float scal
 //               dS = P (dP - D), dS (fp16) to TMEM as the A operand of
 //               dQ += dS K'; at the end of a unit, dQ * scale with the inverse
 //               RoPE to bf16 (warpgroup w takes heads g = w, w+2, ...).
-//   warp 8      TMA producer.   warp 9  TMEM allocator + S/dP issuer.
-//   warp 10     dQ issuer.      warp 11 idle.
+//   warp 8      TMA producer.
+//   warps 9, 11 S/dP issuers of row warpgroups 0 and 1 (each group's 64 key
+//               columns are their own N = 64 MMAs with their own barriers, so
+//               the groups never wait for each other); warp 9 also allocates
+//               TMEM.
+//   warp 10     dQ issuer (per item group 0's key K steps, then group 1's).
 // TMEM: S [0,128) dP [128,256) dS [256,320) dQ of head g at 320 + g*D.
 
 template <int D, int GC, int ST>
@@ -446,9 +450,10 @@ __global__ void __launch_bounds__(384, 1)
                                                 ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_q_full[GC], bar_q_empty[GC];
     __shared__ uint64_t bar_kv_full[ST], bar_kv_empty[ST];
-    __shared__ uint64_t bar_s_full, bar_s_empty, bar_ds_full, bar_ds_empty;
+    // per row warpgroup w: its key columns of S/dP computed (s_full), loaded
+    // (s_empty), its dS written (ds_full) and read by the dQ MMAs (ds_empty)
+    __shared__ uint64_t bar_s_full[2], bar_s_empty[2], bar_ds_full[2], bar_ds_empty[2];
     __shared__ uint64_t bar_dq_done, bar_dq_free, bar_drain;
-    __shared__ uint64_t bar_stg_full[2], bar_stg_free[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_s;
 
@@ -459,23 +464,21 @@ __global__ void __launch_bounds__(384, 1)
         abort_s = 0;
         for (int g = 0; g < GC; ++g) {
             mbar_init(smem_u32(&bar_q_full[g]), 1);
-            mbar_init(smem_u32(&bar_q_empty[g]), 1);
+            mbar_init(smem_u32(&bar_q_empty[g]), 2);   // both S/dP issuers
         }
         for (int s = 0; s < ST; ++s) {
             mbar_init(smem_u32(&bar_kv_full[s]), 1);
             mbar_init(smem_u32(&bar_kv_empty[s]), 1);
         }
-        mbar_init(smem_u32(&bar_s_full), 1);
-        mbar_init(smem_u32(&bar_s_empty), 8);
-        mbar_init(smem_u32(&bar_ds_full), 8);
-        mbar_init(smem_u32(&bar_ds_empty), 1);
+        for (int w2 = 0; w2 < 2; ++w2) {
+            mbar_init(smem_u32(&bar_s_full[w2]), 1);
+            mbar_init(smem_u32(&bar_s_empty[w2]), 4);
+            mbar_init(smem_u32(&bar_ds_full[w2]), 4);
+            mbar_init(smem_u32(&bar_ds_empty[w2]), 1);
+        }
         mbar_init(smem_u32(&bar_dq_done), 1);
         mbar_init(smem_u32(&bar_dq_free), 8);
-        for (int w2 = 0; w2 < 2; ++w2) {
-            mbar_init(smem_u32(&bar_stg_full[w2]), 4);
-            mbar_init(smem_u32(&bar_stg_free[w2]), 1);
-        }
-        mbar_init(smem_u32(&bar_drain), 2);
+        mbar_init(smem_u32(&bar_drain), 3);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -565,21 +568,30 @@ __global__ void __launch_bounds__(384, 1)
                 for (int t = (kt > ST ? kt - ST : 0); t < kt; ++t)
                     mbar_wait_drain(smem_u32(&bar_kv_full[t % ST]), (t / ST) & 1, wc.limit_ns);
             }
-        } else if (warp == 9 || warp == 10) {
+        } else if (warp >= 9) {
             // -------------------------------------------------- MMA issuers ---
-            constexpr uint32_t ID_S = idesc_f16(128, 128, false, false, false);
-            constexpr uint32_t ID_DP = idesc_f16(128, 128, true, false, false);
+            // Row warpgroup w owns key columns [64w, 64w+64) of every item; its
+            // S/dP columns are issued by their own warp (9 for w = 0, 11 for
+            // w = 1) as soon as that group has loaded its previous ones.  Warp
+            // 10 issues dQ += dS K': per item the K steps of group 0's keys,
+            // then group 1's, always in that order (a fixed accumulation
+            // order).
+            constexpr uint32_t ID_S = idesc_f16(128, 64, false, false, false);
+            constexpr uint32_t ID_DP = idesc_f16(128, 64, true, false, false);
             constexpr uint32_t ID_DQ = idesc_f16(128, TL::NPV, false, false, true);
             constexpr uint32_t TSTEP = TL::BYTES >> 4;
+            constexpr uint32_t RHALF = (64 * TL::SWB) >> 4;   // rows 64.. of a K'/V tile
             const uint32_t sbase = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
             const uint32_t tb = __shfl_sync(0xffffffffu, tbase, 0);
             bool ok = true;
             int gi = 0, kt = 0;
-            if (warp == 9) {
+            if (warp != 10) {
+                const int wg = warp == 9 ? 0 : 1;
                 const uint64_t dQ0 = desc_kmajor_base<D>(sbase + C::OFF_Q);
                 const uint64_t dO0 = desc_kmajor_base<D>(sbase + C::OFF_DO);
-                const uint64_t dK0 = desc_kmajor_base<D>(sbase + C::OFF_K);
-                const uint64_t dV0 = desc_kmajor_base<D>(sbase + C::OFF_V);
+                const uint64_t dK0 = desc_kmajor_base<D>(sbase + C::OFF_K) + wg * RHALF;
+                const uint64_t dV0 = desc_kmajor_base<D>(sbase + C::OFF_V) + wg * RHALF;
+                const uint32_t col_s = tb + C::COL_S + 64 * wg, col_dp = tb + C::COL_DP + 64 * wg;
                 for (int k = 0; ok; ++k) {
                     const int u = snake_unit(k, cta, P);
                     if (u >= NU)
@@ -591,7 +603,8 @@ __global__ void __launch_bounds__(384, 1)
                         const int st = kt % ST;
                         if ((g == 0 && !mbar_wait_warp(smem_u32(&bar_kv_full[st]), (kt / ST) & 1, wc)) ||
                             (jk == w.lo && !mbar_wait_warp(smem_u32(&bar_q_full[g]), k & 1, wc)) ||
-                            (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_s_empty), (gi - 1) & 1, wc))) {
+                            (gi >= 1 &&
+                             !mbar_wait_warp(smem_u32(&bar_s_empty[wg]), (gi - 1) & 1, wc))) {
                             ok = false;
                             break;
                         }
@@ -601,13 +614,13 @@ __global__ void __launch_bounds__(384, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_f16_ss(tb + C::COL_S, qd + kmajor_off<D>(kk),
-                                           kd + kmajor_off<D>(kk), ID_S, kk > 0 ? 1u : 0u);
+                                mma_f16_ss(col_s, qd + kmajor_off<D>(kk), kd + kmajor_off<D>(kk),
+                                           ID_S, kk > 0 ? 1u : 0u);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_f16_ss(tb + C::COL_DP, od + kmajor_off<D>(kk),
-                                           vd + kmajor_off<D>(kk), ID_DP, kk > 0 ? 1u : 0u);
-                            mma_commit(smem_u32(&bar_s_full));
+                                mma_f16_ss(col_dp, od + kmajor_off<D>(kk), vd + kmajor_off<D>(kk),
+                                           ID_DP, kk > 0 ? 1u : 0u);
+                            mma_commit(smem_u32(&bar_s_full[wg]));
                             if (jk == w.m)   // last use of head g's Q'/dO in this unit
                                 mma_commit(smem_u32(&bar_q_empty[g]));
                         }
@@ -624,33 +637,38 @@ __global__ void __launch_bounds__(384, 1)
                         break;
                     const DqUnit w = dq_unit<VAR>(u, GC, p);
                     const int nitems = (w.m - w.lo + 1) * GC;
-                    for (int it = 0; it < nitems; ++it, ++gi) {
+                    for (int it = 0; it < nitems && ok; ++it, ++gi) {
                         const int jk = w.lo + it / GC, g = it % GC;
                         const int st = kt % ST;
-                        if (!mbar_wait_warp(smem_u32(&bar_ds_full), gi & 1, wc) ||
-                            (it == 0 && k >= 1 &&
-                             !mbar_wait_warp(smem_u32(&bar_dq_free), (k - 1) & 1, wc))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
                         const uint64_t km = dKm0 + st * TSTEP;
-                        const uint32_t first = (jk > w.lo) ? 1u : 0u;
-                        if (elect_one()) {
+                        for (int wg = 0; wg < 2; ++wg) {
+                            if (!mbar_wait_warp(smem_u32(&bar_ds_full[wg]), gi & 1, wc) ||
+                                (it == 0 && wg == 0 && k >= 1 &&
+                                 !mbar_wait_warp(smem_u32(&bar_dq_free), (k - 1) & 1, wc))) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t first = (jk > w.lo || wg > 0) ? 1u : 0u;
+                            if (elect_one()) {
 #pragma unroll
-                            for (int nc = 0; nc < D / TL::NPV; ++nc)
+                                for (int nc = 0; nc < D / TL::NPV; ++nc)
 #pragma unroll
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_f16_ts(tb + C::COL_DQ + g * D + nc * TL::NPV,
-                                               tb + C::COL_DS + 8 * kk, km + mnmajor_off<D>(nc, kk),
-                                               ID_DQ, kk > 0 ? 1u : first);
-                            mma_commit(smem_u32(&bar_ds_empty));
-                            if (g == GC - 1)
-                                mma_commit(smem_u32(&bar_kv_empty[st]));
-                            if (it == nitems - 1)
-                                mma_commit(smem_u32(&bar_dq_done));
+                                    for (int kq = 0; kq < 4; ++kq)
+                                        mma_f16_ts(tb + C::COL_DQ + g * D + nc * TL::NPV,
+                                                   tb + C::COL_DS + 32 * wg + 8 * kq,
+                                                   km + mnmajor_off<D>(nc, 4 * wg + kq), ID_DQ,
+                                                   kq > 0 ? 1u : first);
+                                mma_commit(smem_u32(&bar_ds_empty[wg]));
+                                if (wg == 1) {
+                                    if (g == GC - 1)
+                                        mma_commit(smem_u32(&bar_kv_empty[st]));
+                                    if (it == nitems - 1)
+                                        mma_commit(smem_u32(&bar_dq_done));
+                                }
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
                         if (g == GC - 1)
                             ++kt;
                     }
@@ -668,6 +686,7 @@ __global__ void __launch_bounds__(384, 1)
     // ---------------------------------------------------- row warpgroups ---
     regs_claim<216>();
     const int w = warp >> 2;                // key-column half of the score tile
+    static_assert(kDqStoreRows == 32, "a warp stores the rows of its TMEM lane quarter");
     const int r = threadIdx.x & 127;        // query row == TMEM lane
     const uint32_t lane_base = tmem_addr(tbase, (warp & 3) * 32, 0);
     float maxds = 0.f;
@@ -736,32 +755,27 @@ __global__ void __launch_bounds__(384, 1)
                         store_direct(g);
                         continue;
                     }
-                    // the staging block is free once this group's previous
-                    // store has read it
+                    // Each warp sends its own 32 rows out with its own TMA
+                    // store (the dq map's box is kDqStoreRows rows); its rows
+                    // of the staging block are free once the warp's previous
+                    // store has read them.
                     if (nepi >= 1) {
-                        if (warp == 4 * w && lane == 0) {
+                        if (lane == 0)
                             bulk_wait_read0();
-                            mbar_arrive(smem_u32(&bar_stg_free[w]));
-                        }
-                        if (!mbar_wait_warp(smem_u32(&bar_stg_free[w]), (nepi - 1) & 1, wc))
-                            return false;
+                        __syncwarp();
                     }
                     epilogue_inverse_rope_stage<D>(lane_base + C::COL_DQ + g * D, p.scale, sn, cs,
                                                    stage, r);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&bar_stg_full[w]));
-                    if (warp == 4 * w) {
-                        if (!mbar_wait_warp(smem_u32(&bar_stg_full[w]), nepi & 1, wc))
-                            return false;
-                        if (lane == 0) {
-                            tma_store_4d(&tmDQ, smem_u32(stage), 0, pend.h0 + g,
-                                         pend.sq.base + pend.m * kRows, pend.sq.bc);
-                            bulk_commit();
-                        }
-                        __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&tmDQ, smem_u32(stage + (warp & 3) * kDqStoreRows * TL::SWB),
+                                     0, pend.h0 + g,
+                                     pend.sq.base + pend.m * kRows + (warp & 3) * kDqStoreRows,
+                                     pend.sq.bc);
+                        bulk_commit();
                     }
+                    __syncwarp();
                     ++nepi;
                 } else {
                     store_direct(g);
@@ -790,7 +804,7 @@ __global__ void __launch_bounds__(384, 1)
         const int nitems = (un.m - un.lo + 1) * GC;
         for (int it = 0; it < nitems; ++it, ++gi) {
             const int jk = un.lo + it / GC, g = it % GC;
-            if (!mbar_wait_warp(smem_u32(&bar_s_full), gi & 1, wc)) {
+            if (!mbar_wait_warp(smem_u32(&bar_s_full[w]), gi & 1, wc)) {
                 ok = false;
                 break;
             }
@@ -808,7 +822,7 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_u32(&bar_s_empty));
+                mbar_arrive(smem_u32(&bar_s_empty[w]));
 
             // the per-head row scalars, selected without dynamic indexing
             float lg = l2[0], dg = dd[0];
@@ -855,7 +869,7 @@ __global__ void __launch_bounds__(384, 1)
                         dk[16 * h + e / 2] = pack_f16x2(d0, d1);
                     }
             }
-            if (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_ds_empty), (gi - 1) & 1, wc)) {
+            if (gi >= 1 && !mbar_wait_warp(smem_u32(&bar_ds_empty[w]), (gi - 1) & 1, wc)) {
                 ok = false;
                 break;
             }
@@ -865,7 +879,7 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_u32(&bar_ds_full));
+                mbar_arrive(smem_u32(&bar_ds_full[w]));
             if (it == 0 && pend_k >= 0 && !epilogue()) {
                 ok = false;
                 break;
@@ -879,8 +893,8 @@ __global__ void __launch_bounds__(384, 1)
     if (ok && pend_k >= 0)
         ok = epilogue();
     if constexpr (C::STAGE) {
-        if (warp == 4 * w && lane == 0)
-            bulk_wait0();
+        if (lane == 0)
+            bulk_wait0();   // this warp's dq rows have left shared memory
     }
     if (maxds > kFp16Max)
         atomicOr(p.status, kDevRange);

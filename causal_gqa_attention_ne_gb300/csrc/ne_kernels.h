@@ -24,7 +24,9 @@ cudaError_t launch_bwd_pre(int d, const AttnParams &p, const void *q, void *qrot
                            void *krot, cudaStream_t stream);
 
 // Backward dQ (query-tile major, recomputes S and dP); `dq` is the tensor
-// map of the output (same layout as q), used by its TMA store (d <= 64).
+// map of the output (same layout as q) with a box of kDqStoreRows rows, used
+// by its TMA stores (d <= 64): each row warp stores its own rows of a head.
+constexpr int kDqStoreRows = 32;
 cudaError_t launch_bwd_dq(int d, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                           const CUtensorMap &dO, const CUtensorMap &dq, const AttnParams &p,
                           cudaStream_t stream);
