@@ -931,11 +931,18 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t *stage = smem + C::OFF_O + wg * TL::BLOCK;
     uint32_t nepi = 0;       // O stores this group has issued
     float mr0 = 0.f, mr1 = 0.f, lr0 = 0.f, lr1 = 0.f;   // running max (log2 units) / sum per slot
-    // Writes O_slot / l of head h (rows of this thread) and its lse.  The
-    // caller folds 1 / l into the scales: O = O_a * fa (+ O_b * fb with a
-    // second accumulator, merge), on packed fp32 pairs.
+    // lse of head h for this thread's row (ln units), rows past the sequence
+    // skipped
+    auto store_lse = [&](const FwdUnit &un, int h, float lse2) {
+        const int t = un.m * kRows + r;
+        if (t < un.sq.len)
+            p.lse[(static_cast<size_t>(un.sq.bc) * p.Hq + h) * p.T + un.sq.base + t] = lse2 * kLn2;
+    };
+    // Writes O_slot / l of head h (rows of this thread).  The caller folds
+    // 1 / l into the scales: O = O_a * fa (+ O_b * fb with a second
+    // accumulator, merge), on packed fp32 pairs.
     auto store_head = [&](const FwdUnit &un, int h, uint32_t oa, bool merge, uint32_t ob, float fa,
-                          float fb, float lse2) -> bool {
+                          float fb) -> bool {
         const int t = un.m * kRows + r;
         // columns c .. c + 31 of this thread's row, scaled, as bf16 pairs
         auto chunk = [&](int c, uint32_t (&pk)[16]) {
@@ -1018,8 +1025,6 @@ __global__ void __launch_bounds__(512, 1)
         } else {
             store_direct();
         }
-        if (t < un.sq.len)
-            p.lse[(static_cast<size_t>(un.sq.bc) * p.Hq + h) * p.T + un.sq.base + t] = lse2 * kLn2;
         return true;
     };
     for (int k = 0; ok; ++k) {
@@ -1179,37 +1184,49 @@ __global__ void __launch_bounds__(512, 1)
             break;
 
         // ---- end of the unit: O / l and lse of this group's heads ----
+        // The split head (odd GC) is merged and stored by group k % 2, so the
+        // two groups' epilogues carry the same work over consecutive units.
+        // What needs only this group's running max and sum comes first, while
+        // the unit's last PV may still run: the other group's half of the
+        // split head is handed over, and the lse of each whole head is written.
+        const int ss = wg == 0 ? C::NSL - 1 : 0;            // this group's split slot
+        const int og = 1 - wg, oss = og == 0 ? C::NSL - 1 : 0;
+        const bool merging = !C::SPLIT || (k & 1) == wg;
+        float inv_l[C::NSL];
+#pragma unroll
+        for (int slot = 0; slot < C::NSL; ++slot) {
+            const float m_s = slot ? mr1 : mr0, l_s = slot ? lr1 : lr0;
+            inv_l[slot] = 1.f;
+            if (C::SPLIT && slot == ss) {
+                if (!merging) {
+                    split_ml[r] = m_s;
+                    split_ml[kRows + r] = l_s;
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&bar_split));
+                }
+            } else {
+                inv_l[slot] = 1.f / l_s;
+                store_lse(un, un.h0 + ((wg * GC) >> 1) + slot, m_s + __log2f(l_s));
+            }
+        }
         // every PV of the unit has completed once PV(n - 1) has
         if (!mbar_wait_warp(smem_u32(&bar_p_free[wg][(n - 1) & 1u]), ((n - 1) >> 1) & 1, wc)) {
             ok = false;
             break;
         }
         tc_fence_after();
-        // The split head (odd GC) is merged and stored by group k % 2, so the
-        // two groups' epilogues carry the same work over consecutive units;
-        // the merging group stores its own head first, the other group
-        // publishes its half first.
-        const int ss = wg == 0 ? C::NSL - 1 : 0;            // this group's split slot
-        const int og = 1 - wg, oss = og == 0 ? C::NSL - 1 : 0;
-        const bool merging = !C::SPLIT || (k & 1) == wg;
+        // the merging group stores its own head first
         for (int i = 0; i < C::NSL && ok; ++i) {
             int slot = i;
             if constexpr (C::SPLIT && C::NSL == 2)
                 slot = (merging == (i == 1)) ? ss : 1 - ss;
-            const int h = un.h0 + ((wg * GC) >> 1) + slot;
-            const float m_s = slot ? mr1 : mr0, l_s = slot ? lr1 : lr0;
-            const uint32_t oa = lane_base + C::COL_O + (wg * C::NSL + slot) * D;
             const bool split = C::SPLIT && slot == ss;
-            if (split && !merging) {
-                // hand this half's max and sum to the merging group
-                split_ml[r] = m_s;
-                split_ml[kRows + r] = l_s;
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&bar_split));
+            if (split && !merging)
                 continue;
-            }
-            float sa = 1.f, sb = 0.f, l_tot = l_s, m_tot = m_s;
+            const int h = un.h0 + ((wg * GC) >> 1) + slot;
+            const uint32_t oa = lane_base + C::COL_O + (wg * C::NSL + slot) * D;
+            float fa = slot ? inv_l[1 % C::NSL] : inv_l[0], fb = 0.f;
             uint32_t ob = 0u;
             if (split) {
                 if (!mbar_wait_warp(smem_u32(&bar_split), k & 1, wc)) {
@@ -1217,15 +1234,19 @@ __global__ void __launch_bounds__(512, 1)
                     break;
                 }
                 tc_fence_after();
+                const float m_s = slot ? mr1 : mr0, l_s = slot ? lr1 : lr0;
                 const float m1 = split_ml[r], l1 = split_ml[kRows + r];
-                m_tot = fmaxf(m_s, m1);
-                sa = ex2_approx(m_s - m_tot);
-                sb = ex2_approx(m1 - m_tot);   // 0 when that half saw no key
-                l_tot = fmaf(l_s, sa, l1 * sb);
+                const float m_tot = fmaxf(m_s, m1);
+                const float sa = ex2_approx(m_s - m_tot);
+                const float sb = ex2_approx(m1 - m_tot);   // 0 when that half saw no key
+                const float l_tot = fmaf(l_s, sa, l1 * sb);
+                const float il = 1.f / l_tot;
+                fa = sa * il;
+                fb = sb * il;
                 ob = lane_base + C::COL_O + (og * C::NSL + oss) * D;
+                store_lse(un, h, m_tot + __log2f(l_tot));
             }
-            const float inv_l = 1.f / l_tot;
-            if (!store_head(un, h, oa, split, ob, sa * inv_l, sb * inv_l, m_tot + __log2f(l_tot))) {
+            if (!store_head(un, h, oa, split, ob, fa, fb)) {
                 ok = false;
                 break;
             }
