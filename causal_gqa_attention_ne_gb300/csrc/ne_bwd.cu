@@ -1288,7 +1288,7 @@ __global__ void __launch_bounds__(512, 1)
                     fetch(it + 1, nl, nd);
                 // The stage's previous item is finished once the TMA has refilled
                 // it, so its lse/D slots can be overwritten.
-                if (!mbar_wait_warp(smem_u32(&bar_q_full[st]), su & 1, wc)) {
+                if (!mbar_wait_warp_idle(smem_u32(&bar_q_full[st]), su & 1, wc)) {
                     ok = false;
                     break;
                 }

@@ -702,7 +702,7 @@ __global__ void __launch_bounds__(512, 1)
                         ++kt;
                     if (!isq && !(jk == w.m && w.h0 == w.j * p.G))
                         continue;   // this K' tile is stored by its diagonal unit
-                    if (!mbar_wait_warp(smem_u32(&bar_sv[nsv % 16]), (nsv / 16) & 1, wc)) {
+                    if (!mbar_wait_warp_idle(smem_u32(&bar_sv[nsv % 16]), (nsv / 16) & 1, wc)) {
                         ok = false;
                         break;
                     }

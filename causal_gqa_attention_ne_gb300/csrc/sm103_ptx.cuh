@@ -131,6 +131,49 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
     return __all_sync(0xffffffffu, ok);
 }
 
+// The same for a warp off the critical path: between polls the thread is
+// suspended until the phase completes or for at most kIdleHintNs, so it does
+// not take issue slots from the computing warps of its sub-partition (waking
+// costs latency, which such a warp can afford).
+constexpr uint32_t kIdleHintNs = 100000;
+
+__device__ __forceinline__ uint32_t mbar_test_idle(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kIdleHintNs)
+        : "memory");
+    return ok;
+}
+
+__device__ __forceinline__ bool mbar_wait_warp_idle(uint32_t bar, uint32_t parity,
+                                                    const WaitCtl &w)
+{
+    bool ok = true;
+    if (!mbar_test_idle(bar, parity)) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            if (mbar_test_idle(bar, parity))
+                break;
+            if (*w.abort) {
+                ok = false;
+                break;
+            }
+            if (global_timer_ns() - t0 > w.limit_ns) {
+                *w.abort = 1u;
+                atomicOr(w.status, kDevTimeout);
+                ok = false;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 // One lane of a fully active warp (the lowest); all 32 lanes must call it.
 // Warp-wide issue loops keep descriptor math warp-uniform, and only the
 // elected lane issues the tcgen05 instruction.
